@@ -1,0 +1,195 @@
+"""fp64 CPU oracle for exact scaled dot-product attention.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+legs of ``bench.py`` (``cpu_baseline`` and ``--impl reference``) may import or
+run anything in ``oracle/``. The CUDA library never links it and the Python
+binding never imports it; it shares no code, header, table or helper with the
+GPU path.
+
+What it computes is the plain definition, materialised, in float64:
+
+* Forward -- the SDPA tutorial page ("(Beta) Implementing High-Performance
+  Transformers with Scaled Dot Product Attention", section "Overview") defines
+  the op as the scaled dot-product attention of "Attention Is All You Need":
+  ``O = softmax(scale * Q K^T [+ causal mask]) V``; the same page, section
+  "Causal Self Attention", passes ``is_causal`` to it.  The FlashAttention
+  news article (QbitAI repost, section "FlashAttention") states that the tiled
+  algorithm is *exact*, so the un-tiled definition is the oracle.
+* The per-row log-sum-exp ``LSE_i = log sum_j exp(S_ij)`` (natural log) is
+  what an IO-aware forward saves for the recomputing backward (same article,
+  same section: attention is recomputed in the backward pass). The pages do
+  not print it; this is the plainest reading of "recompute".
+* Backward -- calculus on the definition (the pages only say the backward
+  recomputes attention): with P the probabilities and dO the output gradient,
+  ``dV = P^T dO``, ``dP = dO V^T``, ``D_i = sum_j P_ij dP_ij``,
+  ``dS = P * (dP - D)``, ``dQ = scale dS K``, ``dK = scale dS^T Q``.
+
+Readings taken where the pages are silent (each listed in the design notes):
+causal masking is top-left aligned (key j is visible to query i iff j <= i);
+``scale`` is always passed explicitly; LSE is natural-log, fp32 on the GPU,
+shape ``[B, H, Lq]`` dense and ``[H, total]`` packed; a unit with Lq = 0
+yields empty outputs; Lk = 0 with Lq > 0 is an error.
+
+Layouts: dense tensors are ``[..., L, d]`` (any leading batch/head dims, the
+tutorial's ``[B, H, L, d]`` and its ``[2, 3, 8]`` example both fit); packed
+variable-length tensors (the tutorial's NestedTensor section) are
+``[total, H, d]`` with ``cu_seqlens`` of length ``nseq + 1``; the same
+offsets serve queries and keys (self-attention).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "attention_probs",
+    "attn_fwd_unit",
+    "attn_bwd_unit",
+    "attn_fwd_ref",
+    "attn_bwd_ref",
+    "attn_fwd_rows",
+]
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def _scores(q: np.ndarray, k: np.ndarray, scale: float, is_causal: bool) -> np.ndarray:
+    """S = scale * Q K^T with masked entries set to -inf (SDPA tutorial, "Overview";
+    causal mask: "Causal Self Attention")."""
+    s = float(scale) * (q @ k.T)
+    if is_causal:
+        lq, lk = s.shape
+        i = np.arange(lq)[:, None]
+        j = np.arange(lk)[None, :]
+        s = np.where(j > i, -np.inf, s)
+    return s
+
+
+def attention_probs(q, k, scale: float, is_causal: bool = False):
+    """P = softmax_j(S_ij) and LSE_i for one (batch, head) unit.
+
+    ``q``: [Lq, d], ``k``: [Lk, d]. Returns ``(P [Lq, Lk], LSE [Lq])`` in float64.
+    The row maximum is subtracted before exponentiating (a rounding measure
+    only; softmax is shift invariant).
+    """
+    q, k = _f64(q), _f64(k)
+    lq, lk = q.shape[0], k.shape[0]
+    if lq == 0:
+        return np.zeros((0, lk)), np.zeros((0,))
+    if lk == 0:
+        raise ValueError("softmax over an empty key set is undefined (Lk = 0 with Lq > 0)")
+    s = _scores(q, k, scale, is_causal)
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    z = np.sum(e, axis=1, keepdims=True)
+    p = e / z
+    lse = (m + np.log(z))[:, 0]
+    return p, lse
+
+
+def attn_fwd_unit(q, k, v, scale: float, is_causal: bool = False):
+    """O = P V and LSE for one unit. ``v``: [Lk, dv]. Returns (O [Lq, dv], LSE [Lq])."""
+    v = _f64(v)
+    p, lse = attention_probs(q, k, scale, is_causal)
+    return p @ v, lse
+
+
+def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False):
+    """Gradients of sum(dO * O) w.r.t. Q, K, V for one unit (chain rule through
+    the softmax; the pages only say the backward recomputes attention)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    if q.shape[0] == 0:
+        return np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    p, _ = attention_probs(q, k, scale, is_causal)
+    dv = p.T @ do
+    dp = do @ v.T
+    dsum = np.sum(p * dp, axis=1, keepdims=True)
+    ds = p * (dp - dsum)
+    dq = float(scale) * (ds @ k)
+    dk = float(scale) * (ds.T @ q)
+    return dq, dk, dv
+
+
+def _units_dense(x: np.ndarray) -> np.ndarray:
+    return x.reshape((-1,) + x.shape[-2:])
+
+
+def _check_cu(cu_seqlens, total: int) -> np.ndarray:
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    if cu.ndim != 1 or cu.size < 1 or cu[0] != 0 or np.any(np.diff(cu) < 0) or cu[-1] != total:
+        raise ValueError("cu_seqlens must start at 0, be non-decreasing and end at the packed length")
+    return cu
+
+
+def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None):
+    """Forward over a whole batch.
+
+    Dense: ``q`` [..., Lq, d], ``k``/``v`` [..., Lk, d] -> ``O`` [..., Lq, d],
+    ``LSE`` [..., Lq]. Packed (``cu_seqlens`` given): ``q``/``k``/``v``
+    [total, H, d] -> ``O`` [total, H, d], ``LSE`` [H, total]; sequence s owns
+    rows ``cu_seqlens[s] : cu_seqlens[s+1]`` of queries and keys (the
+    tutorial's NestedTensor batches without padding).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if cu_seqlens is None:
+        lead = q.shape[:-2]
+        qu, ku, vu = _units_dense(q), _units_dense(k), _units_dense(v)
+        o = np.empty(qu.shape[:2] + (vu.shape[-1],))
+        lse = np.empty(qu.shape[:2])
+        for u in range(qu.shape[0]):
+            o[u], lse[u] = attn_fwd_unit(qu[u], ku[u], vu[u], scale, is_causal)
+        return o.reshape(lead + o.shape[1:]), lse.reshape(lead + lse.shape[1:])
+    total, nh, _ = q.shape
+    cu = _check_cu(cu_seqlens, total)
+    o = np.zeros((total, nh, v.shape[-1]))
+    lse = np.zeros((nh, total))
+    for s in range(cu.size - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b == a:
+            continue
+        for h in range(nh):
+            o[a:b, h], lse[h, a:b] = attn_fwd_unit(q[a:b, h], k[a:b, h], v[a:b, h], scale, is_causal)
+    return o, lse
+
+
+def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=None):
+    """Backward over a whole batch; same layouts as :func:`attn_fwd_ref`.
+    Returns ``(dQ, dK, dV)`` in float64."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    if cu_seqlens is None:
+        qu, ku, vu, du = (_units_dense(x) for x in (q, k, v, do))
+        dq, dk, dv = np.empty_like(qu), np.empty_like(ku), np.empty_like(vu)
+        for u in range(qu.shape[0]):
+            dq[u], dk[u], dv[u] = attn_bwd_unit(qu[u], ku[u], vu[u], du[u], scale, is_causal)
+        return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
+    total, nh, _ = q.shape
+    cu = _check_cu(cu_seqlens, total)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s in range(cu.size - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b == a:
+            continue
+        for h in range(nh):
+            dq[a:b, h], dk[a:b, h], dv[a:b, h] = attn_bwd_unit(
+                q[a:b, h], k[a:b, h], v[a:b, h], do[a:b, h], scale, is_causal)
+    return dq, dk, dv
+
+
+def attn_fwd_rows(q_rows, k, v, row_index, scale: float, is_causal: bool = False):
+    """Forward for selected query rows of one unit (for sampled checks at full size).
+
+    ``q_rows`` [n, d] are the queries at absolute positions ``row_index`` [n]
+    within a unit whose keys/values are ``k`` [Lk, d], ``v`` [Lk, dv]. Row i
+    sees keys j <= row_index[i] when causal. Returns (O [n, dv], LSE [n]).
+    """
+    q_rows, k, v = _f64(q_rows), _f64(k), _f64(v)
+    rows = np.asarray(row_index, dtype=np.int64)
+    s = float(scale) * (q_rows @ k.T)
+    if is_causal:
+        j = np.arange(k.shape[0])[None, :]
+        s = np.where(j > rows[:, None], -np.inf, s)
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    z = np.sum(e, axis=1, keepdims=True)
+    return (e / z) @ v, (m + np.log(z))[:, 0]

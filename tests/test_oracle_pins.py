@@ -1,0 +1,301 @@
+"""Pins for the fp64 oracle: checks against what the mathematics fixes.
+
+None of these retypes the oracle's formula. They compare it with a
+brute-force twin that takes another road (explicit loops, no max shift, full
+softmax Jacobian), with central finite differences, with closed forms and
+invariants of the definition (SDPA tutorial page, section "Overview";
+causal: section "Causal Self Attention"; packed batches: section
+"NestedTensor and Dense tensor support"), and with the library's own math
+path. The last block plants mistakes in copies of the oracle and checks that
+the pins catch each one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import (attention_probs, attn_bwd_ref, attn_bwd_unit, attn_fwd_ref,
+                    attn_fwd_rows, attn_fwd_unit, bwd_bruteforce, fwd_bruteforce)
+from exact_attention_softmax_gb300 import workloads as wl
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def rnd(*shape, seed=0):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------- brute force
+
+@pytest.mark.parametrize("lq,lk,d,causal", [
+    (1, 1, 1, False), (3, 3, 8, False), (3, 3, 8, True), (2, 4, 3, False),
+    (4, 2, 3, True), (4, 4, 5, True), (3, 1, 2, True)])
+def test_fwd_matches_bruteforce(lq, lk, d, causal):
+    q, k, v = rnd(lq, d, seed=1), rnd(lk, d, seed=2), rnd(lk, d + 1, seed=3)
+    scale = 0.7
+    o, lse = attn_fwd_unit(q, k, v, scale, causal)
+    ob, lseb = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), scale, causal)
+    np.testing.assert_allclose(o, np.array(ob), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, np.array(lseb), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("lq,lk,d,causal", [
+    (3, 3, 8, False), (3, 3, 8, True), (2, 4, 3, False), (4, 3, 2, True), (1, 3, 2, False)])
+def test_bwd_matches_bruteforce_jacobian(lq, lk, d, causal):
+    q, k, v, do = rnd(lq, d, seed=4), rnd(lk, d, seed=5), rnd(lk, d, seed=6), rnd(lq, d, seed=7)
+    scale = 1 / math.sqrt(d)
+    got = attn_bwd_unit(q, k, v, do, scale, causal)
+    ref = bwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), do.tolist(), scale, causal)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, np.array(r), rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------- finite differences
+
+def _fd_check(bwd, causal, seed=0, h=1e-6):
+    """Central differences of L = sum(dO * O) against the analytic gradients on
+    the tiny workload's shape (B=2, H=1, L=3, d=8)."""
+    shp = (2, 1, 3, 8)
+    q, k, v, do = (rnd(*shp, seed=seed + i) for i in range(4))
+    scale = 1 / math.sqrt(8)
+
+    def loss(q_, k_, v_):
+        o, _ = attn_fwd_ref(q_, k_, v_, scale, causal)
+        return float(np.sum(do * o))
+
+    grads = bwd(q, k, v, do, scale, causal)
+    worst = 0.0
+    for which, g in enumerate(grads):
+        args = [q, k, v]
+        num = np.zeros_like(args[which])
+        it = np.nditer(args[which], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            num[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        err = np.linalg.norm(num - g) / max(np.linalg.norm(num), 1e-30)
+        worst = max(worst, err)
+    return worst
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_finite_differences(causal):
+    assert _fd_check(attn_bwd_ref, causal) <= 1e-7
+
+
+# ---------------------------------------------------------- invariants / forms
+
+def test_probability_rows_sum_to_one():
+    for causal in (False, True):
+        p, _ = attention_probs(rnd(7, 5, seed=1), rnd(9, 5, seed=2), 0.4, causal)
+        np.testing.assert_allclose(p.sum(1), 1.0, rtol=0, atol=1e-14)
+        assert np.all(p >= 0)
+        if causal:
+            assert np.all(np.triu(p, 1) == 0)
+
+
+def test_single_key_gives_its_value_and_lse():
+    q, k, v = rnd(5, 4, seed=1), rnd(1, 4, seed=2), rnd(1, 4, seed=3)
+    o, lse = attn_fwd_unit(q, k, v, 0.3, False)
+    np.testing.assert_allclose(o, np.repeat(v, 5, 0), atol=1e-15)
+    np.testing.assert_allclose(lse, 0.3 * (q @ k[0]), atol=1e-14)
+
+
+def test_constant_values_give_constant_output():
+    v = np.tile(rnd(1, 6, seed=3), (8, 1))
+    for causal in (False, True):
+        o, _ = attn_fwd_unit(rnd(8, 6, seed=1), rnd(8, 6, seed=2), v, 1.1, causal)
+        np.testing.assert_allclose(o, np.tile(v[:1], (8, 1)), atol=1e-14)
+
+
+def test_causal_first_row_sees_only_first_key():
+    q, k, v = rnd(6, 4, seed=1), rnd(6, 4, seed=2), rnd(6, 4, seed=3)
+    o, lse = attn_fwd_unit(q, k, v, 0.5, True)
+    np.testing.assert_allclose(o[0], v[0], atol=1e-15)
+    assert abs(lse[0] - 0.5 * q[0] @ k[0]) < 1e-14
+
+
+def test_zero_scale_gives_mean_and_log_count():
+    q, k, v = rnd(5, 3, seed=1), rnd(7, 3, seed=2), rnd(7, 3, seed=3)
+    o, lse = attn_fwd_unit(q, k, v, 0.0, False)
+    np.testing.assert_allclose(o, np.tile(v.mean(0), (5, 1)), atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(7), atol=1e-14)
+    o, lse = attn_fwd_unit(q, k, v, 0.0, True)
+    for i in range(5):
+        np.testing.assert_allclose(o[i], v[: i + 1].mean(0), atol=1e-14)
+        assert abs(lse[i] - math.log(i + 1)) < 1e-14
+
+
+def test_two_keys_closed_form():
+    q, k, v = rnd(4, 3, seed=1), rnd(2, 3, seed=2), rnd(2, 5, seed=3)
+    sc = 0.8
+    o, lse = attn_fwd_unit(q, k, v, sc, False)
+    s = sc * q @ k.T
+    sig = 1 / (1 + np.exp(-(s[:, 0] - s[:, 1])))
+    np.testing.assert_allclose(o, sig[:, None] * v[0] + (1 - sig)[:, None] * v[1], atol=1e-14)
+    np.testing.assert_allclose(lse, np.logaddexp(s[:, 0], s[:, 1]), atol=1e-14)
+
+
+def test_key_shift_invariance():
+    q, k, v = rnd(6, 4, seed=1), rnd(6, 4, seed=2), rnd(6, 4, seed=3)
+    u = rnd(4, seed=9)
+    for causal in (False, True):
+        o, lse = attn_fwd_unit(q, k, v, 0.6, causal)
+        o2, lse2 = attn_fwd_unit(q, k + u, v, 0.6, causal)
+        np.testing.assert_allclose(o2, o, atol=1e-13)
+        np.testing.assert_allclose(lse2, lse + 0.6 * q @ u, atol=1e-13)
+
+
+def test_key_value_permutation_invariance():
+    q, k, v = rnd(5, 4, seed=1), rnd(9, 4, seed=2), rnd(9, 3, seed=3)
+    perm = np.random.default_rng(0).permutation(9)
+    o, lse = attn_fwd_unit(q, k, v, 0.5, False)
+    o2, lse2 = attn_fwd_unit(q, k[perm], v[perm], 0.5, False)
+    np.testing.assert_allclose(o2, o, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse, atol=1e-14)
+
+
+def test_packed_equals_dense_per_sequence():
+    lens = [3, 1, 5, 0, 2]
+    H, d = 2, 4
+    x = wl.varlen_inputs(lens, H, d, "f32", "normal", seed=3)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    cu = x["cu_seqlens"].numpy()
+    for causal in (False, True):
+        o, lse = attn_fwd_ref(q, k, v, 0.5, causal, cu)
+        dq, dk, dv = attn_bwd_ref(q, k, v, do, 0.5, causal, cu)
+        assert lse.shape == (H, sum(lens))
+        for s in range(len(lens)):
+            a, b = cu[s], cu[s + 1]
+            for h in range(H):
+                od, ld = attn_fwd_unit(q[a:b, h], k[a:b, h], v[a:b, h], 0.5, causal)
+                np.testing.assert_array_equal(o[a:b, h], od)
+                np.testing.assert_array_equal(lse[h, a:b], ld)
+                g = attn_bwd_unit(q[a:b, h], k[a:b, h], v[a:b, h], do[a:b, h], 0.5, causal)
+                np.testing.assert_array_equal(dq[a:b, h], g[0])
+                np.testing.assert_array_equal(dk[a:b, h], g[1])
+                np.testing.assert_array_equal(dv[a:b, h], g[2])
+
+
+def test_rows_helper_matches_full_unit():
+    q, k, v = rnd(10, 4, seed=1), rnd(10, 4, seed=2), rnd(10, 4, seed=3)
+    rows = np.array([0, 3, 9])
+    for causal in (False, True):
+        o, lse = attn_fwd_unit(q, k, v, 0.5, causal)
+        o2, lse2 = attn_fwd_rows(q[rows], k, v, rows, 0.5, causal)
+        np.testing.assert_allclose(o2, o[rows], atol=1e-14)
+        np.testing.assert_allclose(lse2, lse[rows], atol=1e-14)
+
+
+def test_backward_invariants():
+    q, k, v, do = rnd(6, 4, seed=1), rnd(8, 4, seed=2), rnd(8, 4, seed=3), rnd(6, 4, seed=4)
+    for causal in (False, True):
+        dq, dk, dv = attn_bwd_unit(q, k, v, do, 0.5, causal)
+        # softmax Jacobian rows sum to zero: the key gradients sum to zero
+        np.testing.assert_allclose(dk.sum(0), 0, atol=1e-13)
+        # P rows sum to one: value gradients sum to the summed output gradient
+        np.testing.assert_allclose(dv.sum(0), do.sum(0), atol=1e-13)
+        # a common shift of the keys leaves every gradient unchanged
+        g2 = attn_bwd_unit(q, k + rnd(4, seed=5), v, do, 0.5, causal)
+        for a, b in zip((dq, dk, dv), g2):
+            np.testing.assert_allclose(b, a, atol=1e-12)
+        # linear in dO
+        g3 = attn_bwd_unit(q, k, v, -2.5 * do, 0.5, causal)
+        for a, b in zip((dq, dk, dv), g3):
+            np.testing.assert_allclose(b, -2.5 * a, atol=1e-12)
+
+
+def test_empty_and_invalid_units():
+    o, lse = attn_fwd_unit(np.zeros((0, 4)), rnd(3, 4), rnd(3, 4), 1.0)
+    assert o.shape == (0, 4) and lse.shape == (0,)
+    with pytest.raises(ValueError):
+        attn_fwd_unit(rnd(2, 4), np.zeros((0, 4)), np.zeros((0, 4)), 1.0)
+    with pytest.raises(ValueError):
+        attn_fwd_ref(rnd(4, 1, 2), rnd(4, 1, 2), rnd(4, 1, 2), 1.0, cu_seqlens=[0, 3])
+
+
+# ------------------------------------------------------ library cross-check
+
+@pytest.mark.parametrize("lq,lk,causal", [(5, 5, False), (5, 5, True), (3, 7, True), (7, 3, True)])
+def test_matches_library_math_path(lq, lk, causal):
+    g = torch.Generator().manual_seed(0)
+    q = torch.randn(2, 3, lq, 8, generator=g, dtype=torch.float64, requires_grad=True)
+    k = torch.randn(2, 3, lk, 8, generator=g, dtype=torch.float64, requires_grad=True)
+    v = torch.randn(2, 3, lk, 8, generator=g, dtype=torch.float64, requires_grad=True)
+    do = torch.randn(2, 3, lq, 8, generator=g, dtype=torch.float64)
+    o_t = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=0.35)
+    o_t.backward(do)
+    o, _ = attn_fwd_ref(q.detach().numpy(), k.detach().numpy(), v.detach().numpy(), 0.35, causal)
+    np.testing.assert_allclose(o, o_t.detach().numpy(), atol=1e-12)
+    dq, dk, dv = attn_bwd_ref(q.detach().numpy(), k.detach().numpy(), v.detach().numpy(),
+                              do.numpy(), 0.35, causal)
+    np.testing.assert_allclose(dq, q.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, k.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, v.grad.numpy(), atol=1e-12)
+
+
+# ------------------------------------------------------------ golden fixture
+
+def test_golden_tiny_workload():
+    """Stored oracle outputs for the tiny workload (written by
+    tests/golden/make_golden.py, which calls only the oracle)."""
+    with open(os.path.join(HERE, "golden", "tiny_f32.json")) as f:
+        gold = json.load(f)
+    x = wl.workload_inputs(wl.WORKLOADS["tiny_f32"], seed=gold["seed"])
+    for n in ("q", "k", "v", "do"):
+        np.testing.assert_array_equal(x[n].reshape(-1).numpy(), np.array(gold["inputs"][n], np.float32))
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    o, lse = attn_fwd_ref(q, k, v, gold["scale"], False)
+    dq, dk, dv = attn_bwd_ref(q, k, v, do, gold["scale"], False)
+    for name, val in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(val.reshape(-1), np.array(gold["outputs"][name]), rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------ planted mistakes get caught
+
+def _bwd_mut(kind):
+    def bwd(q, k, v, do, scale, causal):
+        qu, ku, vu, du = (x.reshape((-1,) + x.shape[-2:]) for x in (q, k, v, do))
+        outs = [np.empty_like(qu), np.empty_like(ku), np.empty_like(vu)]
+        for u in range(qu.shape[0]):
+            p, _ = attention_probs(qu[u], ku[u], scale, causal)
+            dv = p.T @ du[u]
+            dp = du[u] @ vu[u].T
+            dsum = np.sum(p * dp, axis=1, keepdims=True)
+            if kind == "D_sign":
+                ds = p * (dp + dsum)
+            elif kind == "D_axis":
+                ds = p * (dp - np.sum(p * dp, axis=0, keepdims=True))
+            else:
+                ds = p * (dp - dsum)
+            dq = scale * (ds @ ku[u])
+            dk = scale * (ds.T @ qu[u])
+            if kind == "no_scale":
+                dq = ds @ ku[u]
+            if kind == "dv_transpose":
+                dv = p @ du[u]  # P used untransposed (square units only)
+            outs[0][u], outs[1][u], outs[2][u] = dq, dk, dv
+        return tuple(o.reshape(x.shape) for o, x in zip(outs, (q, k, v)))
+    return bwd
+
+
+@pytest.mark.parametrize("kind", ["D_sign", "D_axis", "no_scale", "dv_transpose"])
+def test_finite_differences_catch_planted_backward_mistakes(kind):
+    assert _fd_check(_bwd_mut(kind), causal=True) > 1e-3
+
+
+def test_bruteforce_catches_planted_mask_mistake():
+    q, k, v = rnd(4, 3, seed=1), rnd(4, 3, seed=2), rnd(4, 3, seed=3)
+    s = 0.5 * q @ k.T
+    s = np.where(np.arange(4)[None, :] >= np.arange(4)[:, None], -np.inf, s)  # j >= i: wrong
+    s[0, 0] = 0.5 * q[0] @ k[0]
+    p = np.exp(s - s.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    ob, _ = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.5, True)
+    assert np.max(np.abs(p @ v - np.array(ob))) > 1e-3
