@@ -1,0 +1,151 @@
+"""Exact scaled dot-product attention for GB300 (sm_103a): a thin PyTorch
+binding over the C ABI of ``libsdpa_gb300.so`` (``include/sdpa.h``).
+
+The functions here only marshal arguments: they check shapes, allocate
+outputs with PyTorch when the caller passes none, and hand raw device
+pointers plus the current CUDA stream to the library, whose kernels do all of
+the work. Nothing falls back to PyTorch or the CPU; a missing library raises.
+
+Definition (SDPA tutorial page, section "Overview"):
+``O = softmax(scale * Q K^T [+ causal mask]) V`` with the natural-log row
+log-sum-exp ``LSE`` saved for the backward (FlashAttention news article,
+section "FlashAttention": tiled, exact, recomputed in the backward).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+from . import _abi
+from ._abi import SdpaError  # noqa: F401
+
+__all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_device_status",
+           "sdpa_debug_set", "sdpa_last_error", "sdpa_version", "SdpaError"]
+
+
+def _dtype_code(t):
+    import torch
+    codes = {torch.float32: _abi.SDPA_F32, torch.float16: _abi.SDPA_F16, torch.bfloat16: _abi.SDPA_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _vp(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _stream(dev, stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _geometry(q, k, cu_seqlens, max_seqlen):
+    """(B, H, Lq, Lk, d, packed) in the C ABI's convention."""
+    if cu_seqlens is not None:
+        if q.dim() != 3:
+            raise ValueError("packed q must be [total, H, d]")
+        total, H, d = q.shape
+        if max_seqlen is None:
+            raise ValueError("packed batches need max_seqlen (an upper bound on every length)")
+        return cu_seqlens.numel() - 1, H, total, int(max_seqlen), d, True
+    if q.dim() == 3:  # [B, L, d]: one head
+        return q.shape[0], 1, q.shape[1], k.shape[1], q.shape[2], False
+    if q.dim() != 4:
+        raise ValueError("dense q must be [B, H, L, d] (or [B, L, d])")
+    B, H, Lq, d = q.shape
+    return B, H, Lq, k.shape[2], d, False
+
+
+def _check_tensors(ts, dev, dt):
+    for name, t in ts.items():
+        if t is None:
+            continue
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, expected {dev}")
+        if t.dtype != dt:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected {dt}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def sdpa_fwd(q, k, v, o=None, lse=None, *, scale=None, is_causal=False, cu_seqlens=None,
+             max_seqlen=None, stream=None):
+    """Forward pass. Returns ``(O, LSE)``.
+
+    Dense: q [B,H,Lq,d] (or [B,Lq,d]), k/v [B,H,Lk,d]; LSE [B,H,Lq] fp32.
+    Packed: q/k/v [total,H,d], ``cu_seqlens`` int32 [nseq+1] on the device,
+    ``max_seqlen`` >= every length; LSE [H,total] fp32.
+    ``scale`` defaults to 1/sqrt(d).
+    """
+    import torch
+    lib = _abi.load()
+    B, H, Lq, Lk, d, packed = _geometry(q, k, cu_seqlens, max_seqlen)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        shape = (H, Lq) if packed else tuple(q.shape[:-1])
+        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+    _check_tensors({"k": k, "v": v, "o": o}, q.device, q.dtype)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise TypeError("lse must be contiguous float32")
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != q.device):
+        raise TypeError("cu_seqlens must be int32 on the device of q")
+    _abi.check(lib.sdpa_fwd(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), B, H, Lq, Lk, d, float(scale),
+                            int(bool(is_causal)), _vp(cu_seqlens), _dtype_code(q), _stream(q.device, stream)))
+    return o, lse
+
+
+def sdpa_bwd_workspace_size(B, H, Lq, d, dtype_code):
+    """Bytes of device scratch :func:`sdpa_bwd` needs (packed: B=1, Lq=total)."""
+    return int(_abi.load().sdpa_bwd_workspace_size(B, H, Lq, d, dtype_code))
+
+
+def sdpa_bwd(q, k, v, o, lse, dO, dq=None, dk=None, dv=None, *, scale=None, is_causal=False,
+             cu_seqlens=None, max_seqlen=None, workspace=None, stream=None):
+    """Backward pass. Returns ``(dQ, dK, dV)``; layouts as :func:`sdpa_fwd`.
+    ``workspace`` (a uint8 CUDA tensor) is allocated here when not given."""
+    import torch
+    lib = _abi.load()
+    B, H, Lq, Lk, d, packed = _geometry(q, k, cu_seqlens, max_seqlen)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_tensors({"k": k, "v": v, "o": o, "dO": dO, "dq": dq, "dk": dk, "dv": dv}, q.device, q.dtype)
+    code = _dtype_code(q)
+    need = lib.sdpa_bwd_workspace_size(1 if packed else B, H, Lq, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _abi.check(lib.sdpa_bwd(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
+                            B, H, Lq, Lk, d, float(scale), int(bool(is_causal)), _vp(cu_seqlens), code,
+                            _vp(workspace), workspace.numel(), _stream(q.device, stream)))
+    return dq, dk, dv
+
+
+def sdpa_device_status(stream=None):
+    """Synchronise and read/clear the device status word. Returns the raw bits;
+    raises :class:`SdpaError` when a kernel reported a problem."""
+    import torch
+    lib = _abi.load()
+    bits = ctypes.c_uint(0)
+    s = ctypes.c_void_p(stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+    _abi.check(lib.sdpa_device_status(s, ctypes.byref(bits)))
+    return bits.value
+
+
+def sdpa_debug_set(flags: int) -> int:
+    return int(_abi.load().sdpa_debug_set(int(flags)))
+
+
+def sdpa_last_error() -> str:
+    return _abi.load().sdpa_last_error().decode()
+
+
+def sdpa_version() -> int:
+    return int(_abi.load().sdpa_version())

@@ -1,0 +1,255 @@
+// api.cu -- the C ABI declared in include/sdpa.h: argument checks, tensor-map
+// construction, the device status word, and dispatch to the kernels.
+// All checks run on the host before anything is launched; no call allocates.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sdpa.h"
+
+namespace sdpa {
+namespace {
+
+thread_local std::string g_last_error;
+int g_debug_flags = 0;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SDPA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// One status word per device that loads the library; kernels OR bits into it.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {nullptr};
+
+int status_ptr(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SDPA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  if (g_status_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    g_status_ptr[dev] = static_cast<unsigned*>(ptr);
+  }
+  *out = g_status_ptr[dev];
+  return SDPA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  if (g_encode) return SDPA_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return SDPA_OK;
+}
+
+// 3-D tiled map over 16-bit elements: dims {d, n1, n2}, byte strides of
+// dims 1 and 2, box {box0, box1, box2}.
+int make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d, uint64_t n1, uint64_t n2,
+             uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2) {
+  const cuuint64_t dims[3] = {d, n1, n2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw = box0 * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+  return SDPA_OK;
+}
+
+// Map for a q/k/v-like tensor with `rows` rows per unit (dense) or `total`
+// packed tokens, tiled in 128-row boxes of 64 (d >= 64) or 32 (d = 32) columns.
+int make_operand_map(CUtensorMap* m, const void* base, int dtype, bool packed, int B, int H, int rows, int d) {
+  const uint32_t blk = d >= 64 ? 64 : static_cast<uint32_t>(d);
+  const uint64_t es = 2;
+  if (!packed)
+    return make_map(m, base, dtype, d, rows, static_cast<uint64_t>(B) * H, d * es, static_cast<uint64_t>(rows) * d * es,
+                    blk, 128, 1);
+  return make_map(m, base, dtype, d, H, rows, d * es, static_cast<uint64_t>(H) * d * es, blk, 1, 128);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int Lq,
+                 int Lk, int d, float scale, int is_causal, const int* cu, int dtype, bool* noop) {
+  *noop = false;
+  if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return fail(SDPA_ERR_ARG, "unknown dtype %d", dtype);
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d <= 0)
+    return fail(SDPA_ERR_ARG, "sizes must be non-negative and d positive (B=%d H=%d Lq=%d Lk=%d d=%d)", B, H, Lq, Lk, d);
+  if (!std::isfinite(scale)) return fail(SDPA_ERR_ARG, "scale must be finite");
+  if (is_causal != 0 && is_causal != 1) return fail(SDPA_ERR_ARG, "is_causal must be 0 or 1");
+  if (dtype == SDPA_F32) {
+    if (d > 128) return fail(SDPA_ERR_UNSUPPORTED, "float32 path supports d <= 128 (got %d)", d);
+  } else if (d != 32 && d != 64 && d != 128) {
+    return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 path supports d in {32, 64, 128} (got %d)", d);
+  }
+  if (B == 0 || H == 0 || Lq == 0) {
+    *noop = true;
+    return SDPA_OK;
+  }
+  if (cu == nullptr && Lk == 0) return fail(SDPA_ERR_ARG, "Lk = 0 with Lq > 0: softmax over no keys");
+  if (!q || !k || !v || !o || !lse) return fail(SDPA_ERR_ARG, "null tensor pointer");
+  if (dtype != SDPA_F32 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o)))
+    return fail(SDPA_ERR_ARG, "fp16/bf16 tensors must be 16-byte aligned");
+  if (cu != nullptr && Lk == 0) {
+    // every sequence must then be empty; nothing to compute
+    *noop = true;
+  }
+  return SDPA_OK;
+}
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq, int Lk,
+                        int d, float scale, int is_causal, const int* cu_seqlens, int dtype, void* stream) {
+  g_last_error.clear();
+  bool noop = false;
+  int rc = check_common(q, k, v, o, lse, B, H, Lq, Lk, d, scale, is_causal, cu_seqlens, dtype, &noop);
+  if (rc != SDPA_OK || noop) return rc;
+  Problem p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.H = H; p.Lq = Lq; p.Lk = Lk; p.d = d;
+  p.scale = scale; p.causal = is_causal; p.cu_seqlens = cu_seqlens;
+  p.debug = g_debug_flags;
+  rc = status_ptr(&p.status);
+  if (rc != SDPA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == SDPA_F32) {
+    e = launch_fwd_simt(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "forward (fp32) launch");
+    return SDPA_OK;
+  }
+  rc = get_encoder();
+  if (rc != SDPA_OK) return rc;
+  const bool packed = cu_seqlens != nullptr;
+  FwdMaps maps;
+  const int rq = Lq, rk = packed ? Lq : Lk;
+  if ((rc = make_operand_map(&maps.q, q, dtype, packed, B, H, rq, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.k, k, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.v, v, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
+  e = launch_fwd_tc(p, dtype, maps, s);
+  if (e != cudaSuccess) return cuda_fail(e, "forward (tensor-core) launch");
+  return SDPA_OK;
+}
+
+extern "C" size_t sdpa_bwd_workspace_size(int B, int H, int Lq, int d, int dtype) {
+  if (B <= 0 || H <= 0 || Lq <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Lq;
+  const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
+  if (dtype == SDPA_F32) return delta;
+  return delta + rows * d * sizeof(float);
+}
+
+extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                        const int* cu_seqlens, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  bool noop = false;
+  int rc = check_common(q, k, v, o, lse, B, H, Lq, Lk, d, scale, is_causal, cu_seqlens, dtype, &noop);
+  if (rc != SDPA_OK) return rc;
+  if (noop) return SDPA_OK;
+  if (!dO || !dq || !dk || !dv) return fail(SDPA_ERR_ARG, "null gradient pointer");
+  if (dtype != SDPA_F32 && !(aligned16(dO) && aligned16(dq) && aligned16(dk) && aligned16(dv)))
+    return fail(SDPA_ERR_ARG, "fp16/bf16 gradients must be 16-byte aligned");
+  if (cu_seqlens != nullptr) return fail(SDPA_ERR_UNSUPPORTED, "packed (cu_seqlens) backward is not implemented");
+  if (dtype != SDPA_F32 && d == 32) return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 backward supports d in {64, 128}");
+  const size_t need = sdpa_bwd_workspace_size(B, H, Lq, d, dtype);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace == nullptr ? 0 : workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(SDPA_ERR_ARG, "workspace must be 256-byte aligned");
+
+  BwdProblem bp{};
+  Problem& p = bp.f;
+  p.q = q; p.k = k; p.v = v; p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
+  p.B = B; p.H = H; p.Lq = Lq; p.Lk = Lk; p.d = d;
+  p.scale = scale; p.causal = is_causal; p.cu_seqlens = cu_seqlens;
+  p.debug = g_debug_flags;
+  rc = status_ptr(&p.status);
+  if (rc != SDPA_OK) return rc;
+  bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
+  const size_t rows = static_cast<size_t>(B) * H * Lq;
+  bp.delta = static_cast<float*>(workspace);
+  bp.dq_acc = dtype == SDPA_F32 ? nullptr
+                                : reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * 4 + 255) / 256 * 256);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_prep(bp, dtype, dtype == SDPA_F32 ? 0 : 1, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward prep launch");
+  if (dtype == SDPA_F32) {
+    e = launch_bwd_simt(bp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward (fp32) launch");
+    return SDPA_OK;
+  }
+  rc = get_encoder();
+  if (rc != SDPA_OK) return rc;
+  BwdMaps maps;
+  if ((rc = make_operand_map(&maps.q, q, dtype, false, B, H, Lq, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.k, k, dtype, false, B, H, Lk, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.v, v, dtype, false, B, H, Lk, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.dO, dO, dtype, false, B, H, Lq, d)) != SDPA_OK) return rc;
+  e = launch_bwd_tc(bp, dtype, maps, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward (tensor-core) launch");
+  e = launch_dq_convert(bp, dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dQ convert launch");
+  return SDPA_OK;
+}
+
+extern "C" int sdpa_device_status(void* stream, unsigned* bits) {
+  g_last_error.clear();
+  unsigned* ptr = nullptr;
+  int rc = status_ptr(&ptr);
+  if (rc != SDPA_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned word = 0;
+  e = cudaMemcpy(&word, ptr, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (word != 0) {
+    e = cudaMemset(ptr, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  }
+  if (bits) *bits = word;
+  if (word & SDPA_STATUS_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", word);
+  if (word & SDPA_STATUS_SEQLEN) return fail(SDPA_ERR_ARG, "a packed sequence is longer than max_seqlen (status 0x%x)", word);
+  return SDPA_OK;
+}
+
+extern "C" int sdpa_debug_set(int flags) {
+  const int old = g_debug_flags;
+  g_debug_flags = flags;
+  return old;
+}
+
+extern "C" const char* sdpa_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int sdpa_version(void) { return 100; }

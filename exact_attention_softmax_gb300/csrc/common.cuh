@@ -1,0 +1,63 @@
+// common.cuh -- definitions shared by the C-ABI layer and the kernels of the
+// GB300 exact-attention library (internal; not part of the public header).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sdpa {
+
+constexpr unsigned kStatusTimeout = 1u;  // == SDPA_STATUS_TIMEOUT
+constexpr unsigned kStatusSeqlen = 2u;   // == SDPA_STATUS_SEQLEN
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per mbarrier wait
+
+// Debug switches (testing only; zero in normal use).
+constexpr int kDebugDropQArrive = 1;  // forward producer never loads Q: every wait times out
+
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+// One attention problem as the kernels see it. Dense: q/o [B,H,Lq,d],
+// k/v [B,H,Lk,d], lse [B,H,Lq]. Packed (cu_seqlens != nullptr): q/k/v/o
+// [total,H,d] with total = Lq, lse [H,total], Lk = max sequence length.
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, Lq, Lk, d;
+  float scale;
+  int causal;
+  const int* cu_seqlens;
+  unsigned* status;  // device status word (bit flags above)
+  int debug;
+};
+
+struct BwdProblem {
+  Problem f;          // q, k, v, o, lse as in the forward
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;       // [rows] fp32 workspace: rowsum(dO * O)
+  float* dq_acc;      // [rows, d] fp32 workspace (tensor-core path only)
+};
+
+// Tensor maps for the tensor-core kernels (built on the host by the C-ABI layer).
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+struct BwdMaps {
+  CUtensorMap q, k, v, dO;
+};
+
+// Launchers (each in its own translation unit).
+cudaError_t launch_fwd_simt(const Problem& p, cudaStream_t s);
+cudaError_t launch_bwd_simt(const BwdProblem& p, cudaStream_t s);
+cudaError_t launch_fwd_tc(const Problem& p, int dtype, const FwdMaps& maps, cudaStream_t s);
+cudaError_t launch_bwd_prep(const BwdProblem& p, int dtype, int zero_dq_acc, cudaStream_t s);
+cudaError_t launch_bwd_tc(const BwdProblem& p, int dtype, const BwdMaps& maps, cudaStream_t s);
+cudaError_t launch_dq_convert(const BwdProblem& p, int dtype, cudaStream_t s);
+
+}  // namespace sdpa

@@ -1,0 +1,289 @@
+// simt_f32.cu -- plain-fp32 attention kernels (FFMA + expf, no tensor cores,
+// no TF32) for float32 inputs, where the 1e-5 error budget rules out reduced
+// precision operands.
+//
+// Forward: one thread per query row streams K/V tiles through shared memory
+// and keeps a running maximum m, running sum l and unnormalised output, rescaled
+// whenever m grows (the online softmax that lets the FlashAttention news
+// article's tiled algorithm, section "FlashAttention", stay exact). It writes
+// O = acc / l and LSE = m + log l.
+// Backward (recompute, same section): one kernel walks keys per query row for
+// dQ, another walks queries per key row for dK and dV; both rebuild
+// P_ij = exp(scale q_i.k_j - LSE_i) and dS_ij = P_ij (dO_i.v_j - D_i) with
+// D_i = rowsum(dO_i * O_i) from the prep kernel.
+#include "common.cuh"
+
+namespace sdpa {
+namespace {
+
+constexpr int kRows = 128;   // query (or key) rows per block
+constexpr int kTile = 32;    // rows of the other operand staged per step
+
+struct Unit {
+  int len_q, len_k;   // rows of this (batch|sequence, head)
+  long long base;     // element offset of row 0
+  long long stride;   // elements between consecutive rows
+  long long stat;     // offset of row 0 in lse / delta
+};
+
+__device__ __forceinline__ Unit unit_of(const Problem& p, int b, int h) {
+  Unit u;
+  if (p.cu_seqlens == nullptr) {
+    u.len_q = p.Lq;
+    u.len_k = p.Lk;
+    u.stride = p.d;
+    u.base = (static_cast<long long>(b) * p.H + h) * p.Lq * p.d;
+    u.stat = (static_cast<long long>(b) * p.H + h) * p.Lq;
+  } else {
+    const int s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
+    u.len_q = u.len_k = s1 - s0;
+    u.stride = static_cast<long long>(p.H) * p.d;
+    u.base = static_cast<long long>(s0) * p.H * p.d + static_cast<long long>(h) * p.d;
+    u.stat = static_cast<long long>(h) * p.Lq + s0;
+  }
+  return u;
+}
+// Dense K/V rows live in their own [B,H,Lk,d] tensor.
+__device__ __forceinline__ long long kv_base(const Problem& p, int b, int h, const Unit& u) {
+  if (p.cu_seqlens == nullptr) return (static_cast<long long>(b) * p.H + h) * p.Lk * p.d;
+  return u.base;
+}
+
+template <int DMAX>
+__global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const Unit u = unit_of(p, b, h);
+  if (p.cu_seqlens != nullptr && u.len_q > p.Lk) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+  }
+  const int row0 = blockIdx.x * kRows;
+  if (row0 >= u.len_q) return;
+  const int row = row0 + threadIdx.x;
+  const bool live = row < u.len_q;
+  const int d = p.d;
+  const float* Q = static_cast<const float*>(p.q) + u.base;
+  const long long kvb = kv_base(p, b, h, u);
+  const float* K = static_cast<const float*>(p.k) + kvb;
+  const float* V = static_cast<const float*>(p.v) + kvb;
+
+  __shared__ float sk[kTile][DMAX];
+  __shared__ float sv[kTile][DMAX];
+
+  float qr[DMAX], acc[DMAX];
+#pragma unroll
+  for (int c = 0; c < DMAX; ++c) {
+    qr[c] = (live && c < d) ? Q[row * u.stride + c] : 0.f;
+    acc[c] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  int kend = u.len_k;
+  if (p.causal) kend = min(kend, min(row0 + kRows, u.len_q));
+  for (int kb = 0; kb < kend; kb += kTile) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTile * DMAX; e += kRows) {
+      const int r = e / DMAX, c = e % DMAX;
+      const bool ok = (kb + r < u.len_k) && c < d;
+      sk[r][c] = ok ? K[(kb + r) * u.stride + c] : 0.f;
+      sv[r][c] = ok ? V[(kb + r) * u.stride + c] : 0.f;
+    }
+    __syncthreads();
+    if (!live) continue;
+    for (int jj = 0; jj < kTile; ++jj) {
+      const int key = kb + jj;
+      if (key >= u.len_k || (p.causal && key > row)) break;
+      float s = 0.f;
+#pragma unroll
+      for (int c = 0; c < DMAX; ++c) s = fmaf(qr[c], sk[jj][c], s);
+      s *= p.scale;
+      if (s > m) {
+        const float corr = expf(m - s);
+        l *= corr;
+#pragma unroll
+        for (int c = 0; c < DMAX; ++c) acc[c] *= corr;
+        m = s;
+      }
+      const float e = expf(s - m);
+      l += e;
+#pragma unroll
+      for (int c = 0; c < DMAX; ++c) acc[c] = fmaf(e, sv[jj][c], acc[c]);
+    }
+  }
+  if (!live) return;
+  float* O = static_cast<float*>(p.o) + u.base;
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int c = 0; c < DMAX; ++c)
+    if (c < d) O[row * u.stride + c] = acc[c] * inv;
+  p.lse[u.stat + row] = m + logf(l);
+}
+
+// dQ_i = scale * sum_j P_ij (dO_i.v_j - D_i) k_j
+template <int DMAX>
+__global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
+  const Problem& p = bp.f;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const Unit u = unit_of(p, b, h);
+  const int row0 = blockIdx.x * kRows;
+  if (row0 >= u.len_q) return;
+  const int row = row0 + threadIdx.x;
+  const bool live = row < u.len_q;
+  const int d = p.d;
+  const long long kvb = kv_base(p, b, h, u);
+  const float* Q = static_cast<const float*>(p.q) + u.base;
+  const float* dO = static_cast<const float*>(bp.dO) + u.base;
+  const float* K = static_cast<const float*>(p.k) + kvb;
+  const float* V = static_cast<const float*>(p.v) + kvb;
+
+  __shared__ float sk[kTile][DMAX];
+  __shared__ float sv[kTile][DMAX];
+  float qr[DMAX], dor[DMAX], dq[DMAX];
+#pragma unroll
+  for (int c = 0; c < DMAX; ++c) {
+    qr[c] = (live && c < d) ? Q[row * u.stride + c] : 0.f;
+    dor[c] = (live && c < d) ? dO[row * u.stride + c] : 0.f;
+    dq[c] = 0.f;
+  }
+  const float lse = live ? p.lse[u.stat + row] : 0.f;
+  const float D = live ? bp.delta[u.stat + row] : 0.f;
+  int kend = u.len_k;
+  if (p.causal) kend = min(kend, min(row0 + kRows, u.len_q));
+  for (int kb = 0; kb < kend; kb += kTile) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTile * DMAX; e += kRows) {
+      const int r = e / DMAX, c = e % DMAX;
+      const bool ok = (kb + r < u.len_k) && c < d;
+      sk[r][c] = ok ? K[(kb + r) * u.stride + c] : 0.f;
+      sv[r][c] = ok ? V[(kb + r) * u.stride + c] : 0.f;
+    }
+    __syncthreads();
+    if (!live) continue;
+    for (int jj = 0; jj < kTile; ++jj) {
+      const int key = kb + jj;
+      if (key >= u.len_k || (p.causal && key > row)) break;
+      float s = 0.f, dp = 0.f;
+#pragma unroll
+      for (int c = 0; c < DMAX; ++c) {
+        s = fmaf(qr[c], sk[jj][c], s);
+        dp = fmaf(dor[c], sv[jj][c], dp);
+      }
+      const float pr = expf(s * p.scale - lse);
+      const float ds = pr * (dp - D);
+#pragma unroll
+      for (int c = 0; c < DMAX; ++c) dq[c] = fmaf(ds, sk[jj][c], dq[c]);
+    }
+  }
+  if (!live) return;
+  float* dQ = static_cast<float*>(bp.dq) + u.base;
+#pragma unroll
+  for (int c = 0; c < DMAX; ++c)
+    if (c < d) dQ[row * u.stride + c] = dq[c] * p.scale;
+}
+
+// dV_j = sum_i P_ij dO_i ; dK_j = scale * sum_i P_ij (dO_i.v_j - D_i) q_i
+template <int DMAX>
+__global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
+  const Problem& p = bp.f;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const Unit u = unit_of(p, b, h);
+  const int key0 = blockIdx.x * kRows;
+  if (key0 >= u.len_k) return;
+  const int key = key0 + threadIdx.x;
+  const bool live = key < u.len_k;
+  const int d = p.d;
+  const long long kvb = kv_base(p, b, h, u);
+  const float* Q = static_cast<const float*>(p.q) + u.base;
+  const float* dO = static_cast<const float*>(bp.dO) + u.base;
+  const float* K = static_cast<const float*>(p.k) + kvb;
+  const float* V = static_cast<const float*>(p.v) + kvb;
+
+  __shared__ float sq[kTile][DMAX];
+  __shared__ float sdo[kTile][DMAX];
+  __shared__ float slse[kTile], sD[kTile];
+  float kr[DMAX], vr[DMAX], dk[DMAX], dv[DMAX];
+#pragma unroll
+  for (int c = 0; c < DMAX; ++c) {
+    kr[c] = (live && c < d) ? K[key * u.stride + c] : 0.f;
+    vr[c] = (live && c < d) ? V[key * u.stride + c] : 0.f;
+    dk[c] = 0.f;
+    dv[c] = 0.f;
+  }
+  const int qstart = p.causal ? key0 : 0;
+  for (int qb = qstart; qb < u.len_q; qb += kTile) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTile * DMAX; e += kRows) {
+      const int r = e / DMAX, c = e % DMAX;
+      const bool ok = (qb + r < u.len_q) && c < d;
+      sq[r][c] = ok ? Q[(qb + r) * u.stride + c] : 0.f;
+      sdo[r][c] = ok ? dO[(qb + r) * u.stride + c] : 0.f;
+    }
+    if (threadIdx.x < kTile) {
+      const int r = qb + threadIdx.x;
+      slse[threadIdx.x] = r < u.len_q ? p.lse[u.stat + r] : 0.f;
+      sD[threadIdx.x] = r < u.len_q ? bp.delta[u.stat + r] : 0.f;
+    }
+    __syncthreads();
+    if (!live) continue;
+    for (int ii = 0; ii < kTile; ++ii) {
+      const int qi = qb + ii;
+      if (qi >= u.len_q) break;
+      if (p.causal && key > qi) continue;
+      float s = 0.f, dp = 0.f;
+#pragma unroll
+      for (int c = 0; c < DMAX; ++c) {
+        s = fmaf(sq[ii][c], kr[c], s);
+        dp = fmaf(sdo[ii][c], vr[c], dp);
+      }
+      const float pr = expf(s * p.scale - slse[ii]);
+      const float ds = pr * (dp - sD[ii]);
+#pragma unroll
+      for (int c = 0; c < DMAX; ++c) {
+        dv[c] = fmaf(pr, sdo[ii][c], dv[c]);
+        dk[c] = fmaf(ds, sq[ii][c], dk[c]);
+      }
+    }
+  }
+  if (!live) return;
+  float* dK = static_cast<float*>(bp.dk) + kvb;
+  float* dV = static_cast<float*>(bp.dv) + kvb;
+#pragma unroll
+  for (int c = 0; c < DMAX; ++c) {
+    if (c < d) {
+      dK[key * u.stride + c] = dk[c] * p.scale;
+      dV[key * u.stride + c] = dv[c];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const Problem& p, cudaStream_t s) {
+  const bool packed = p.cu_seqlens != nullptr;
+  const int rows = packed ? p.Lk : p.Lq;  // packed: Lk bounds every sequence length
+  dim3 grid((rows + kRows - 1) / kRows, p.H, p.B);
+  if (grid.x == 0) return cudaSuccess;
+  if (p.d <= 32) fwd_f32_kernel<32><<<grid, kRows, 0, s>>>(p);
+  else if (p.d <= 64) fwd_f32_kernel<64><<<grid, kRows, 0, s>>>(p);
+  else fwd_f32_kernel<128><<<grid, kRows, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_simt(const BwdProblem& bp, cudaStream_t s) {
+  const Problem& p = bp.f;
+  const bool packed = p.cu_seqlens != nullptr;
+  const int rq = packed ? p.Lk : p.Lq;
+  const int rk = p.Lk;
+  dim3 gq((rq + kRows - 1) / kRows, p.H, p.B), gk((rk + kRows - 1) / kRows, p.H, p.B);
+  if (p.d <= 32) {
+    if (gq.x) bwd_dq_f32_kernel<32><<<gq, kRows, 0, s>>>(bp);
+    if (gk.x) bwd_dkdv_f32_kernel<32><<<gk, kRows, 0, s>>>(bp);
+  } else if (p.d <= 64) {
+    if (gq.x) bwd_dq_f32_kernel<64><<<gq, kRows, 0, s>>>(bp);
+    if (gk.x) bwd_dkdv_f32_kernel<64><<<gk, kRows, 0, s>>>(bp);
+  } else {
+    if (gq.x) bwd_dq_f32_kernel<128><<<gq, kRows, 0, s>>>(bp);
+    if (gk.x) bwd_dkdv_f32_kernel<128><<<gk, kRows, 0, s>>>(bp);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sdpa

@@ -1,0 +1,137 @@
+/*
+ * sdpa.h -- C ABI of the GB300 (sm_103a) exact scaled dot-product attention.
+ *
+ * The operation (SDPA tutorial page "(Beta) Implementing High-Performance
+ * Transformers with Scaled Dot Product Attention", section "Overview"):
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V
+ *
+ * computed IO-aware as in the FlashAttention news article (QbitAI repost,
+ * section "FlashAttention"): the kernels tile Q and K/V through on-chip
+ * memory so the Lq x Lk score matrix never reaches HBM; the forward keeps a
+ * running row maximum and row sum across K/V blocks and saves the per-row
+ * log-sum-exp, and the backward recomputes the probabilities from Q, K and
+ * that log-sum-exp instead of storing them.
+ *
+ * General rules for every call:
+ *  - All tensor arguments are DEVICE pointers owned by the caller, on the
+ *    device that is current for the calling thread. The library allocates
+ *    nothing, keeps no reference after the call returns, and runs
+ *    asynchronously on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - Tensors are contiguous. Element type is `dtype` (sdpa_dtype) for
+ *    q/k/v/o/dO/dq/dk/dv; lse is always float32.
+ *  - Dense layout (cu_seqlens == NULL): q, o, dO, dq are [B, H, Lq, d];
+ *    k, v, dk, dv are [B, H, Lk, d]; lse is [B, H, Lq].
+ *  - Packed variable-length layout (cu_seqlens != NULL; the tutorial's
+ *    NestedTensor batches, section "NestedTensor and Dense tensor support"):
+ *    q, k, v, o (and gradients) are [total, H, d] with the tokens of
+ *    sequence s at rows cu_seqlens[s] .. cu_seqlens[s+1]-1; the same offsets
+ *    serve queries and keys (self-attention). `cu_seqlens` is a device int32
+ *    array of B+1 non-decreasing offsets starting at 0. In this mode B is the
+ *    number of sequences, Lq is the packed token count `total`
+ *    (= cu_seqlens[B]) and Lk is an upper bound on every sequence length
+ *    (max_seqlen); lse is [H, total].
+ *  - Causal masking is top-left aligned: query i sees keys j <= i (within its
+ *    sequence when packed).
+ *  - Return value: SDPA_OK or a negative sdpa_status. Argument errors are
+ *    detected on the host before anything is launched. A nonzero return
+ *    leaves a message for sdpa_last_error(). Errors found by a kernel while
+ *    it runs (a bounded wait that gave up, a packed sequence longer than Lk)
+ *    are recorded in a device status word that sdpa_device_status() reads.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SDPA_F32 = 0, SDPA_F16 = 1, SDPA_BF16 = 2 } sdpa_dtype;
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_ARG = -1,         /* null pointer, non-positive size, bad scale, Lk = 0 with Lq > 0 */
+  SDPA_ERR_UNSUPPORTED = -2, /* head dim / dtype / mode this build does not implement */
+  SDPA_ERR_CUDA = -3,        /* a CUDA runtime call failed (message names it) */
+  SDPA_ERR_TIMEOUT = -4,     /* a kernel's bounded wait gave up (from sdpa_device_status) */
+  SDPA_ERR_WORKSPACE = -5    /* workspace NULL or smaller than sdpa_bwd_workspace_size() */
+} sdpa_status;
+
+/* Bits of the device status word (see sdpa_device_status). */
+#define SDPA_STATUS_TIMEOUT 1u   /* an mbarrier wait exceeded its time limit; outputs invalid */
+#define SDPA_STATUS_SEQLEN 2u    /* a packed sequence is longer than Lk (max_seqlen); outputs invalid */
+
+/*
+ * Forward: O and LSE.
+ *   q, k, v : inputs (layouts above), dtype `dtype`.
+ *   o       : output, same layout as q.
+ *   lse     : float32 output, natural-log log-sum-exp of each query row
+ *             (lse_i = log sum_j exp(scale * q_i . k_j) over visible j).
+ *   B, H, Lq, Lk, d : sizes (packed mode: see the layout rules above).
+ *   scale   : the softmax scale (usually 1/sqrt(d)); must be finite.
+ *   is_causal : 0 or 1.
+ * Supported: dtype F32 with d <= 128 (plain fp32 arithmetic, no TF32);
+ * F16 / BF16 with d in {32, 64, 128} (tensor cores, fp32 accumulation).
+ * Lq == 0 (or B == 0 / H == 0) is a no-op that returns SDPA_OK.
+ */
+int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+             const int* cu_seqlens, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace sdpa_bwd needs for these sizes (a float32 row
+ * statistic D = rowsum(dO * O) and a float32 dQ accumulator, both over the
+ * query rows). Packed mode: pass B = 1 and Lq = total. Never fails; returns
+ * 0 when nothing is needed.
+ */
+size_t sdpa_bwd_workspace_size(int B, int H, int Lq, int d, int dtype);
+
+/*
+ * Backward: gradients of sum(dO * O) w.r.t. q, k, v, recomputing the
+ * probabilities from q, k and the forward's lse (the pages' "recompute in
+ * the backward pass").
+ *   q, k, v, o, lse : the forward's inputs and outputs (o and lse exactly as
+ *                     sdpa_fwd wrote them).
+ *   dO      : upstream gradient, layout of o.
+ *   dq, dk, dv : outputs, layouts of q, k, v; fully overwritten.
+ *   workspace : device scratch of at least sdpa_bwd_workspace_size() bytes,
+ *               256-byte aligned; its contents on entry do not matter.
+ * Other arguments as for sdpa_fwd. Supported: F32 with d <= 128; F16/BF16
+ * with d in {64, 128}; packed (cu_seqlens != NULL) batches return
+ * SDPA_ERR_UNSUPPORTED in this version.
+ */
+int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv,
+             int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+             const int* cu_seqlens, int dtype,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device. Returns SDPA_OK, SDPA_ERR_TIMEOUT (bit SDPA_STATUS_TIMEOUT
+ * was set), SDPA_ERR_ARG (bit SDPA_STATUS_SEQLEN was set) or SDPA_ERR_CUDA.
+ * If `bits` is not NULL the raw word is stored there.
+ */
+int sdpa_device_status(void* stream, unsigned* bits);
+
+/*
+ * Testing aid: sets debug flags for later calls on any thread and returns the
+ * previous value. Flag 1 makes the forward tensor-core kernel skip its Q load,
+ * so every wait in it runs out and sdpa_device_status() reports
+ * SDPA_ERR_TIMEOUT after about a second. 0 (the default) is normal operation.
+ */
+int sdpa_debug_set(int flags);
+
+/* Message for the last nonzero return on the calling thread ("" if none). */
+const char* sdpa_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int sdpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads without
+a GPU, exports every function include/sdpa.h declares, and rejects bad
+arguments before anything reaches CUDA (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_softmax_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = ctypes.c_void_p(0x100000)  # never dereferenced: every call below fails validation first
+
+
+def _header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(sdpa_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib(built_lib):
+    return _abi.load(built_lib)
+
+
+def test_library_exports_every_declared_function(lib):
+    declared = _header_functions()
+    assert {"sdpa_fwd", "sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_last_error"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(_abi.SIGNATURES) >= declared
+
+
+def test_version_and_empty_error(lib):
+    assert lib.sdpa_version() >= 100
+    assert lib.sdpa_last_error() == b""
+
+
+def _fwd(lib, B=1, H=1, Lq=4, Lk=4, d=64, scale=0.125, causal=0, cu=None, dtype=1, ptr=FAKE):
+    return lib.sdpa_fwd(ptr, ptr, ptr, ptr, ptr, B, H, Lq, Lk, d, scale, causal, cu, dtype, None)
+
+
+def test_argument_errors(lib):
+    assert _fwd(lib, dtype=7) == _abi.SDPA_ERR_ARG
+    assert b"dtype" in lib.sdpa_last_error()
+    assert _fwd(lib, d=0) == _abi.SDPA_ERR_ARG
+    assert _fwd(lib, B=-1) == _abi.SDPA_ERR_ARG
+    assert _fwd(lib, scale=float("nan")) == _abi.SDPA_ERR_ARG
+    assert _fwd(lib, scale=float("inf")) == _abi.SDPA_ERR_ARG
+    assert _fwd(lib, causal=2) == _abi.SDPA_ERR_ARG
+    assert _fwd(lib, Lk=0) == _abi.SDPA_ERR_ARG            # softmax over no keys
+    assert _fwd(lib, ptr=ctypes.c_void_p(0)) == _abi.SDPA_ERR_ARG
+    misaligned = ctypes.c_void_p(0x100008)
+    assert _fwd(lib, ptr=misaligned) == _abi.SDPA_ERR_ARG   # TMA needs 16-byte aligned tensors
+
+
+def test_unsupported_shapes(lib):
+    assert _fwd(lib, d=48) == _abi.SDPA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=256, dtype=2) == _abi.SDPA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=129, dtype=0) == _abi.SDPA_ERR_UNSUPPORTED
+    assert b"d" in lib.sdpa_last_error()
+
+
+def test_empty_problems_are_noops(lib):
+    # nothing to compute: returns OK without touching CUDA or the pointers
+    assert _fwd(lib, Lq=0, ptr=ctypes.c_void_p(0)) == _abi.SDPA_OK
+    assert _fwd(lib, B=0, ptr=ctypes.c_void_p(0)) == _abi.SDPA_OK
+    assert _fwd(lib, H=0, ptr=ctypes.c_void_p(0)) == _abi.SDPA_OK
+
+
+def test_workspace_size_and_errors(lib):
+    assert lib.sdpa_bwd_workspace_size(0, 1, 1, 64, 1) == 0
+    # fp32: only the row statistic D, rounded up to 256 bytes
+    assert lib.sdpa_bwd_workspace_size(2, 1, 3, 8, 0) == 256
+    # fp16: D plus an fp32 dQ accumulator
+    B, H, L, d = 32, 8, 1024, 64
+    n = B * H * L
+    assert lib.sdpa_bwd_workspace_size(B, H, L, d, 1) == (n * 4 + 255) // 256 * 256 + n * d * 4
+    args = [FAKE] * 9 + [B, H, L, L, d, 0.125, 1, None, 1]
+    assert lib.sdpa_bwd(*args, FAKE, 16, None) == _abi.SDPA_ERR_WORKSPACE
+    assert lib.sdpa_bwd(*args, None, 1 << 40, None) == _abi.SDPA_ERR_WORKSPACE
+    assert b"workspace" in lib.sdpa_last_error()
+    # packed backward is not in this version
+    args_p = [FAKE] * 9 + [2, H, 100, 64, d, 0.125, 0, FAKE, 1]
+    assert lib.sdpa_bwd(*args_p, FAKE, 1 << 30, None) == _abi.SDPA_ERR_UNSUPPORTED
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _abi.load(str(tmp_path / "nope.so"))
