@@ -84,13 +84,14 @@ int make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d, uint64_t n
 
 // Map for a q/k/v-like tensor with `rows` rows per unit (dense) or `total`
 // packed tokens, tiled in 128-row boxes of 64 (d >= 64) or 32 (d = 32) columns.
-int make_operand_map(CUtensorMap* m, const void* base, int dtype, bool packed, int B, int H, int rows, int d) {
+int make_operand_map(CUtensorMap* m, const void* base, int dtype, bool packed, int B, int H, int rows, int d,
+                     uint32_t box_rows = 128) {
   const uint32_t blk = d >= 64 ? 64 : static_cast<uint32_t>(d);
   const uint64_t es = 2;
   if (!packed)
     return make_map(m, base, dtype, d, rows, static_cast<uint64_t>(B) * H, d * es, static_cast<uint64_t>(rows) * d * es,
-                    blk, 128, 1);
-  return make_map(m, base, dtype, d, H, rows, d * es, static_cast<uint64_t>(H) * d * es, blk, 1, 128);
+                    blk, box_rows, 1);
+  return make_map(m, base, dtype, d, H, rows, d * es, static_cast<uint64_t>(H) * d * es, blk, 1, box_rows);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -211,10 +212,11 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
   rc = get_encoder();
   if (rc != SDPA_OK) return rc;
   BwdMaps maps;
-  if ((rc = make_operand_map(&maps.q, q, dtype, false, B, H, Lq, d)) != SDPA_OK) return rc;
+  const uint32_t bq = d == 128 ? 64 : 128;  // query rows per backward step
+  if ((rc = make_operand_map(&maps.q, q, dtype, false, B, H, Lq, d, bq)) != SDPA_OK) return rc;
   if ((rc = make_operand_map(&maps.k, k, dtype, false, B, H, Lk, d)) != SDPA_OK) return rc;
   if ((rc = make_operand_map(&maps.v, v, dtype, false, B, H, Lk, d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.dO, dO, dtype, false, B, H, Lq, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.dO, dO, dtype, false, B, H, Lq, d, bq)) != SDPA_OK) return rc;
   e = launch_bwd_tc(bp, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward (tensor-core) launch");
   e = launch_dq_convert(bp, dtype, s);

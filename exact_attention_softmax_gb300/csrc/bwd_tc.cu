@@ -1,6 +1,458 @@
-// bwd_tc.cu -- placeholder until the tensor-core backward lands.
-#include "common.cuh"
+// bwd_tc.cu -- exact attention backward on the sm_103a tensor cores.
+//
+// Recomputation as in the FlashAttention news article (QbitAI repost, section
+// "FlashAttention"): the probabilities are rebuilt from Q, K and the saved
+// log-sum-exp rather than stored. Each CTA keeps one 128-key block of K and V
+// (and its dK, dV accumulators in TMEM) and streams the query tiles that can
+// see it. Per query tile i of BQ rows, with everything transposed so that keys
+// sit on TMEM lanes:
+//
+//   S^T  = K Q_i^T                (tcgen05, TMEM)
+//   dP^T = V dO_i^T               (tcgen05, TMEM)
+//   P^T  = exp(scale S^T - LSE_i),  dS^T = P^T * (dP^T - D_i)
+//                                 (one thread per key row, written to SMEM)
+//   dV  += P^T dO_i ;  dK += dS^T Q_i                      (tcgen05, TMEM)
+//   dQ_i partial = dS K   (d <= 64: M = query rows)
+//             or  (K^T dS^T)^T (d = 128: M = head dims)    (tcgen05, TMEM)
+//
+// and the dQ partial is added into an fp32 accumulator in global memory with
+// one bulk shared->global reduce per tile. dK = scale * dK_acc and dV are
+// written at the end; dQ = scale * dQ_acc is rounded by a separate kernel.
+//
+// Warps: 0-3 build P^T / dS^T (then write dV), 4-7 drain dQ (then write dK),
+// 8 loads with TMA, 9 issues the MMAs from one thread.
+#include <type_traits>
+
+#include "ptx.cuh"
 
 namespace sdpa {
-cudaError_t launch_bwd_tc(const BwdProblem&, int, const BwdMaps&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BK = 128;          // keys per CTA
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BCfg {
+  static constexpr int BQ = D == 128 ? 64 : 128;            // query rows per step
+  static constexpr bool kDqT = D == 128;                     // dQ computed transposed
+  static constexpr int kBlk = D >= 64 ? 64 : D;
+  static constexpr int kNBlk = D / kBlk;
+  static constexpr uint32_t kSw = D >= 64 ? kSwizzle128B : kSwizzle64B;
+  static constexpr int kRowBytes = kBlk * 2;
+  static constexpr int kSbo = 8 * kRowBytes;
+  static constexpr int kKColBlk = BK * kRowBytes;            // column block of a K/V tile
+  static constexpr int kQColBlk = BQ * kRowBytes;            // column block of a Q/dO tile
+  static constexpr int kKTile = BK * D * 2;
+  static constexpr int kQTile = BQ * D * 2;
+  static constexpr int kPColBlk = BK * 128;                  // P^T / dS^T: [128 keys][64 queries] blocks
+  static constexpr int kPBytes = BK * BQ * 2;
+  static constexpr int kDqBytes = BQ * D * 4;                // fp32 dQ staging tile
+  static constexpr int kStages = 2;
+  // shared memory map
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKTile;
+  static constexpr int kOffQ = kOffV + kKTile;                          // kStages Q tiles
+  static constexpr int kOffDO = kOffQ + kStages * kQTile;               // kStages dO tiles
+  static constexpr int kOffPT = kOffDO + kStages * kQTile;
+  static constexpr int kOffDST = kOffPT + kPBytes;
+  static constexpr int kOffDQ = kOffDST + kPBytes;
+  static constexpr int kOffStat = kOffDQ + kDqBytes;                    // kStages x (lse2[BQ], delta[BQ])
+  static constexpr int kOffBar = kOffStat + kStages * BQ * 8;
+  static constexpr int kSmem = kOffBar + 256 + 1024;
+  // TMEM columns
+  static constexpr uint32_t kTS = 0, kTdP = BQ, kTdV = 2 * BQ, kTdK = 2 * BQ + D, kTdQ = 2 * BQ + 2 * D;
+};
+
+struct __align__(8) BBars {
+  uint64_t kv;
+  uint64_t full[2];
+  uint64_t empty[2];
+  uint64_t s;
+  uint64_t p;
+  uint64_t dq_full;
+  uint64_t dq_free;
+  uint64_t kv_done;
+  uint64_t done;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+               ::"l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+template <int D, typename T, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO) {
+  using C = BCfg<D>;
+  constexpr int BQ = C::BQ;
+  const Problem& p = bp.f;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BBars* bars = reinterpret_cast<BBars*>(smem + C::kOffBar);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  const int units = p.B * p.H;
+  const int unit = blockIdx.x % units;
+  const int kblk = blockIdx.x / units;
+  const int key0 = kblk * BK;
+  const int Lq = p.Lq, Lk = p.Lk;
+  const int nq = (Lq + BQ - 1) / BQ;
+  const int i0 = CAUSAL ? min(nq, key0 / BQ) : 0;
+  const int nsteps = nq - i0;
+  if (key0 >= Lk) return;
+
+  const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
+  const uint32_t sPT = smem_u32(smem + C::kOffPT), sDST = smem_u32(smem + C::kOffDST);
+  const uint32_t sDQ = smem_u32(smem + C::kOffDQ);
+  float* stat = reinterpret_cast<float*>(smem + C::kOffStat);   // [stage][2][BQ]
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->full[i], 32);
+      mbar_init(&bars->empty[i], 1);
+    }
+    mbar_init(&bars->s, 1);
+    mbar_init(&bars->p, 128);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->kv_done, 1);
+    mbar_init(&bars->done, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile uint32_t* abort_flag = &bars->abort_flag;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_expect_tx(&bars->kv, 2 * C::kKTile);
+      for (int cb = 0; cb < C::kNBlk; ++cb) {
+        tma_load_3d(smem + C::kOffK + cb * C::kKColBlk, &tmK, &bars->kv, cb * C::kBlk, key0, unit);
+        tma_load_3d(smem + C::kOffV + cb * C::kKColBlk, &tmV, &bars->kv, cb * C::kBlk, key0, unit);
+      }
+    }
+    const float* lse = p.lse + static_cast<long long>(unit) * Lq;
+    const float* delta = bp.delta + static_cast<long long>(unit) * Lq;
+    int s = 0;
+    for (; s < nsteps; ++s) {
+      const int stage = s & 1, round = s >> 1;
+      bool ok = true;
+      if (lane == 0 && round > 0) ok = mbar_wait(&bars->empty[stage], (round - 1) & 1, abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const int q0 = (i0 + s) * BQ;
+      float* st = stat + stage * 2 * BQ;
+      for (int c = lane; c < BQ; c += 32) {
+        const int q = q0 + c;
+        st[c] = q < Lq ? lse[q] * kLog2e : INFINITY;
+        st[BQ + c] = q < Lq ? delta[q] : 0.f;
+      }
+      if (lane == 0) {
+        mbar_expect_tx(&bars->full[stage], 2 * C::kQTile);
+        for (int cb = 0; cb < C::kNBlk; ++cb) {
+          tma_load_3d(smem + C::kOffQ + stage * C::kQTile + cb * C::kQColBlk, &tmQ, &bars->full[stage],
+                      cb * C::kBlk, q0, unit);
+          tma_load_3d(smem + C::kOffDO + stage * C::kQTile + cb * C::kQColBlk, &tmDO, &bars->full[stage],
+                      cb * C::kBlk, q0, unit);
+        }
+      } else {
+        mbar_arrive(&bars->full[stage]);
+      }
+    }
+    if (lane == 0 && *abort_flag) {
+      mbar_wait_drain(&bars->kv, 0);
+      for (int f = max(0, s - 2); f < s; ++f) mbar_wait_drain(&bars->full[f & 1], (f >> 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
+      constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BK, BQ);            // S^T, dP^T: M = keys, N = queries
+      constexpr uint32_t idKV = idesc_f16(fmt, 0, 1, BK, D);            // dV, dK: M = keys, N = D
+      constexpr uint32_t idQ = C::kDqT ? idesc_f16(fmt, 1, 1, D, BQ)    // dQ^T: M = D, N = queries
+                                       : idesc_f16(fmt, 1, 1, BQ, D);   // dQ: M = queries, N = D
+      bool ok = mbar_wait(&bars->kv, 0, abort_flag, p.status);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int stage = s & 1;
+        if (!(ok = mbar_wait(&bars->full[stage], (s >> 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        const uint32_t q = sQ + stage * C::kQTile, dO = sDO + stage * C::kQTile;
+        // S^T = K Q^T and dP^T = V dO^T (K-major operands, contraction over D)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t cb = ks * 16 / C::kBlk, within = (ks * 16 % C::kBlk) * 2;
+          mma_ss(tmem + C::kTS, smem_desc(sK + cb * C::kKColBlk + within, 16, C::kSbo, C::kSw),
+                 smem_desc(q + cb * C::kQColBlk + within, 16, C::kSbo, C::kSw), idS, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t cb = ks * 16 / C::kBlk, within = (ks * 16 % C::kBlk) * 2;
+          mma_ss(tmem + C::kTdP, smem_desc(sV + cb * C::kKColBlk + within, 16, C::kSbo, C::kSw),
+                 smem_desc(dO + cb * C::kQColBlk + within, 16, C::kSbo, C::kSw), idS, ks > 0);
+        }
+        mma_commit(&bars->s);
+        if (!(ok = mbar_wait(&bars->p, s & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q (A K-major over queries, B MN-major)
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks) {
+          const uint32_t aoff = (ks / 4) * C::kPColBlk + (ks % 4) * 32;
+          const uint32_t boff = ks * 16 * C::kRowBytes;
+          const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
+          mma_ss(tmem + C::kTdV, smem_desc(sPT + aoff, 16, 1024, kSwizzle128B),
+                 smem_desc(dO + boff, C::kQColBlk, C::kSbo, C::kSw), idKV, acc);
+          mma_ss(tmem + C::kTdK, smem_desc(sDST + aoff, 16, 1024, kSwizzle128B),
+                 smem_desc(q + boff, C::kQColBlk, C::kSbo, C::kSw), idKV, acc);
+        }
+        if (s > 0 && !(ok = mbar_wait(&bars->dq_free, (s - 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // dQ partial: contraction over the 128 keys, both operands MN-major
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks) {
+          const uint32_t kb_off = ks * 16 * C::kRowBytes;   // 16 key rows of the K tile
+          const uint32_t ds_off = ks * 16 * 128;            // 16 key rows of dS^T
+          if (C::kDqT) {
+            mma_ss(tmem + C::kTdQ, smem_desc(sK + kb_off, C::kKColBlk, C::kSbo, C::kSw),
+                   smem_desc(sDST + ds_off, C::kPColBlk, 1024, kSwizzle128B), idQ, ks > 0);
+          } else {
+            mma_ss(tmem + C::kTdQ, smem_desc(sDST + ds_off, C::kPColBlk, 1024, kSwizzle128B),
+                   smem_desc(sK + kb_off, C::kKColBlk, C::kSbo, C::kSw), idQ, ks > 0);
+          }
+        }
+        mma_commit(&bars->dq_full);
+        mma_commit(&bars->empty[stage]);
+      }
+      mma_commit(&bars->kv_done);
+      mma_commit(&bars->done);
+      mbar_wait_drain(&bars->done, 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------ P^T and dS^T, then dV
+    const int r = threadIdx.x & 127;                         // key row == TMEM lane
+    const int key = key0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c = p.scale * kLog2e;
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      const int stage = s & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s, s & 1, abort_flag, p.status) &&
+                                       mbar_wait(&bars->full[stage], (s >> 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = (i0 + s) * BQ;
+      const float* lse2 = stat + stage * 2 * BQ;
+      const float* dl = lse2 + BQ;
+      const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
+#pragma unroll 1
+      for (int cc = 0; cc < BQ / 32; ++cc) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tmem + lane_off + C::kTS + cc * 32, sv);
+        tmem_ld32(tmem + lane_off + C::kTdP + cc * 32, dv);
+        tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pr[2], ds[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = cc * 32 + 2 * e + h;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h]), c, -lse2[col]));
+            if (need_mask && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
+            pr[h] = pv;
+            ds[h] = pv * (__uint_as_float(dv[2 * e + h]) - dl[col]);
+          }
+          pk[e] = Pack2<T>::pack(pr[0], pr[1]);
+          dk[e] = Pack2<T>::pack(ds[0], ds[1]);
+        }
+        // [key row][query] in 128-byte swizzled rows, 64 queries per column block
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int chunk = cc * 4 + ch;           // 8-query chunk index
+          const uint32_t off = (chunk / 8) * C::kPColBlk + r * 128 + (((chunk % 8) ^ (r & 7)) << 4);
+          st_shared_v4(sPT + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          st_shared_v4(sDST + off, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_done, 0, abort_flag, p.status));
+    if (ok) {
+      tc_fence_after();
+      T* dvrow = static_cast<T*>(bp.dv) + (static_cast<long long>(unit) * Lk + key) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + C::kTdV + cc * 32, o);
+        tmem_ld_wait();
+        if (nsteps == 0) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (key < Lk) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = Pack2<T>::pack(__uint_as_float(o[8 * e + 0]), __uint_as_float(o[8 * e + 1]));
+            w.y = Pack2<T>::pack(__uint_as_float(o[8 * e + 2]), __uint_as_float(o[8 * e + 3]));
+            w.z = Pack2<T>::pack(__uint_as_float(o[8 * e + 4]), __uint_as_float(o[8 * e + 5]));
+            w.w = Pack2<T>::pack(__uint_as_float(o[8 * e + 6]), __uint_as_float(o[8 * e + 7]));
+            *reinterpret_cast<uint4*>(dvrow + cc * 32 + 8 * e) = w;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ dQ drain, then dK
+    const int r = threadIdx.x & 127;                          // TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float* dq_unit = bp.dq_acc + static_cast<long long>(unit) * Lq * D;
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, s & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = (i0 + s) * BQ;
+      if (r == 0) bulk_wait_read0();          // the previous reduce has read the staging tile
+      named_bar_sync(1, 128);
+      if (C::kDqT) {
+        // lane r = head dim r; columns = BQ queries -> staging [query][D]
+#pragma unroll 1
+        for (int cc = 0; cc < BQ / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + C::kTdQ + cc * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) st_shared_f32(sDQ + ((cc * 32 + e) * D + r) * 4, __uint_as_float(o[e]));
+        }
+      } else {
+        // lane r = query row r; columns = D -> staging [query][D]
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + C::kTdQ + cc * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            st_shared_v4(sDQ + (r * D + cc * 32 + e * 4) * 4, o[e * 4], o[e * 4 + 1], o[e * 4 + 2], o[e * 4 + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (r == 0) {
+        const int rows = min(BQ, Lq - q0);
+        bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0) * D, sDQ, static_cast<uint32_t>(rows * D * 4));
+        bulk_commit();
+      }
+    }
+    if (r == 0) bulk_wait0();
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_done, 0, abort_flag, p.status));
+    if (ok) {
+      tc_fence_after();
+      const int key = key0 + r;
+      T* dkrow = static_cast<T*>(bp.dk) + (static_cast<long long>(unit) * Lk + key) * D;
+      const float sc = p.scale;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + C::kTdK + cc * 32, o);
+        tmem_ld_wait();
+        if (nsteps == 0) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (key < Lk) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = Pack2<T>::pack(__uint_as_float(o[8 * e + 0]) * sc, __uint_as_float(o[8 * e + 1]) * sc);
+            w.y = Pack2<T>::pack(__uint_as_float(o[8 * e + 2]) * sc, __uint_as_float(o[8 * e + 3]) * sc);
+            w.z = Pack2<T>::pack(__uint_as_float(o[8 * e + 4]) * sc, __uint_as_float(o[8 * e + 5]) * sc);
+            w.w = Pack2<T>::pack(__uint_as_float(o[8 * e + 6]) * sc, __uint_as_float(o[8 * e + 7]) * sc);
+            *reinterpret_cast<uint4*>(dkrow + cc * 32 + 8 * e) = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, typename T, bool CAUSAL>
+cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
+  auto kern = bwd_tc_kernel<D, T, CAUSAL>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  const Problem& p = bp.f;
+  const long long blocks = static_cast<long long>((p.Lk + BK - 1) / BK) * p.B * p.H;
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(blocks), kThreads, BCfg<D>::kSmem, s>>>(bp, m.q, m.k, m.v, m.dO);
+  return cudaGetLastError();
+}
+
+template <int D, typename T>
+cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
+  return bp.f.causal ? launch_one<D, T, true>(bp, m, s) : launch_one<D, T, false>(bp, m, s);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdProblem& bp, int dtype, const BwdMaps& m, cudaStream_t s) {
+  if (bp.f.cu_seqlens != nullptr) return cudaErrorNotSupported;
+  if (dtype == kF16) {
+    if (bp.f.d == 64) return launch_d<64, __half>(bp, m, s);
+    if (bp.f.d == 128) return launch_d<128, __half>(bp, m, s);
+  } else if (dtype == kBF16) {
+    if (bp.f.d == 64) return launch_d<64, __nv_bfloat16>(bp, m, s);
+    if (bp.f.d == 128) return launch_d<128, __nv_bfloat16>(bp, m, s);
+  }
+  return cudaErrorNotSupported;
+}
+
 }  // namespace sdpa
