@@ -1,0 +1,505 @@
+"""Benchmark of the GB300 exact-attention library.
+
+``python bench.py --gpus N --steps K --warmup W`` (N > 1 under torchrun) prints
+one JSON line. A step is one pass of the measured workload -- by default the
+dense fp16 forward the SDPA tutorial's dispatcher benchmark uses (B=32, H=32,
+L=1024, d=32, torch.rand inputs, non-causal) -- through the library's C ABI.
+Device time is taken with CUDA events on the launching stream, with L2
+flushed (a 256 MiB write) before every timed step; ``e2e`` repeats the same
+steps with the inputs copied in from pinned host memory and the outputs
+copied back inside the timed region. Every rank runs its own replica (the
+work per GPU is fixed: weak scaling); rank 0 prints the aggregate.
+
+The same line carries the roofline of the dominant kernel, the fp64 CPU
+oracle timed on a bounded sample on the host cores, SM clocks sampled during
+the timed region, and (N = 1, rank 0) per-workload results for all five
+workloads (forward and backward TFLOP/s, microseconds per call, fraction of
+the measured tensor peak).
+
+``--impl reference`` times the oracle itself on the host cores (each step a
+bounded sample of the same workload) and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SDPA fwd/bwd TFLOP/s and µs/call at 1 GB300; fraction of dense fp16/bf16 peak"
+HEADLINE = "dense_f16_d32"
+# The tutorial's own number for this exact workload (flash backend, 2262.901 us,
+# hardware not stated) expressed in the same unit: 4*B*H*L*L*d / t.
+PAGES_TFLOPS = 4.0 * 32 * 32 * 1024 * 1024 * 32 / 2262.901e-6 / 1e12
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read only) in a
+    background thread; falls back to one nvidia-smi query if NVML is absent."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle",
+               0x2: "applications_clocks_setting", 0x10: "sync_boost"}
+
+    def __init__(self, index=0, period=0.005):
+        self.index, self.period = index, period
+        self.samples, self.reasons = [], 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) == 0:
+                    self._nvml, self._h = nv, h
+                    mx = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                        self.max_mhz = mx.value
+                    self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                        getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            self._nvml = None
+
+    def _sample_nvml(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+            self.samples.append(clk.value)
+        if self._reason_fn(self._h, ctypes.byref(rs)) == 0:
+            self.reasons |= rs.value
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self._sample_nvml()
+            except Exception:
+                return
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._sample_nvml()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def stop(self):
+        if self._nvml is not None:
+            self._stop.set()
+            self._t.join()
+            self._sample_nvml()
+        else:
+            self._smi_once()
+        names = sorted(n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle")
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+    def _smi_once(self):
+        import subprocess
+        try:
+            out = subprocess.run(["nvidia-smi", f"--id={self.index}", "--query-gpu=clocks.sm,clocks.max.sm",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20).stdout
+            a, b = out.strip().split(",")[:2]
+            self.samples.append(float(a))
+            self.max_mhz = float(b)
+        except Exception:
+            pass
+
+
+# --------------------------------------------------------------- helpers
+def kernel_source_hash(name):
+    """Short hash of a kernel's source (its .cu plus the shared device headers)."""
+    csrc = os.path.join(ROOT, "exact_attention_softmax_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted([name, "ptx.cuh", "common.cuh"]):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    prof = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof):
+        return None
+    want = kernel_source_hash(kernel_file)
+    for fn in sorted(os.listdir(prof)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(prof, fn)).read()
+        for m in re.finditer(r"traffic_per_launch:\s*workload=(\S+)\s+bytes=(\d+)\s+source=(\w+)", text):
+            if m.group(1) == workload and m.group(3) == want:
+                return int(m.group(2))
+    return None
+
+
+def oracle_sample(w, x, budget_s, max_units=None):
+    """Time the fp64 oracle (as it stands) on whole units of the workload until
+    ``budget_s`` seconds of CPU work; returns (flops, seconds, description)."""
+    import numpy as np
+    from oracle import attn_fwd_unit
+    done_flops, t_total, n = 0.0, 0.0, 0
+    if w.varlen:
+        cu = x["cu_seqlens"].numpy()
+        units = [("s", s, h) for s in range(w.nseq) for h in range(w.H)]
+    else:
+        units = [("d", b, h) for b in range(w.B) for h in range(w.H)]
+    order = np.random.default_rng(0).permutation(len(units))
+    for idx in order:
+        kind, a, h = units[idx]
+        if kind == "s":
+            lo, hi = int(cu[a]), int(cu[a + 1])
+            q, k, v = (x[t][lo:hi, h].double().numpy() for t in ("q", "k", "v"))
+            f = 4.0 * w.d * (hi - lo) ** 2 * (0.5 if w.causal else 1.0)
+        else:
+            q, k, v = (x[t][a, h].double().numpy() for t in ("q", "k", "v"))
+            f = 4.0 * w.d * w.Lq * w.Lk * (0.5 if w.causal else 1.0)
+        t0 = time.perf_counter()
+        attn_fwd_unit(q, k, v, w.scale, w.causal)
+        t_total += time.perf_counter() - t0
+        done_flops += f
+        n += 1
+        if t_total >= budget_s or (max_units and n >= max_units):
+            break
+    desc = f"{n} of {len(units)} (unit, head) slices of {w.name}, forward, fp64 NumPy"
+    return done_flops, t_total, desc
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- our arm
+class Runner:
+    """Holds device inputs/outputs of one workload and runs its calls."""
+
+    def __init__(self, w, x, dev, with_bwd):
+        import torch
+        import exact_attention_softmax_gb300 as ops
+        self.ops, self.w, self.dev = ops, w, dev
+        self.q, self.k, self.v = (x[n].to(dev) for n in ("q", "k", "v"))
+        self.kw = {}
+        if w.varlen:
+            self.kw = dict(cu_seqlens=x["cu_seqlens"].to(dev), max_seqlen=x["max_seqlen"])
+        self.o = torch.empty_like(self.q)
+        lshape = (w.H, self.q.shape[0]) if w.varlen else tuple(self.q.shape[:-1])
+        self.lse = torch.empty(lshape, dtype=torch.float32, device=dev)
+        self.with_bwd = with_bwd
+        if with_bwd:
+            self.do = x["do"].to(dev)
+            self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+            code = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[self.q.dtype]
+            n = ops.sdpa_bwd_workspace_size(self.q.shape[0], w.H, self.q.shape[2], w.d, code)
+            self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+
+    def fwd(self):
+        self.ops.sdpa_fwd(self.q, self.k, self.v, self.o, self.lse, scale=self.w.scale,
+                          is_causal=self.w.causal, **self.kw)
+
+    def bwd(self):
+        self.ops.sdpa_bwd(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv,
+                          scale=self.w.scale, is_causal=self.w.causal, workspace=self.ws)
+
+
+def time_calls(fn, iters, flush, stream):
+    """Per-call device times (ms) with an L2 flush before each call."""
+    import torch
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ts]
+
+
+def per_workload_results(dev, flush, peaks, peak_kind):
+    """Forward (and backward) timings of all five workloads (N = 1 only)."""
+    import torch
+    from exact_attention_softmax_gb300 import workloads as wl
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for name, w in wl.WORKLOADS.items():
+        x = wl.workload_inputs(w, seed=0)
+        r = Runner(w, x, dev, w.bwd)
+        lengths = x.get("lengths")
+        ff = wl.fwd_flops(w, lengths)
+        iters = 5 if name == "long_causal_bf16_d128" else 20
+        for _ in range(3):
+            r.fwd()
+            if w.bwd:
+                r.bwd()
+        torch.cuda.synchronize()
+        tf = time_calls(r.fwd, iters, flush, stream)
+        res = {"fwd_us": 1e3 * statistics.median(tf), "fwd_us_min": 1e3 * min(tf)}
+        res["fwd_tflops"] = ff / (res["fwd_us"] * 1e-6) / 1e12
+        res["fwd_frac_of_peak"] = res["fwd_tflops"] / peaks["bf16_tflops"] if w.dtype != "f32" else None
+        if name == "dense_f16_d32":
+            min_bytes = 2 * 4 * w.B * w.H * w.Lq * w.d + 4 * w.B * w.H * w.Lq
+            res["fwd_hbm_gbs"] = min_bytes / (res["fwd_us"] * 1e-6) / 1e9
+            res["fwd_frac_of_hbm"] = res["fwd_hbm_gbs"] / peaks["hbm_gbs"]
+        if w.bwd:
+            tb = time_calls(r.bwd, iters, flush, stream)
+            bf = wl.bwd_flops(w, lengths)
+            res["bwd_us"] = 1e3 * statistics.median(tb)
+            res["bwd_tflops"] = bf / (res["bwd_us"] * 1e-6) / 1e12
+            res["bwd_frac_of_peak"] = res["bwd_tflops"] / peaks["bf16_tflops"] if w.dtype != "f32" else None
+        res["fwd_gflop"] = ff / 1e9
+        res["peak"] = f"{peak_kind} bf16 dense {peaks['bf16_tflops']:.1f} TFLOP/s"
+        out[name] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in res.items()}
+        del r, x
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from exact_attention_softmax_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import exact_attention_softmax_gb300 as ops
+    ops._abi.load()
+
+    peaks, peak_kind = load_peaks()
+    w = wl.WORKLOADS[args.workload]
+    x = wl.workload_inputs(w, seed=rank)
+    lengths = x.get("lengths")
+    do_fwd = args.passes in ("fwd", "both")
+    do_bwd = args.passes in ("bwd", "both")
+    if do_bwd and not w.bwd:
+        raise SystemExit(f"workload {w.name} has no backward")
+    flops = (wl.fwd_flops(w, lengths) if do_fwd else 0.0) + (wl.bwd_flops(w, lengths) if do_bwd else 0.0)
+    r = Runner(w, x, dev, with_bwd=do_bwd)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = (1 if do_fwd else 0) + (3 if do_bwd else 0)
+
+    def step():
+        if do_fwd:
+            r.fwd()
+        if do_bwd:
+            r.bwd()
+
+    r.fwd()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    ops.sdpa_device_status()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    clocks = ClockSampler(local).start()
+    barrier()
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        evs.append((a, b))
+    barrier()
+    clk = clocks.stop()
+    kernel_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(kernel_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ops.sdpa_device_status()
+
+    # ---- end to end: pinned host inputs in, outputs out, inside the timed region
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.empty(r.o.shape, dtype=r.o.dtype).pin_memory()
+    hl = torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    if w.varlen:
+        h2d += x["cu_seqlens"].numel() * 4
+    d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+    if do_bwd:
+        hd = x["do"].pin_memory()
+        hg = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (r.dq, r.dk, r.dv)]
+        h2d += hd.numel() * hd.element_size()
+        d2h += sum(t.numel() * t.element_size() for t in hg)
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        r.q.copy_(hq, non_blocking=True)
+        r.k.copy_(hk, non_blocking=True)
+        r.v.copy_(hv, non_blocking=True)
+        if do_bwd:
+            r.do.copy_(hd, non_blocking=True)
+        r.fwd()
+        if do_bwd:
+            r.bwd()
+            for h, g in zip(hg, (r.dq, r.dk, r.dv)):
+                h.copy_(g, non_blocking=True)
+        ho.copy_(r.o, non_blocking=True)
+        hl.copy_(r.lse, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    barrier()
+    e2e_ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    # the end-to-end step always runs the forward (the backward needs its O and LSE)
+    e2e_flops = flops + (wl.fwd_flops(w, lengths) if not do_fwd else 0.0)
+    e2e_value = world * e2e_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    avg_kernel_s = statistics.mean(kernel_ms) * 1e-3
+    kern_file = "fwd_tc.cu" if do_fwd and not do_bwd else "bwd_tc.cu"
+    kern_name = "fwd_tc_kernel" if kern_file == "fwd_tc.cu" else "bwd_tc_kernel"
+    achieved = flops / avg_kernel_s / 1e12
+    traffic = profiled_traffic(kern_file, args.workload)
+    shape = (f"B={w.B} H={w.H} Lq={w.Lq} Lk={w.Lk} d={w.d}" if not w.varlen else
+             f"{w.nseq} packed sequences (max {w.max_len}, total {x['q'].shape[0]}) H={w.H} d={w.d}")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "us_per_call": round(1e3 * total_ms / args.steps, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (round(value / world / PAGES_TFLOPS, 3)
+                        if args.workload == HEADLINE and args.passes == "fwd" else None),
+        "dtype": w.dtype,
+        "data": "synthetic (seeded torch.rand / torch.randn of the workload's shape)",
+        "config": {"workload": f"{w.name}: {shape} {w.dtype} {w.dist} "
+                               f"{'causal' if w.causal else 'non-causal'} {args.passes}",
+                   "flops_per_step": flops, "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas x{world} (one independent problem per GPU)"},
+        "roofline": {"kernel": kern_name, "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "peak_source": f"{peak_kind} dense bf16 burst (fp16 has the same tensor rate)",
+                     "traffic": traffic},
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, s, desc = oracle_sample(w, x, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
+                                "kind": "oracle", "sample": desc + f", {s:.1f} s"}
+    if rank == 0 and world == 1 and not args.no_extras:
+        line["per_workload"] = per_workload_results(dev, flush, peaks, peak_kind)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 oracle, as it stands, on the host cores; each step is a bounded
+    sample of the workload (whole (batch, head) slices)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from exact_attention_softmax_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    x = wl.workload_inputs(w, seed=0)
+    per_step_units = 2
+    for _ in range(args.warmup):
+        oracle_sample(w, x, budget_s=0.0, max_units=1)
+    flops = secs = 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, s, desc = oracle_sample(w, x, budget_s=1e9, max_units=per_step_units)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample_per_step": desc},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": host_cores(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--pass", dest="passes", choices=["fwd", "bwd", "both"], default="fwd",
+                    help="what one step runs (the headline workload is a forward-only workload)")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
