@@ -107,9 +107,12 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   BBars* bars = reinterpret_cast<BBars*>(smem + C::kOffBar);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  const int units = p.B * p.H;
-  const int unit = blockIdx.x % units;
-  const int kblk = blockIdx.x / units;
+  // Unit-major order: the key blocks of one (batch, head) run side by side and
+  // share its Q / dO through L2; under causal masking key block 0 (the most
+  // query tiles) goes first.
+  const int nkb = (p.Lk + BK - 1) / BK;
+  const int unit = blockIdx.x / nkb;
+  const int kblk = blockIdx.x % nkb;
   const int key0 = kblk * BK;
   const int Lq = p.Lq, Lk = p.Lk;
   const int nq = (Lq + BQ - 1) / BQ;

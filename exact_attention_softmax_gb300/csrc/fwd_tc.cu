@@ -93,10 +93,11 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   int unit, pair, len_q, len_k, tok0 = 0, h = 0;
   {
-    const int units = PACKED ? p.H * p.B : p.H * p.B;
+    // Unit-major order: the CTAs of one (batch|sequence, head) run side by side
+    // and share its K/V through L2; under causal masking the longest rows go first.
     const int npairs = ((PACKED ? p.Lk : p.Lq) + 2 * BM - 1) / (2 * BM);
-    unit = blockIdx.x % units;
-    const int ord = blockIdx.x / units;
+    unit = blockIdx.x / npairs;
+    const int ord = blockIdx.x % npairs;
     pair = CAUSAL ? (npairs - 1 - ord) : ord;
     if (PACKED) {
       const int s = unit / p.H;
