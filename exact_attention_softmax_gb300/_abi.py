@@ -28,6 +28,8 @@ SIGNATURES = {
     "sdpa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "sdpa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                       _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
+    "sdpa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                              _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "sdpa_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "sdpa_debug_set": (_i, [_i]),
     "sdpa_last_error": (ctypes.c_char_p, []),

@@ -125,6 +125,17 @@ int check_common(const void* q, const void* k, const void* v, const void* o, con
 }
 
 }  // namespace
+
+int set_last_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
 }  // namespace sdpa
 
 using namespace sdpa;

@@ -52,6 +52,9 @@ struct BwdMaps {
   CUtensorMap q, k, v, dO;
 };
 
+// Records the message sdpa_last_error() returns on this thread; returns `code`.
+int set_last_error(int code, const char* fmt, ...);
+
 // Launchers (each in its own translation unit).
 cudaError_t launch_fwd_simt(const Problem& p, cudaStream_t s);
 cudaError_t launch_bwd_simt(const BwdProblem& p, cudaStream_t s);

@@ -109,6 +109,29 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass for callers that cannot allocate device memory: it takes the
+ * same arguments as sdpa_bwd except the workspace and cu_seqlens (dense
+ * layout only), and uses a scratch array of 16 MiB compiled into the library
+ * instead. The pages have no counterpart to this call; it exists because some
+ * callers run where no allocation is possible -- a pre-sized memory pool that
+ * must not grow, a plugin or embedded runtime that is handed only its input
+ * and output buffers, a host that forbids cudaMalloc after start-up.
+ *   Limit: sdpa_bwd_workspace_size(B, H, Lq, d, dtype) must not exceed
+ *   16 MiB (B*H*Lq*(d+1)*4 bytes, rounded, for fp16/bf16); larger problems
+ *   return SDPA_ERR_WORKSPACE before anything is launched.
+ *   The first call on each device looks up the array's device address while
+ *   that device is current; make that first call before any stream capture.
+ *   Every call on a device shares the one array (it is held until the process
+ *   exits and keeps the last call's contents; each call re-initialises what it
+ *   needs), so calls whose kernels may overlap on the GPU race and must be
+ *   ordered by the caller (same stream, or events). No call allocates.
+ */
+int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv,
+                     int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                     int dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device. Returns SDPA_OK, SDPA_ERR_TIMEOUT (bit SDPA_STATUS_TIMEOUT
  * was set), SDPA_ERR_ARG (bit SDPA_STATUS_SEQLEN was set) or SDPA_ERR_CUDA.
