@@ -18,8 +18,11 @@
 //               LSE = (m + log2 l) ln 2.
 //
 // The two tiles alternate on the tensor cores: while one softmax group works
-// on its tile, the MMAs of the other tile run. TMEM columns: S_0 [0,128),
-// S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+// on its tile, the MMAs of the other tile run. A softmax group releases S_t as
+// soon as it holds the row in registers, so Q_t K_{j+1}^T runs under its
+// exponentials; P is double-buffered in shared memory for d <= 64, and O is
+// rescaled only when a row maximum grows past a threshold. TMEM columns:
+// S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -35,6 +38,10 @@ constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// The running maximum used in the exponent is only raised when a row's new
+// maximum exceeds it by more than this (log2 units), so P <= 2^8 and O is
+// rescaled rarely; the result is the same because O and l share the maximum.
+constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
 struct Cfg {
@@ -45,22 +52,31 @@ struct Cfg {
   static constexpr int kSbo = 8 * kRowBytes;                  // 8-row group stride
   static constexpr int kColBlkBytes = 128 * kRowBytes;        // one column block of a 128-row tile
   static constexpr int kTileBytes = 128 * D * 2;              // a Q, K or V tile
-  static constexpr int kPBytes = BM * BN * 2;                 // a P tile (two 64-key blocks)
-  static constexpr int kSlots = D == 128 ? 3 : (D == 64 ? 6 : 8);
+  static constexpr int kSlots = D == 128 ? 5 : (D == 64 ? 12 : 16);
   static constexpr int kOffQ = 0;
   static constexpr int kOffSlots = 2 * kTileBytes;
-  static constexpr int kOffP = kOffSlots + kSlots * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffSlots + kSlots * kTileBytes;
   static constexpr int kSmem = kOffBar + 512 + 1024;          // barriers + alignment slack
+  static_assert(kSmem <= 232448, "shared memory budget");
+  // TMEM columns. P (BN fp16/bf16 per row, two per 32-bit column) has its own
+  // columns when they fit; at d = 128 it overlays the upper half of S_t, which
+  // is dead once the softmax group holds S_t in registers.
+  static constexpr bool kPAlias = D == 128;
+  static constexpr uint32_t kColS = 0;                        // + t * BN
+  static constexpr uint32_t kColO = 2 * BN;                   // + t * D
+  static constexpr uint32_t kColP = kPAlias ? BN / 2 : 2 * BN + 2 * D;   // + t * (kPAlias ? BN : BN / 2)
+  static constexpr uint32_t kPStride = kPAlias ? BN : BN / 2;
+  static_assert(kPAlias || kColP + 2 * (BN / 2) <= 512, "TMEM budget");
 };
 
 struct __align__(8) Bars {
   uint64_t q;
-  uint64_t full[8];
-  uint64_t empty[8];
-  uint64_t s[2];
-  uint64_t p[2];
-  uint64_t o[2];
+  uint64_t full[16];
+  uint64_t empty[16];
+  uint64_t s_full[2];     // S_t written by the tensor cores
+  uint64_t s_free[2];     // S_t read into registers by its softmax group
+  uint64_t p_full[2];     // P_t in TMEM (and O_t rescaled)
+  uint64_t pv_done[2];    // O_t += P_t V_j finished
   uint64_t done;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -68,6 +84,27 @@ struct __align__(8) Bars {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+// (a0, a1) * (c, c) + (b, b) as one packed fp32x2 FMA.
+__device__ __forceinline__ void fma2(float& o0, float& o1, float a0, float a1, float c, float b) {
+  uint64_t x, y, z, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(c));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(z) : "f"(b));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o0), "=f"(o1) : "l"(r));
+}
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  uint64_t x, y, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(a0), "f"(a1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(r));
 }
 
 // Number of K/V blocks tile rows [r, r+128) need.
@@ -104,7 +141,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       h = unit % p.H;
       tok0 = p.cu_seqlens[s];
       len_q = len_k = p.cu_seqlens[s + 1] - tok0;
-      if (len_q > p.Lk && pair == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+      if (len_q > p.Lk && ord == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
     } else {
       len_q = p.Lq;
       len_k = p.Lk;
@@ -118,7 +155,6 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
 
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sSlots = smem_u32(smem + C::kOffSlots);
-  const uint32_t sP = smem_u32(smem + C::kOffP);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q, 1);
@@ -127,9 +163,10 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       mbar_init(&bars->empty[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->s[t], 1);
-      mbar_init(&bars->p[t], BM);
-      mbar_init(&bars->o[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->s_free[t], BM);
+      mbar_init(&bars->p_full[t], BM);
+      mbar_init(&bars->pv_done[t], 1);
     }
     mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
@@ -142,8 +179,15 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
   volatile uint32_t* abort_flag = &bars->abort_flag;
+  // All 512 columns are allocated, so the allocation starts at lane 0, column
+  // 0; the constant keeps TMEM addresses compile-time known. Anything else is
+  // reported as a failed wait and the CTA drains.
+  constexpr uint32_t tmem = 0;
+  if (bars->tmem_base != 0u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusTimeout);
+    *abort_flag = 1u;
+  }
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -153,7 +197,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       tma_prefetch_desc(&tmV);
       auto c1 = [&](int row) { return PACKED ? h : row; };
       auto c2 = [&](int row) { return PACKED ? tok0 + row : unit; };
-      if (!(p.debug & kDebugDropQArrive)) {
+      if (!(p.debug & kDebugDropQArrive) && !*abort_flag) {
         const uint32_t qbytes = (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0);
         mbar_expect_tx(&bars->q, qbytes);
         for (int t = 0; t < 2; ++t) {
@@ -164,6 +208,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
                         cb * C::kBlk, c1(row), c2(row));
         }
       }
+      // ring order: K_0, V_0, K_1, V_1, ...
       int it = 0;
       for (int j = 0; j < nmax && !*abort_flag; ++j) {
         for (int kv = 0; kv < 2; ++kv, ++it) {
@@ -186,74 +231,77 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
-      constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BM, BN);
-      constexpr uint32_t idO = idesc_f16(fmt, 0, 1, BM, D);
-      auto issue_qk = [&](int t, int slot) {
-        const uint32_t qa = sQ + t * C::kTileBytes;
-        const uint32_t kb = sSlots + slot * C::kTileBytes;
+    // The whole warp runs this loop with warp-uniform operands; lane 0 issues.
+    const uint32_t leader = lane == 0 ? 1u : 0u;
+    constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
+    constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BM, BN);
+    constexpr uint32_t idO = idesc_f16(fmt, 0, 1, BM, D);
+    // descriptors of the operand tiles; advancing the start address by `off`
+    // bytes adds off >> 4 to the descriptor (the address field cannot carry)
+    const uint64_t dQ0 = smem_desc(sQ, 16, C::kSbo, C::kSw);
+    const uint64_t dSlot0K = smem_desc(sSlots, 16, C::kSbo, C::kSw);
+    const uint64_t dSlot0V = smem_desc(sSlots, C::kColBlkBytes, C::kSbo, C::kSw);
+    auto issue_qk = [&](int t, int slot) {
+      const uint64_t a = dQ0 + ((t * C::kTileBytes) >> 4);
+      const uint64_t b = dSlot0K + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks * 16 / C::kBlk) * C::kColBlkBytes + (ks * 16 % C::kBlk) * 2;
-          mma_ss(tmem + t * BN, smem_desc(qa + off, 16, C::kSbo, C::kSw), smem_desc(kb + off, 16, C::kSbo, C::kSw),
-                 idS, ks > 0);
-        }
-      };
-      auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t pa = sP + t * C::kPBytes;
-        const uint32_t vb = sSlots + slot * C::kTileBytes;
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = ((ks * 16 / C::kBlk) * C::kColBlkBytes + (ks * 16 % C::kBlk) * 2) >> 4;
+        mma_ss_p(tmem + C::kColS + t * BN, a + off, b + off, idS, ks > 0, leader);
+      }
+    };
+    auto issue_pv = [&](int t, int slot, bool acc) {
+      const uint64_t b = dSlot0V + ((slot * C::kTileBytes) >> 4);
+      const uint32_t a = tmem + C::kColP + t * C::kPStride;
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t a = smem_desc(pa + (ks / 4) * (BM * 128) + (ks % 4) * 32, 16, 1024, kSwizzle128B);
-          const uint64_t b = smem_desc(vb + ks * 16 * C::kRowBytes, C::kColBlkBytes, C::kSbo, C::kSw);
-          mma_ss(tmem + 2 * BN + t * D, a, b, idO, (acc || ks > 0) ? 1u : 0u);
-        }
-      };
-      int it = 0;
-      bool ok = mbar_wait(&bars->q, 0, abort_flag, p.status);
-      if (ok) {
-        const int slot = it % C::kSlots;
-        ok = mbar_wait(&bars->full[slot], (it / C::kSlots) & 1, abort_flag, p.status);
-        if (ok) {
-          tc_fence_after();
-          if (n0 > 0) { issue_qk(0, slot); mma_commit(&bars->s[0]); }
-          if (n1 > 0) { issue_qk(1, slot); mma_commit(&bars->s[1]); }
-          mma_commit(&bars->empty[slot]);
-          ++it;
-        }
+      for (int ks = 0; ks < BN / 16; ++ks) {
+        const uint32_t boff = (ks * 16 * C::kRowBytes) >> 4;
+        mma_ts_p(tmem + C::kColO + t * D, a + ks * 8, b + boff, idO, (acc || ks > 0) ? 1u : 0u, leader);
       }
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int vslot = it % C::kSlots;
-        if (!(ok = mbar_wait(&bars->full[vslot], (it / C::kSlots) & 1, abort_flag, p.status))) break;
-        ++it;
-        const bool has_next = j + 1 < nmax;
-        int kslot = 0;
-        if (has_next) {
-          kslot = it % C::kSlots;
-          if (!(ok = mbar_wait(&bars->full[kslot], (it / C::kSlots) & 1, abort_flag, p.status))) break;
-          ++it;
-        }
-        tc_fence_after();
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int nt = t == 0 ? n0 : n1;
-          if (j >= nt) continue;
-          if (!(ok = mbar_wait(&bars->p[t], j & 1, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_pv(t, vslot, j > 0);
-          if (j == nt - 1) {
-            mma_commit(&bars->o[t]);
-          } else {
-            issue_qk(t, kslot);
-            mma_commit(&bars->s[t]);
-          }
-        }
-        mma_commit(&bars->empty[vslot]);
-        if (has_next) mma_commit(&bars->empty[kslot]);
-      }
-      mma_commit(&bars->done);
-      mbar_wait_drain(&bars->done, 0);
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+    };
+    auto full_wait = [&](int pos) { return wait_all(&bars->full[pos % C::kSlots], (pos / C::kSlots) & 1); };
+    bool ok = wait_all(&bars->q, 0) && full_wait(0);
+    if (ok) {
+      tc_fence_after();
+      if (n0 > 0) { issue_qk(0, 0); mma_commit_p(&bars->s_full[0], leader); }
+      if (n1 > 0) { issue_qk(1, 0); mma_commit_p(&bars->s_full[1], leader); }
+      mma_commit_p(&bars->empty[0], leader);
     }
+    for (int j = 0; j < nmax && ok; ++j) {
+      // K_{j+1} sits at ring position 2j+2, V_j at 2j+1
+      const bool has_next = j + 1 < nmax;
+      const int kpos = 2 * j + 2, vpos = 2 * j + 1;
+      if (has_next && !(ok = full_wait(kpos))) break;
+      if (!(ok = full_wait(vpos))) break;
+      tc_fence_after();
+      for (int t = 0; t < 2 && ok; ++t) {
+        const int nt = t == 0 ? n0 : n1;
+        if (j >= nt) continue;
+        if (!C::kPAlias && j + 1 < nt) {
+          // S_t may be overwritten once its softmax group holds it in registers
+          if (!(ok = wait_all(&bars->s_free[t], j & 1))) break;
+          tc_fence_after();
+          issue_qk(t, kpos % C::kSlots);
+          mma_commit_p(&bars->s_full[t], leader);
+        }
+        if (!(ok = wait_all(&bars->p_full[t], j & 1))) break;
+        tc_fence_after();
+        issue_pv(t, vpos % C::kSlots, j > 0);
+        mma_commit_p(&bars->pv_done[t], leader);
+        if (C::kPAlias && j + 1 < nt) {
+          // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
+          issue_qk(t, kpos % C::kSlots);
+          mma_commit_p(&bars->s_full[t], leader);
+        }
+      }
+      mma_commit_p(&bars->empty[vpos % C::kSlots], leader);
+      if (has_next) mma_commit_p(&bars->empty[kpos % C::kSlots], leader);
+    }
+    mma_commit_p(&bars->done, leader);
+    mbar_wait_drain(&bars->done, 0);
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp / 4;
@@ -262,16 +310,18 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     const int rl = threadIdx.x & 127;        // row within the tile == TMEM lane
     const int row = rt + rl;                  // row within the unit
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + t * BN;
-    const uint32_t tO = tmem + lane_off + 2 * BN + t * D;
-    const uint32_t pRow = sP + t * C::kPBytes + rl * 128;
+    const uint32_t tS = tmem + lane_off + C::kColS + t * BN;
+    const uint32_t tO = tmem + lane_off + C::kColO + t * D;
+    const uint32_t tP = tmem + lane_off + C::kColP + t * C::kPStride;
     const float c = p.scale * kLog2e;
-    float m = -INFINITY, l = 0.f;
+    float m_run = -INFINITY, l = 0.f;        // maximum used in the exponent (base 2), running sum
     bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      // warp-uniform decision: the TMEM accesses that follow are warp-collective
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
+    };
     for (int j = 0; j < nt; ++j) {
-      // warp-uniform decision: the TMEM loads below are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s[t], j & 1, abort_flag, p.status));
-      if (!ok) break;
+      if (!(ok = wait_all(&bars->s_full[t], j & 1))) break;
       tc_fence_after();
       uint32_t sr[BN];
       tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -279,55 +329,87 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
       tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
       tmem_ld_wait();
+      if (!C::kPAlias) {
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[t]);
+      }
       float* x = reinterpret_cast<float*>(sr);
       const int kbase = j * BN;
-      const bool need_mask = (kbase + BN > len_k) || (CAUSAL && kbase + BN - 1 > rt);
-      if (need_mask) {
+      if ((kbase + BN > len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
 #pragma unroll
         for (int i = 0; i < BN; ++i) {
           const int key = kbase + i;
           if (key >= len_k || (CAUSAL && key > row)) x[i] = -INFINITY;
         }
       }
-      float mx = x[0];
+      // row maximum: four independent chains of three-input max
+      float mx0 = max3f(x[0], x[1], x[2]), mx1 = max3f(x[3], x[4], x[5]);
+      float mx2 = max3f(x[6], x[7], x[8]), mx3 = max3f(x[9], x[10], x[11]);
 #pragma unroll
-      for (int i = 1; i < BN; ++i) mx = fmaxf(mx, x[i]);
-      const float m_new = fmaxf(m, mx * c);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);
-      float sum = 0.f;
-#pragma unroll
-      for (int chunk = 0; chunk < BN / 8; ++chunk) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = ex2_approx(fmaf(x[chunk * 8 + 2 * e], c, -m_use));
-          const float b = ex2_approx(fmaf(x[chunk * 8 + 2 * e + 1], c, -m_use));
-          sum += a + b;
-          pk[e] = Pack2<T>::pack(a, b);
-        }
-        const uint32_t addr = pRow + (chunk / 8) * (BM * 128) + (((chunk % 8) ^ (rl & 7)) << 4);
-        st_shared_v4(addr, pk[0], pk[1], pk[2], pk[3]);
+      for (int i = 12; i < BN - 4; i += 8) {
+        mx0 = max3f(mx0, x[i], x[i + 1]);
+        mx1 = max3f(mx1, x[i + 2], x[i + 3]);
+        mx2 = max3f(mx2, x[i + 4], x[i + 5]);
+        mx3 = max3f(mx3, x[i + 6], x[i + 7]);
       }
-      l = l * alpha + sum;
-      if (j > 0 && __any_sync(0xffffffffu, m_new > m)) {
+      mx0 = max3f(mx0, x[BN - 4], x[BN - 3]);
+      mx1 = max3f(mx1, x[BN - 2], x[BN - 1]);
+      const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * c;
+      const bool grow = mx > m_run + kRescaleThreshold;
+      const float m_new = grow ? mx : m_run;
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2_approx(m_run - m_use);
+      // exponentials into packed registers, stored to TMEM in two halves; the
+      // first half is computed before waiting for P_t's columns to be free
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tO + cc * 32, o);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[BN / 4];
+#pragma unroll
+        for (int chunk = 0; chunk < BN / 16; ++chunk) {
+          const float* xc = x + half * (BN / 2) + chunk * 8;
+          float e[8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], c, -m_use);
+            e[2 * u] = ex2_approx(e[2 * u]);
+            e[2 * u + 1] = ex2_approx(e[2 * u + 1]);
+          }
+          add2(s0, s1, e[0], e[1]);
+          add2(s2, s3, e[2], e[3]);
+          add2(s0, s1, e[4], e[5]);
+          add2(s2, s3, e[6], e[7]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pk[chunk * 4 + u] = Pack2<T>::pack(e[2 * u], e[2 * u + 1]);
+        }
+        // P_t's columns are free once O_t += P_{j-1} V_{j-1} has finished (at d = 128
+        // they overlay S_t, already in registers, and that MMA finished before S_j)
+        if (half == 0 && !C::kPAlias && j > 0) ok = wait_all(&bars->pv_done[t], (j - 1) & 1);
+        if (!ok) break;
+        tmem_st32(tP + half * 32, pk);
+      }
+      if (!ok) break;
+      l = l * alpha + ((s0 + s1) + (s2 + s3));
+      m_run = m_new;
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O_t holds P_{j-1} V_{j-1} here: waited above, or (d = 128) finished before S_j
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t o[16];
+          tmem_ld16(tO + cc * 16, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + cc * 32, o);
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st16(tO + cc * 16, o);
         }
         tmem_st_wait();
       }
-      m = m_new;
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p[t]);
+      mbar_arrive(&bars->p_full[t]);
     }
-    if (nt > 0 && ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o[t], 0, abort_flag, p.status));
+    if (nt > 0 && ok) ok = wait_all(&bars->pv_done[t], (nt - 1) & 1);
     if (nt > 0 && ok) {
       tc_fence_after();
       const float inv = 1.f / l;
@@ -335,7 +417,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       T* orow = static_cast<T*>(p.o) +
                 (PACKED ? (static_cast<long long>(tok0 + row) * p.H + h) * D
                         : (static_cast<long long>(unit) * len_q + row) * D);
-#pragma unroll
+#pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tO + cc * 32, o);
@@ -355,7 +437,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       if (live) {
         const long long li = PACKED ? static_cast<long long>(h) * p.Lq + tok0 + row
                                     : static_cast<long long>(unit) * len_q + row;
-        p.lse[li] = (m + __log2f(l)) * kLn2;
+        p.lse[li] = (m_run + __log2f(l)) * kLn2;
       }
     }
   }
@@ -364,7 +446,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(bars->tmem_base, kTmemCols);
   }
 }
 
