@@ -32,9 +32,8 @@ namespace {
 
 constexpr int BM = 128;          // rows per Q tile
 constexpr int BN = 128;          // keys per K/V block
-constexpr int kThreads = 320;    // 8 softmax warps + producer + MMA
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;      // first MMA warp (also allocates TMEM)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -66,6 +65,12 @@ struct Cfg {
   static constexpr uint32_t kColO = 2 * BN;                   // + t * D
   static constexpr uint32_t kColP = kPAlias ? BN / 2 : 2 * BN + 2 * D;   // + t * (kPAlias ? BN : BN / 2)
   static constexpr uint32_t kPStride = kPAlias ? BN : BN / 2;
+  // MMA issue: with P in its own columns each Q tile gets its own MMA warp, so
+  // the tiles' waits and issues do not serialise; when P overlays S the two
+  // tiles' chains are serial and one warp alternating between them keeps the
+  // tensor cores busier.
+  static constexpr int kMmaWarps = kPAlias ? 1 : 2;
+  static constexpr int kThreads = (8 + 1 + kMmaWarps) * 32;
   static_assert(kPAlias || kColP + 2 * (BN / 2) <= 512, "TMEM budget");
 };
 
@@ -118,7 +123,7 @@ __device__ __forceinline__ int tile_blocks(int r, int len_q, int len_k) {
 }
 
 template <int D, typename T, bool CAUSAL, bool PACKED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = Cfg<D>;
@@ -160,7 +165,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     mbar_init(&bars->q, 1);
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars->full[i], 1);
-      mbar_init(&bars->empty[i], 1);
+      mbar_init(&bars->empty[i], C::kMmaWarps);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -168,7 +173,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       mbar_init(&bars->p_full[t], BM);
       mbar_init(&bars->pv_done[t], 1);
     }
-    mbar_init(&bars->done, 1);
+    mbar_init(&bars->done, C::kMmaWarps);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -229,79 +234,83 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         for (int f = first; f < it; ++f) mbar_wait_drain(&bars->full[f % C::kSlots], (f / C::kSlots) & 1);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp && warp < kMmaWarp + C::kMmaWarps) {
     // ------------------------------------------------------------ MMA issue
-    // The whole warp runs this loop with warp-uniform operands; lane 0 issues.
-    const uint32_t leader = lane == 0 ? 1u : 0u;
-    constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
-    constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BM, BN);
-    constexpr uint32_t idO = idesc_f16(fmt, 0, 1, BM, D);
-    // descriptors of the operand tiles; advancing the start address by `off`
-    // bytes adds off >> 4 to the descriptor (the address field cannot carry)
-    const uint64_t dQ0 = smem_desc(sQ, 16, C::kSbo, C::kSw);
-    const uint64_t dSlot0K = smem_desc(sSlots, 16, C::kSbo, C::kSw);
-    const uint64_t dSlot0V = smem_desc(sSlots, C::kColBlkBytes, C::kSbo, C::kSw);
-    auto issue_qk = [&](int t, int slot) {
-      const uint64_t a = dQ0 + ((t * C::kTileBytes) >> 4);
-      const uint64_t b = dSlot0K + ((slot * C::kTileBytes) >> 4);
+    // Warp w serves Q tiles [t_lo, t_hi); lane 0 issues. Every MMA warp
+    // consumes every K/V fill: a slot's empty barrier takes one commit from each.
+    const int t_lo = C::kMmaWarps == 2 ? warp - kMmaWarp : 0;
+    const int t_hi = C::kMmaWarps == 2 ? t_lo + 1 : 2;
+    if (lane == 0) {
+      constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
+      constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BM, BN);
+      constexpr uint32_t idO = idesc_f16(fmt, 0, 1, BM, D);
+      // descriptors of the operand tiles; advancing the start address by `off`
+      // bytes adds off >> 4 to the descriptor (the address field cannot carry)
+      const uint64_t dQ = smem_desc(sQ, 16, C::kSbo, C::kSw);
+      const uint64_t dSlot0K = smem_desc(sSlots, 16, C::kSbo, C::kSw);
+      const uint64_t dSlot0V = smem_desc(sSlots, C::kColBlkBytes, C::kSbo, C::kSw);
+      auto issue_qk = [&](int t, int slot) {
+        const uint64_t a = dQ + ((t * C::kTileBytes) >> 4);
+        const uint64_t b = dSlot0K + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = ((ks * 16 / C::kBlk) * C::kColBlkBytes + (ks * 16 % C::kBlk) * 2) >> 4;
-        mma_ss_p(tmem + C::kColS + t * BN, a + off, b + off, idS, ks > 0, leader);
-      }
-    };
-    auto issue_pv = [&](int t, int slot, bool acc) {
-      const uint64_t b = dSlot0V + ((slot * C::kTileBytes) >> 4);
-      const uint32_t a = tmem + C::kColP + t * C::kPStride;
-#pragma unroll
-      for (int ks = 0; ks < BN / 16; ++ks) {
-        const uint32_t boff = (ks * 16 * C::kRowBytes) >> 4;
-        mma_ts_p(tmem + C::kColO + t * D, a + ks * 8, b + boff, idO, (acc || ks > 0) ? 1u : 0u, leader);
-      }
-    };
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
-    };
-    auto full_wait = [&](int pos) { return wait_all(&bars->full[pos % C::kSlots], (pos / C::kSlots) & 1); };
-    bool ok = wait_all(&bars->q, 0) && full_wait(0);
-    if (ok) {
-      tc_fence_after();
-      if (n0 > 0) { issue_qk(0, 0); mma_commit_p(&bars->s_full[0], leader); }
-      if (n1 > 0) { issue_qk(1, 0); mma_commit_p(&bars->s_full[1], leader); }
-      mma_commit_p(&bars->empty[0], leader);
-    }
-    for (int j = 0; j < nmax && ok; ++j) {
-      // K_{j+1} sits at ring position 2j+2, V_j at 2j+1
-      const bool has_next = j + 1 < nmax;
-      const int kpos = 2 * j + 2, vpos = 2 * j + 1;
-      if (has_next && !(ok = full_wait(kpos))) break;
-      if (!(ok = full_wait(vpos))) break;
-      tc_fence_after();
-      for (int t = 0; t < 2 && ok; ++t) {
-        const int nt = t == 0 ? n0 : n1;
-        if (j >= nt) continue;
-        if (!C::kPAlias && j + 1 < nt) {
-          // S_t may be overwritten once its softmax group holds it in registers
-          if (!(ok = wait_all(&bars->s_free[t], j & 1))) break;
-          tc_fence_after();
-          issue_qk(t, kpos % C::kSlots);
-          mma_commit_p(&bars->s_full[t], leader);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks * 16 / C::kBlk) * C::kColBlkBytes + (ks * 16 % C::kBlk) * 2) >> 4;
+          mma_ss(tmem + C::kColS + t * BN, a + off, b + off, idS, ks > 0);
         }
-        if (!(ok = wait_all(&bars->p_full[t], j & 1))) break;
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint64_t b = dSlot0V + ((slot * C::kTileBytes) >> 4);
+        const uint32_t a = tmem + C::kColP + t * C::kPStride;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ts(tmem + C::kColO + t * D, a + ks * 8, b + ((ks * 16 * C::kRowBytes) >> 4), idO,
+                 (acc || ks > 0) ? 1u : 0u);
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort_flag, p.status); };
+      auto full_wait = [&](int pos) { return wait(&bars->full[pos % C::kSlots], (pos / C::kSlots) & 1); };
+      bool ok = wait(&bars->q, 0) && full_wait(0);
+      if (ok) {
         tc_fence_after();
-        issue_pv(t, vpos % C::kSlots, j > 0);
-        mma_commit_p(&bars->pv_done[t], leader);
-        if (C::kPAlias && j + 1 < nt) {
-          // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
-          issue_qk(t, kpos % C::kSlots);
-          mma_commit_p(&bars->s_full[t], leader);
+        for (int t = t_lo; t < t_hi; ++t) {
+          if ((t == 0 ? n0 : n1) == 0) continue;
+          issue_qk(t, 0);
+          mma_commit(&bars->s_full[t]);
         }
+        mma_commit(&bars->empty[0]);
       }
-      mma_commit_p(&bars->empty[vpos % C::kSlots], leader);
-      if (has_next) mma_commit_p(&bars->empty[kpos % C::kSlots], leader);
+      for (int j = 0; j < nmax && ok; ++j) {
+        // K_{j+1} sits at ring position 2j+2, V_j at 2j+1
+        const bool has_next = j + 1 < nmax;
+        const int kpos = 2 * j + 2, vpos = 2 * j + 1;
+        if (has_next && !(ok = full_wait(kpos))) break;
+        if (!(ok = full_wait(vpos))) break;
+        tc_fence_after();
+        for (int t = t_lo; t < t_hi && ok; ++t) {
+          const int nt = t == 0 ? n0 : n1;
+          if (j >= nt) continue;
+          if (!C::kPAlias && j + 1 < nt) {
+            // S_t may be overwritten once its softmax group holds it in registers
+            if (!(ok = wait(&bars->s_free[t], j & 1))) break;
+            tc_fence_after();
+            issue_qk(t, kpos % C::kSlots);
+            mma_commit(&bars->s_full[t]);
+          }
+          if (!(ok = wait(&bars->p_full[t], j & 1))) break;
+          tc_fence_after();
+          issue_pv(t, vpos % C::kSlots, j > 0);
+          mma_commit(&bars->pv_done[t]);
+          if (C::kPAlias && j + 1 < nt) {
+            // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
+            issue_qk(t, kpos % C::kSlots);
+            mma_commit(&bars->s_full[t]);
+          }
+        }
+        mma_commit(&bars->empty[vpos % C::kSlots]);
+        if (has_next) mma_commit(&bars->empty[kpos % C::kSlots]);
+      }
+      mma_commit(&bars->done);
+      mbar_wait_drain(&bars->done, 0);
     }
-    mma_commit_p(&bars->done, leader);
-    mbar_wait_drain(&bars->done, 0);
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp / 4;
@@ -468,7 +477,7 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
   const long long blocks = npairs * units;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), kThreads, Cfg<D>::kSmem, s>>>(p, m.q, m.k, m.v);
+  kern<<<static_cast<unsigned>(blocks), Cfg<D>::kThreads, Cfg<D>::kSmem, s>>>(p, m.q, m.k, m.v);
   return cudaGetLastError();
 }
 
