@@ -23,6 +23,7 @@
 // exponentials; P is double-buffered in shared memory for d <= 64, and O is
 // rescaled only when a row maximum grows past a threshold. TMEM columns:
 // S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+#include <atomic>
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -35,12 +36,25 @@ constexpr int BN = 128;          // keys per K/V block
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;      // first MMA warp (also allocates TMEM)
 constexpr uint32_t kTmemCols = 512;
+// Register split (launch: 384 threads x 168): softmax groups 200, the
+// producer / MMA group 104; 256 * 200 + 128 * 104 = 64512 = 384 * 168,
+// and per SM sub-partition 200 + 200 + 104 <= 512 registers per lane.
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsControl = 104;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // The running maximum used in the exponent is only raised when a row's new
 // maximum exceeds it by more than this (log2 units), so P <= 2^8 and O is
 // rescaled rarely; the result is the same because O and l share the maximum.
 constexpr float kRescaleThreshold = 8.0f;
+
+// Dynamic work distribution: each launch takes one slot of {next item, CTAs
+// finished}; CTAs claim items with atomicAdd and the last CTA to finish puts
+// the slot back to zero. Launches in flight at the same time use different
+// slots (a host-side counter walks the slots in turn).
+constexpr int kSchedSlots = 1024;
+__device__ unsigned g_fwd_sched[2 * kSchedSlots];
+constexpr int kItemQueue = 4;
 
 template <int D>
 struct Cfg {
@@ -70,26 +84,30 @@ struct Cfg {
   // tiles' chains are serial and one warp alternating between them keeps the
   // tensor cores busier.
   static constexpr int kMmaWarps = kPAlias ? 1 : 2;
-  static constexpr int kThreads = (8 + 1 + kMmaWarps) * 32;
+  // Three warpgroups: two softmax groups and one for the producer and MMA
+  // warps (the rest of it idles), so that registers can move between them.
+  static constexpr int kThreads = 384;
   static_assert(kPAlias || kColP + 2 * (BN / 2) <= 512, "TMEM budget");
 };
 
 struct __align__(8) Bars {
-  uint64_t q;
+  uint64_t q_full[2];     // Q_t loaded for the current work item
+  uint64_t q_empty[2];    // last S_t = Q_t K^T of a work item finished: Q_t may be reloaded
   uint64_t full[16];
   uint64_t empty[16];
   uint64_t s_full[2];     // S_t written by the tensor cores
   uint64_t s_free[2];     // S_t read into registers by its softmax group
   uint64_t p_full[2];     // P_t in TMEM (and O_t rescaled)
   uint64_t pv_done[2];    // O_t += P_t V_j finished
+  uint64_t o_free[2];     // O_t read out by the epilogue: the next item may overwrite it
+  uint64_t item_full[4];  // work-item queue from the producer to the other roles
+  uint64_t item_empty[4];
+  int item[4];
   uint64_t done;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float m;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
@@ -122,56 +140,74 @@ __device__ __forceinline__ int tile_blocks(int r, int len_q, int len_k) {
   return min(nkv, last_row / BN + 1);
 }
 
+// One work item: 256 query rows (two 128-row tiles) of one (batch|sequence, head).
+struct Item {
+  int unit, h, tok0, len_q, len_k, r0, n0, n1, nmax;
+};
+
+// Items are numbered unit-major, so the items of one (batch|sequence, head) run
+// side by side and share its K/V through L2; under causal masking the longest
+// rows of each unit come first.
+template <bool CAUSAL, bool PACKED>
+__device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npairs) {
+  Item it;
+  it.unit = idx / npairs;
+  const int ord = idx % npairs;
+  const int pair = CAUSAL ? (npairs - 1 - ord) : ord;
+  it.h = 0;
+  it.tok0 = 0;
+  if (PACKED) {
+    const int s = it.unit / p.H;
+    it.h = it.unit % p.H;
+    it.tok0 = p.cu_seqlens[s];
+    it.len_q = it.len_k = p.cu_seqlens[s + 1] - it.tok0;
+    if (it.len_q > p.Lk && ord == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+  } else {
+    it.len_q = p.Lq;
+    it.len_k = p.Lk;
+  }
+  it.r0 = pair * 2 * BM;
+  it.n0 = tile_blocks<CAUSAL>(it.r0, it.len_q, it.len_k);
+  it.n1 = tile_blocks<CAUSAL>(it.r0 + BM, it.len_q, it.len_k);
+  it.nmax = max(it.n0, it.n1);
+  return it;
+}
+
 template <int D, typename T, bool CAUSAL, bool PACKED>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
-              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              unsigned* sched) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
 
-  // ---- which unit and which rows
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int unit, pair, len_q, len_k, tok0 = 0, h = 0;
-  {
-    // Unit-major order: the CTAs of one (batch|sequence, head) run side by side
-    // and share its K/V through L2; under causal masking the longest rows go first.
-    const int npairs = ((PACKED ? p.Lk : p.Lq) + 2 * BM - 1) / (2 * BM);
-    unit = blockIdx.x / npairs;
-    const int ord = blockIdx.x % npairs;
-    pair = CAUSAL ? (npairs - 1 - ord) : ord;
-    if (PACKED) {
-      const int s = unit / p.H;
-      h = unit % p.H;
-      tok0 = p.cu_seqlens[s];
-      len_q = len_k = p.cu_seqlens[s + 1] - tok0;
-      if (len_q > p.Lk && ord == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
-    } else {
-      len_q = p.Lq;
-      len_k = p.Lk;
-    }
-  }
-  const int r0 = pair * 2 * BM;
-  const int n0 = tile_blocks<CAUSAL>(r0, len_q, len_k);
-  const int n1 = tile_blocks<CAUSAL>(r0 + BM, len_q, len_k);
-  const int nmax = max(n0, n1);
-  if (nmax == 0) return;
+  // Persistent: CTA b starts with work item b, then claims items dynamically.
+  const int npairs = ((PACKED ? p.Lk : p.Lq) + 2 * BM - 1) / (2 * BM);
+  const int nitems = npairs * p.B * p.H;
 
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sSlots = smem_u32(smem + C::kOffSlots);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q, 1);
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars->full[i], 1);
       mbar_init(&bars->empty[i], C::kMmaWarps);
     }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->q_empty[t], 1);
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->s_free[t], BM);
       mbar_init(&bars->p_full[t], BM);
       mbar_init(&bars->pv_done[t], 1);
+      mbar_init(&bars->o_free[t], BM);
+    }
+    for (int i = 0; i < kItemQueue; ++i) {
+      mbar_init(&bars->item_full[i], 1);
+      mbar_init(&bars->item_empty[i], 8 + C::kMmaWarps);   // one arrival per consuming warp
     }
     mbar_init(&bars->done, C::kMmaWarps);
     bars->abort_flag = 0;
@@ -194,44 +230,69 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     *abort_flag = 1u;
   }
 
-  if (warp == kProducerWarp) {
+  if (warp >= 8) {
+   // producer, MMA and idle warps
+   regs_dec<kRegsControl>();
+   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      auto c1 = [&](int row) { return PACKED ? h : row; };
-      auto c2 = [&](int row) { return PACKED ? tok0 + row : unit; };
-      if (!(p.debug & kDebugDropQArrive) && !*abort_flag) {
-        const uint32_t qbytes = (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0);
-        mbar_expect_tx(&bars->q, qbytes);
-        for (int t = 0; t < 2; ++t) {
-          if ((t == 0 ? n0 : n1) == 0) continue;
-          const int row = r0 + t * BM;
+      int fill = 0;             // ring position of the next K/V fill (K_0, V_0, K_1, V_1, ... per item)
+      int qloads[2] = {0, 0};   // Q loads so far per tile
+      bool ok = true;
+      int idx = blockIdx.x;
+      for (int k = 0;; ++k) {
+        // publish the item (or the end marker) to the other roles
+        const int q = k % kItemQueue;
+        if (k >= kItemQueue && !(ok = mbar_wait(&bars->item_empty[q], (k / kItemQueue - 1) & 1, abort_flag, p.status)))
+          break;
+        if (!ok || idx >= nitems) idx = -1;
+        bars->item[q] = idx;
+        mbar_arrive(&bars->item_full[q]);
+        if (idx < 0) break;
+        const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
+        idx = static_cast<int>(atomicAdd(sched, 1u)) + static_cast<int>(gridDim.x);
+        if (it.nmax == 0) continue;
+        auto c1 = [&](int row) { return PACKED ? it.h : row; };
+        auto c2 = [&](int row) { return PACKED ? it.tok0 + row : it.unit; };
+        for (int t = 0; t < 2 && ok; ++t) {
+          if ((t == 0 ? it.n0 : it.n1) == 0) continue;
+          if (qloads[t] > 0 && !(ok = mbar_wait(&bars->q_empty[t], (qloads[t] - 1) & 1, abort_flag, p.status))) break;
+          ++qloads[t];
+          if (p.debug & kDebugDropQArrive) continue;
+          mbar_expect_tx(&bars->q_full[t], C::kTileBytes);
+          const int row = it.r0 + t * BM;
           for (int cb = 0; cb < C::kNBlk; ++cb)
-            tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q,
+            tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[t],
                         cb * C::kBlk, c1(row), c2(row));
+        }
+        for (int j = 0; j < it.nmax && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++fill) {
+            const int slot = fill % C::kSlots;
+            const int round = fill / C::kSlots;
+            if (round > 0 && !(ok = mbar_wait(&bars->empty[slot], (round - 1) & 1, abort_flag, p.status))) break;
+            mbar_expect_tx(&bars->full[slot], C::kTileBytes);
+            const CUtensorMap* m = kv ? &tmV : &tmK;
+            const int row = j * BN;
+            for (int cb = 0; cb < C::kNBlk; ++cb)
+              tma_load_3d(smem + C::kOffSlots + slot * C::kTileBytes + cb * C::kColBlkBytes, m, &bars->full[slot],
+                          cb * C::kBlk, c1(row), c2(row));
+          }
         }
       }
-      // ring order: K_0, V_0, K_1, V_1, ...
-      int it = 0;
-      for (int j = 0; j < nmax && !*abort_flag; ++j) {
-        for (int kv = 0; kv < 2; ++kv, ++it) {
-          const int slot = it % C::kSlots;
-          const int round = it / C::kSlots;
-          if (round > 0 && !mbar_wait(&bars->empty[slot], (round - 1) & 1, abort_flag, p.status)) break;
-          mbar_expect_tx(&bars->full[slot], C::kTileBytes);
-          const CUtensorMap* m = kv ? &tmV : &tmK;
-          const int row = j * BN;
-          for (int cb = 0; cb < C::kNBlk; ++cb)
-            tma_load_3d(smem + C::kOffSlots + slot * C::kTileBytes + cb * C::kColBlkBytes, m, &bars->full[slot],
-                        cb * C::kBlk, c1(row), c2(row));
-        }
+      // the last CTA to finish claiming resets this launch's scheduler slot
+      if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+        atomicExch(sched, 0u);
+        atomicExch(sched + 1, 0u);
       }
       if (*abort_flag) {
         // Let copies already issued land before the CTA's shared memory is released.
-        const int first = max(0, it - C::kSlots);
-        for (int f = first; f < it; ++f) mbar_wait_drain(&bars->full[f % C::kSlots], (f / C::kSlots) & 1);
+        for (int f = max(0, fill - C::kSlots); f < fill; ++f)
+          mbar_wait_drain(&bars->full[f % C::kSlots], (f / C::kSlots) & 1);
+        for (int t = 0; t < 2; ++t)
+          if (qloads[t] > 0 && !(p.debug & kDebugDropQArrive)) mbar_wait_drain(&bars->q_full[t], (qloads[t] - 1) & 1);
       }
     }
   } else if (warp >= kMmaWarp && warp < kMmaWarp + C::kMmaWarps) {
@@ -268,184 +329,230 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort_flag, p.status); };
       auto full_wait = [&](int pos) { return wait(&bars->full[pos % C::kSlots], (pos / C::kSlots) & 1); };
-      bool ok = wait(&bars->q, 0) && full_wait(0);
-      if (ok) {
+      int fill = 0;
+      int qloads[2] = {0, 0};    // Q tiles consumed per tile slot
+      int blocks[2] = {0, 0};    // K/V blocks processed per tile slot (barrier phases)
+      int items[2] = {0, 0};     // work items finished per tile slot
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int q = k % kItemQueue;
+        if (!(ok = wait(&bars->item_full[q], (k / kItemQueue) & 1))) break;
+        const int idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
+        mbar_arrive(&bars->item_empty[q]);
+        if (idx < 0) break;
+        const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
+        if (it.nmax == 0) continue;
+        // first S_t of the item
+        for (int t = t_lo; t < t_hi && ok; ++t) {
+          if ((t == 0 ? it.n0 : it.n1) == 0) continue;
+          if (!(ok = wait(&bars->q_full[t], qloads[t] & 1))) break;
+          ++qloads[t];
+          // the previous item's last S_t must have been read (P overlaying S is
+          // ordered behind the last P.V on the tensor cores instead)
+          if (!C::kPAlias && blocks[t] > 0 && !(ok = wait(&bars->s_free[t], (blocks[t] - 1) & 1))) break;
+        }
+        if (!ok || !(ok = full_wait(fill))) break;
         tc_fence_after();
         for (int t = t_lo; t < t_hi; ++t) {
-          if ((t == 0 ? n0 : n1) == 0) continue;
-          issue_qk(t, 0);
+          const int nt = t == 0 ? it.n0 : it.n1;
+          if (nt == 0) continue;
+          issue_qk(t, fill % C::kSlots);
           mma_commit(&bars->s_full[t]);
+          if (nt == 1) mma_commit(&bars->q_empty[t]);
         }
-        mma_commit(&bars->empty[0]);
-      }
-      for (int j = 0; j < nmax && ok; ++j) {
-        // K_{j+1} sits at ring position 2j+2, V_j at 2j+1
-        const bool has_next = j + 1 < nmax;
-        const int kpos = 2 * j + 2, vpos = 2 * j + 1;
-        if (has_next && !(ok = full_wait(kpos))) break;
-        if (!(ok = full_wait(vpos))) break;
-        tc_fence_after();
-        for (int t = t_lo; t < t_hi && ok; ++t) {
-          const int nt = t == 0 ? n0 : n1;
-          if (j >= nt) continue;
-          if (!C::kPAlias && j + 1 < nt) {
-            // S_t may be overwritten once its softmax group holds it in registers
-            if (!(ok = wait(&bars->s_free[t], j & 1))) break;
-            tc_fence_after();
-            issue_qk(t, kpos % C::kSlots);
-            mma_commit(&bars->s_full[t]);
-          }
-          if (!(ok = wait(&bars->p_full[t], j & 1))) break;
+        mma_commit(&bars->empty[fill % C::kSlots]);
+        for (int j = 0; j < it.nmax && ok; ++j) {
+          // K_{j+1} sits at ring position fill + 2j + 2, V_j at fill + 2j + 1
+          const bool has_next = j + 1 < it.nmax;
+          const int kpos = fill + 2 * j + 2, vpos = fill + 2 * j + 1;
+          if (has_next && !(ok = full_wait(kpos))) break;
+          if (!(ok = full_wait(vpos))) break;
           tc_fence_after();
-          issue_pv(t, vpos % C::kSlots, j > 0);
-          mma_commit(&bars->pv_done[t]);
-          if (C::kPAlias && j + 1 < nt) {
-            // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
-            issue_qk(t, kpos % C::kSlots);
-            mma_commit(&bars->s_full[t]);
+          for (int t = t_lo; t < t_hi && ok; ++t) {
+            const int nt = t == 0 ? it.n0 : it.n1;
+            if (j >= nt) continue;
+            const int g = blocks[t] + j;
+            if (!C::kPAlias && j + 1 < nt) {
+              // S_t may be overwritten once its softmax group holds it in registers
+              if (!(ok = wait(&bars->s_free[t], g & 1))) break;
+              tc_fence_after();
+              issue_qk(t, kpos % C::kSlots);
+              mma_commit(&bars->s_full[t]);
+              if (j + 2 == nt) mma_commit(&bars->q_empty[t]);
+            }
+            if (!(ok = wait(&bars->p_full[t], g & 1))) break;
+            // O_t is overwritten by the item's first P.V: the previous item's
+            // epilogue must have read it
+            if (j == 0 && items[t] > 0 && !(ok = wait(&bars->o_free[t], (items[t] - 1) & 1))) break;
+            tc_fence_after();
+            issue_pv(t, vpos % C::kSlots, j > 0);
+            mma_commit(&bars->pv_done[t]);
+            if (C::kPAlias && j + 1 < nt) {
+              // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
+              issue_qk(t, kpos % C::kSlots);
+              mma_commit(&bars->s_full[t]);
+              if (j + 2 == nt) mma_commit(&bars->q_empty[t]);
+            }
           }
+          mma_commit(&bars->empty[vpos % C::kSlots]);
+          if (has_next) mma_commit(&bars->empty[kpos % C::kSlots]);
         }
-        mma_commit(&bars->empty[vpos % C::kSlots]);
-        if (has_next) mma_commit(&bars->empty[kpos % C::kSlots]);
+        for (int t = t_lo; t < t_hi; ++t) {
+          const int nt = t == 0 ? it.n0 : it.n1;
+          blocks[t] += nt;
+          if (nt > 0) ++items[t];
+        }
+        fill += 2 * it.nmax;
       }
       mma_commit(&bars->done);
       mbar_wait_drain(&bars->done, 0);
     }
+   }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int t = warp / 4;
-    const int nt = t == 0 ? n0 : n1;
-    const int rt = r0 + t * BM;
     const int rl = threadIdx.x & 127;        // row within the tile == TMEM lane
-    const int row = rt + rl;                  // row within the unit
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS + t * BN;
     const uint32_t tO = tmem + lane_off + C::kColO + t * D;
     const uint32_t tP = tmem + lane_off + C::kColP + t * C::kPStride;
     const float c = p.scale * kLog2e;
-    float m_run = -INFINITY, l = 0.f;        // maximum used in the exponent (base 2), running sum
-    bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       // warp-uniform decision: the TMEM accesses that follow are warp-collective
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
     };
-    for (int j = 0; j < nt; ++j) {
-      if (!(ok = wait_all(&bars->s_full[t], j & 1))) break;
-      tc_fence_after();
-      uint32_t sr[BN];
-      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      tmem_ld_wait();
-      if (!C::kPAlias) {
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[t]);
-      }
-      float* x = reinterpret_cast<float*>(sr);
-      const int kbase = j * BN;
-      if ((kbase + BN > len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
-#pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          const int key = kbase + i;
-          if (key >= len_k || (CAUSAL && key > row)) x[i] = -INFINITY;
-        }
-      }
-      // row maximum: four independent chains of three-input max
-      float mx0 = max3f(x[0], x[1], x[2]), mx1 = max3f(x[3], x[4], x[5]);
-      float mx2 = max3f(x[6], x[7], x[8]), mx3 = max3f(x[9], x[10], x[11]);
-#pragma unroll
-      for (int i = 12; i < BN - 4; i += 8) {
-        mx0 = max3f(mx0, x[i], x[i + 1]);
-        mx1 = max3f(mx1, x[i + 2], x[i + 3]);
-        mx2 = max3f(mx2, x[i + 4], x[i + 5]);
-        mx3 = max3f(mx3, x[i + 6], x[i + 7]);
-      }
-      mx0 = max3f(mx0, x[BN - 4], x[BN - 3]);
-      mx1 = max3f(mx1, x[BN - 2], x[BN - 1]);
-      const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * c;
-      const bool grow = mx > m_run + kRescaleThreshold;
-      const float m_new = grow ? mx : m_run;
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - m_use);
-      // exponentials into packed registers, stored to TMEM in two halves; the
-      // first half is computed before waiting for P_t's columns to be free
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[BN / 4];
-#pragma unroll
-        for (int chunk = 0; chunk < BN / 16; ++chunk) {
-          const float* xc = x + half * (BN / 2) + chunk * 8;
-          float e[8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], c, -m_use);
-            e[2 * u] = ex2_approx(e[2 * u]);
-            e[2 * u + 1] = ex2_approx(e[2 * u + 1]);
-          }
-          add2(s0, s1, e[0], e[1]);
-          add2(s2, s3, e[2], e[3]);
-          add2(s0, s1, e[4], e[5]);
-          add2(s2, s3, e[6], e[7]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) pk[chunk * 4 + u] = Pack2<T>::pack(e[2 * u], e[2 * u + 1]);
-        }
-        // P_t's columns are free once O_t += P_{j-1} V_{j-1} has finished (at d = 128
-        // they overlay S_t, already in registers, and that MMA finished before S_j)
-        if (half == 0 && !C::kPAlias && j > 0) ok = wait_all(&bars->pv_done[t], (j - 1) & 1);
-        if (!ok) break;
-        tmem_st32(tP + half * 32, pk);
-      }
-      if (!ok) break;
-      l = l * alpha + ((s0 + s1) + (s2 + s3));
-      m_run = m_new;
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_t holds P_{j-1} V_{j-1} here: waited above, or (d = 128) finished before S_j
+    int blocks = 0;   // K/V blocks processed by this tile slot so far (barrier phases)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int q = k % kItemQueue;
+      if (!(ok = wait_all(&bars->item_full[q], (k / kItemQueue) & 1))) break;
+      const int idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[q]);
+      if (idx < 0) break;
+      const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
+      const int nt = t == 0 ? it.n0 : it.n1;
+      if (nt == 0) continue;
+      const int rt = it.r0 + t * BM;
+      const int row = rt + rl;                // row within the unit
+      float m_run = -INFINITY, l = 0.f;      // maximum used in the exponent (base 2), running sum
+      for (int j = 0; j < nt; ++j) {
+        const int g = blocks + j;
+        if (!(ok = wait_all(&bars->s_full[t], g & 1))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < D / 16; ++cc) {
-          uint32_t o[16];
-          tmem_ld16(tO + cc * 16, o);
-          tmem_ld_wait();
+        uint32_t sr[BN];
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_ld_wait();
+        if (!C::kPAlias) {
+          tc_fence_before();
+          mbar_arrive(&bars->s_free[t]);
+        }
+        float* x = reinterpret_cast<float*>(sr);
+        const int kbase = j * BN;
+        if ((kbase + BN > it.len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st16(tO + cc * 16, o);
+          for (int i = 0; i < BN; ++i) {
+            const int key = kbase + i;
+            if (key >= it.len_k || (CAUSAL && key > row)) x[i] = -INFINITY;
+          }
+        }
+        // row maximum: four independent chains of three-input max
+        float mx0 = max3f(x[0], x[1], x[2]), mx1 = max3f(x[3], x[4], x[5]);
+        float mx2 = max3f(x[6], x[7], x[8]), mx3 = max3f(x[9], x[10], x[11]);
+#pragma unroll
+        for (int i = 12; i < BN - 4; i += 8) {
+          mx0 = max3f(mx0, x[i], x[i + 1]);
+          mx1 = max3f(mx1, x[i + 2], x[i + 3]);
+          mx2 = max3f(mx2, x[i + 4], x[i + 5]);
+          mx3 = max3f(mx3, x[i + 6], x[i + 7]);
+        }
+        mx0 = max3f(mx0, x[BN - 4], x[BN - 3]);
+        mx1 = max3f(mx1, x[BN - 2], x[BN - 1]);
+        const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * c;
+        const bool grow = mx > m_run + kRescaleThreshold;
+        const float m_new = grow ? mx : m_run;
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2_approx(m_run - m_use);
+        // exponentials into packed registers, stored to TMEM in two halves; the
+        // first half is computed before waiting for P_t's columns to be free
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[BN / 4];
+#pragma unroll
+          for (int chunk = 0; chunk < BN / 16; ++chunk) {
+            const float* xc = x + half * (BN / 2) + chunk * 8;
+            float e[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], c, -m_use);
+              e[2 * u] = ex2_approx(e[2 * u]);
+              e[2 * u + 1] = ex2_approx(e[2 * u + 1]);
+            }
+            add2(s0, s1, e[0], e[1]);
+            add2(s2, s3, e[2], e[3]);
+            add2(s0, s1, e[4], e[5]);
+            add2(s2, s3, e[6], e[7]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pk[chunk * 4 + u] = Pack2<T>::pack(e[2 * u], e[2 * u + 1]);
+          }
+          // P_t's columns are free once O_t += P_{j-1} V_{j-1} has finished (at d = 128
+          // they overlay S_t, already in registers, and that MMA finished before S_j)
+          if (half == 0 && !C::kPAlias && j > 0) ok = wait_all(&bars->pv_done[t], (g - 1) & 1);
+          if (!ok) break;
+          tmem_st32(tP + half * 32, pk);
+        }
+        if (!ok) break;
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
+        m_run = m_new;
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_t holds P_{j-1} V_{j-1} here: waited above, or (d = 128) finished before S_j
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t o[16];
+            tmem_ld16(tO + cc * 16, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(tO + cc * 16, o);
+          }
         }
         tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
-    }
-    if (nt > 0 && ok) ok = wait_all(&bars->pv_done[t], (nt - 1) & 1);
-    if (nt > 0 && ok) {
+      if (!ok || !(ok = wait_all(&bars->pv_done[t], (blocks + nt - 1) & 1))) break;
+      blocks += nt;
+      // epilogue: O = O / l rounded once, LSE = (m + log2 l) ln 2. O_t is read
+      // into packed registers first and released to the next item's first P.V.
       tc_fence_after();
       const float inv = 1.f / l;
-      const bool live = row < len_q;
-      T* orow = static_cast<T*>(p.o) +
-                (PACKED ? (static_cast<long long>(tok0 + row) * p.H + h) * D
-                        : (static_cast<long long>(unit) * len_q + row) * D);
-#pragma unroll 1
+      uint32_t ov[D / 2];
+#pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tO + cc * 32, o);
         tmem_ld_wait();
-        if (live) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = Pack2<T>::pack(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-            w.y = Pack2<T>::pack(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-            w.z = Pack2<T>::pack(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-            w.w = Pack2<T>::pack(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + cc * 32 + 8 * e) = w;
-          }
-        }
+        for (int e = 0; e < 16; ++e)
+          ov[cc * 16 + e] = Pack2<T>::pack(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
       }
-      if (live) {
-        const long long li = PACKED ? static_cast<long long>(h) * p.Lq + tok0 + row
-                                    : static_cast<long long>(unit) * len_q + row;
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+      if (row < it.len_q) {
+        T* orow = static_cast<T*>(p.o) +
+                  (PACKED ? (static_cast<long long>(it.tok0 + row) * p.H + it.h) * D
+                          : (static_cast<long long>(it.unit) * it.len_q + row) * D);
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e)
+          *reinterpret_cast<uint4*>(orow + 8 * e) = make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
+        const long long li = PACKED ? static_cast<long long>(it.h) * p.Lq + it.tok0 + row
+                                    : static_cast<long long>(it.unit) * it.len_q + row;
         p.lse[li] = (m_run + __log2f(l)) * kLn2;
       }
     }
@@ -471,13 +578,34 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
+  static int sm_count[64] = {0};
+  if (dev < 64 && sm_count[dev] == 0) {
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const int sms = dev < 64 ? sm_count[dev] : 1;
   const int rows = PACKED ? p.Lk : p.Lq;
   const long long npairs = (rows + 2 * BM - 1) / (2 * BM);
-  const long long units = static_cast<long long>(p.B) * p.H;
-  const long long blocks = npairs * units;
-  if (blocks == 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), Cfg<D>::kThreads, Cfg<D>::kSmem, s>>>(p, m.q, m.k, m.v);
+  const long long items = npairs * p.B * p.H;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // d <= 64: persistent, one CTA per SM (each needs most of the SM's SMEM and all
+  // of its TMEM) claiming items until none are left, so an item's prologue and
+  // epilogue overlap its neighbours'. d = 128: one CTA per item measured faster
+  // (its items are long, and the hardware's block scheduler balances them).
+  const long long want = D == 128 ? items : (items < sms ? items : sms);
+  const unsigned grid = static_cast<unsigned>(want);
+  static unsigned* sched_base[64] = {nullptr};
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (sched_base[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_fwd_sched);
+    if (e != cudaSuccess) return e;
+    sched_base[dev] = static_cast<unsigned*>(ptr);
+  }
+  static std::atomic<unsigned> launches{0};
+  unsigned* sched = sched_base[dev] + 2 * (launches.fetch_add(1) % kSchedSlots);
+  kern<<<grid, Cfg<D>::kThreads, Cfg<D>::kSmem, s>>>(p, m.q, m.k, m.v, sched);
   return cudaGetLastError();
 }
 
