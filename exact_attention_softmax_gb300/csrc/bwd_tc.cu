@@ -4,23 +4,24 @@
 // "FlashAttention"): the probabilities are rebuilt from Q, K and the saved
 // log-sum-exp rather than stored. Each CTA keeps one 128-key block of K and V
 // (and its dK, dV accumulators in TMEM) and streams the query tiles that can
-// see it. Per query tile i of BQ rows, with everything transposed so that keys
-// sit on TMEM lanes:
+// see it. Per query tile i of BQ rows, with keys on TMEM lanes:
 //
-//   S^T  = K Q_i^T                (tcgen05, TMEM)
-//   dP^T = V dO_i^T               (tcgen05, TMEM)
-//   P^T  = exp(scale S^T - LSE_i),  dS^T = P^T * (dP^T - D_i)
-//                                 (one thread per key row, written to SMEM)
-//   dV  += P^T dO_i ;  dK += dS^T Q_i                      (tcgen05, TMEM)
-//   dQ_i partial = dS K   (d <= 64: M = query rows)
-//             or  (K^T dS^T)^T (d = 128: M = head dims)    (tcgen05, TMEM)
+//   S^T  = K Q_i^T,  dP^T = V dO_i^T                          (tcgen05, TMEM)
+//   P^T  = exp(scale S^T - LSE_i),  dS^T = P^T * (dP^T - D_i)  (CUDA cores -> SMEM)
+//   dV  += P^T dO_i ;  dK += dS^T Q_i                          (tcgen05, TMEM)
+//   dQ_i partial = dS K   (d = 64: M = query rows)
+//             or  (K^T dS^T)^T (d = 128: M = head dims)       (tcgen05, TMEM)
 //
 // and the dQ partial is added into an fp32 accumulator in global memory with
 // one bulk shared->global reduce per tile. dK = scale * dK_acc and dV are
 // written at the end; dQ = scale * dQ_acc is rounded by a separate kernel.
 //
-// Warps: 0-3 build P^T / dS^T (then write dV), 4-7 drain dQ (then write dK),
-// 8 loads with TMA, 9 issues the MMAs from one thread.
+// Warps: 0-3 and 4-7 build P^T / dS^T for the first and second half of the
+// tile's queries (then write dV and dK); 8-11 drain dQ; 12 loads with TMA;
+// 13 issues S^T and dP^T; 14 issues dV, dK and dQ; 15 idles. The softmax
+// groups release S^T / dP^T as soon as they hold them in registers, so the
+// next tile's S^T, dP^T run under their arithmetic, and dQ has two TMEM
+// buffers so its drain overlaps the next tile.
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -29,15 +30,23 @@ namespace sdpa {
 namespace {
 
 constexpr int BK = 128;          // keys per CTA
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 512;
+constexpr int kDqWarp0 = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaSWarp = 13;
+constexpr int kMmaGWarp = 14;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+// Register split (launch: 512 threads x 128): softmax groups 160, dQ drain and
+// control groups 96; 256 * 160 + 256 * 96 = 65536 = 512 * 128, and per SM
+// sub-partition 160 + 160 + 96 + 96 = 512 registers per lane.
+constexpr uint32_t kRegsSoftmax = 160;
+constexpr uint32_t kRegsOther = 96;
 
 template <int D>
 struct BCfg {
   static constexpr int BQ = D == 128 ? 64 : 128;            // query rows per step
+  static constexpr int kHalf = BQ / 2;                       // query columns per softmax group
   static constexpr bool kDqT = D == 128;                     // dQ computed transposed
   static constexpr int kBlk = D >= 64 ? 64 : D;
   static constexpr int kNBlk = D / kBlk;
@@ -63,18 +72,23 @@ struct BCfg {
   static constexpr int kOffStat = kOffDQ + kDqBytes;                    // kStages x (lse2[BQ], delta[BQ])
   static constexpr int kOffBar = kOffStat + kStages * BQ * 8;
   static constexpr int kSmem = kOffBar + 256 + 1024;
-  // TMEM columns
+  static_assert(kSmem <= 232448, "shared memory budget");
+  // TMEM columns: S^T, dP^T, dV, dK, two dQ buffers
+  static constexpr int kDqCols = kDqT ? BQ : D;
   static constexpr uint32_t kTS = 0, kTdP = BQ, kTdV = 2 * BQ, kTdK = 2 * BQ + D, kTdQ = 2 * BQ + 2 * D;
+  static_assert(kTdQ + 2 * kDqCols <= 512, "TMEM budget");
 };
 
 struct __align__(8) BBars {
   uint64_t kv;
   uint64_t full[2];
   uint64_t empty[2];
-  uint64_t s;
-  uint64_t p;
-  uint64_t dq_full;
-  uint64_t dq_free;
+  uint64_t s_full;     // S^T, dP^T of the current tile in TMEM
+  uint64_t s_free;     // ... read into registers by both softmax groups
+  uint64_t pds_full;   // P^T, dS^T in shared memory
+  uint64_t pds_free;   // ... consumed by the dV, dK, dQ MMAs
+  uint64_t dq_full[2];
+  uint64_t dq_free[2];
   uint64_t kv_done;
   uint64_t done;
   uint32_t tmem_base;
@@ -118,7 +132,6 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   const int nq = (Lq + BQ - 1) / BQ;
   const int i0 = CAUSAL ? min(nq, key0 / BQ) : 0;
   const int nsteps = nq - i0;
-  if (key0 >= Lk) return;
 
   const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
   const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
@@ -131,29 +144,38 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->full[i], 32);
       mbar_init(&bars->empty[i], 1);
+      mbar_init(&bars->dq_full[i], 1);
+      mbar_init(&bars->dq_free[i], 128);
     }
-    mbar_init(&bars->s, 1);
-    mbar_init(&bars->p, 128);
-    mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 256);
+    mbar_init(&bars->pds_full, 256);
+    mbar_init(&bars->pds_free, 2);     // dV/dK warp and dQ warp
     mbar_init(&bars->kv_done, 1);
-    mbar_init(&bars->done, 1);
+    mbar_init(&bars->done, 2);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaSWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
   volatile uint32_t* abort_flag = &bars->abort_flag;
+  // All 512 columns are allocated, so the allocation starts at column 0.
+  constexpr uint32_t tmem = 0;
+  if (bars->tmem_base != 0u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusTimeout);
+    *abort_flag = 1u;
+  }
 
-  if (warp == kProducerWarp) {
+  if (warp >= kDqWarp0) {
+   regs_dec<kRegsOther>();
+   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !*abort_flag) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -166,186 +188,150 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     }
     const float* lse = p.lse + static_cast<long long>(unit) * Lq;
     const float* delta = bp.delta + static_cast<long long>(unit) * Lq;
+    // The row statistics of step s + 1 are fetched into registers while step s
+    // is in flight, so their latency hides behind the wait for a free stage.
+    constexpr int kPer = BQ / 32;
+    float nl[kPer], nd[kPer];
+    auto fetch = [&](int step) {
+      const int q0 = (i0 + step) * BQ;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int q = q0 + lane + 32 * u;
+        const bool in = step < nsteps && q < Lq;
+        nl[u] = in ? lse[q] * kLog2e : INFINITY;
+        nd[u] = in ? delta[q] : 0.f;
+      }
+    };
+    fetch(0);
     int s = 0;
     for (; s < nsteps; ++s) {
       const int stage = s & 1, round = s >> 1;
-      bool ok = true;
-      if (lane == 0 && round > 0) ok = mbar_wait(&bars->empty[stage], (round - 1) & 1, abort_flag, p.status);
+      bool ok = !*abort_flag;
+      if (ok && lane == 0 && round > 0) ok = mbar_wait(&bars->empty[stage], (round - 1) & 1, abort_flag, p.status);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       const int q0 = (i0 + s) * BQ;
-      float* st = stat + stage * 2 * BQ;
-      for (int c = lane; c < BQ; c += 32) {
-        const int q = q0 + c;
-        st[c] = q < Lq ? lse[q] * kLog2e : INFINITY;
-        st[BQ + c] = q < Lq ? delta[q] : 0.f;
-      }
       if (lane == 0) {
-        mbar_expect_tx(&bars->full[stage], 2 * C::kQTile);
+        mbar_expect_tx_only(&bars->full[stage], 2 * C::kQTile);
         for (int cb = 0; cb < C::kNBlk; ++cb) {
           tma_load_3d(smem + C::kOffQ + stage * C::kQTile + cb * C::kQColBlk, &tmQ, &bars->full[stage],
                       cb * C::kBlk, q0, unit);
           tma_load_3d(smem + C::kOffDO + stage * C::kQTile + cb * C::kQColBlk, &tmDO, &bars->full[stage],
                       cb * C::kBlk, q0, unit);
         }
-      } else {
-        mbar_arrive(&bars->full[stage]);
       }
+      float* st = stat + stage * 2 * BQ;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        st[lane + 32 * u] = nl[u];
+        st[BQ + lane + 32 * u] = nd[u];
+      }
+      mbar_arrive(&bars->full[stage]);
+      fetch(s + 1);
     }
     if (lane == 0 && *abort_flag) {
       mbar_wait_drain(&bars->kv, 0);
       for (int f = max(0, s - 2); f < s; ++f) mbar_wait_drain(&bars->full[f & 1], (f >> 1) & 1);
     }
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaSWarp || warp == kMmaGWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
-      constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BK, BQ);            // S^T, dP^T: M = keys, N = queries
-      constexpr uint32_t idKV = idesc_f16(fmt, 0, 1, BK, D);            // dV, dK: M = keys, N = D
-      constexpr uint32_t idQ = C::kDqT ? idesc_f16(fmt, 1, 1, D, BQ)    // dQ^T: M = D, N = queries
-                                       : idesc_f16(fmt, 1, 1, BQ, D);   // dQ: M = queries, N = D
-      bool ok = mbar_wait(&bars->kv, 0, abort_flag, p.status);
-      for (int s = 0; s < nsteps && ok; ++s) {
-        const int stage = s & 1;
-        if (!(ok = mbar_wait(&bars->full[stage], (s >> 1) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        const uint32_t q = sQ + stage * C::kQTile, dO = sDO + stage * C::kQTile;
-        // S^T = K Q^T and dP^T = V dO^T (K-major operands, contraction over D)
+      auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort_flag, p.status); };
+      bool ok = wait(&bars->kv, 0);
+      if (warp == kMmaSWarp) {
+        // S^T = K Q^T and dP^T = V dO^T (K-major operands, contraction over D),
+        // and the dQ partial of the previous tile
+        constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BK, BQ);
+        constexpr uint32_t idQ = C::kDqT ? idesc_f16(fmt, 1, 1, D, BQ)    // dQ^T: M = D, N = queries
+                                         : idesc_f16(fmt, 1, 1, BQ, D);   // dQ: M = queries, N = D
+        const uint64_t dKm = smem_desc(sK, C::kKColBlk, C::kSbo, C::kSw);
+        const uint64_t dDSm = smem_desc(sDST, C::kPColBlk, 1024, kSwizzle128B);
+        auto issue_dq = [&](int t) {
+          if (!wait(&bars->pds_full, t & 1)) return false;
+          const int buf = t & 1;
+          if (t >= 2 && !wait(&bars->dq_free[buf], ((t - 2) >> 1) & 1)) return false;
+          tc_fence_after();
+          const uint32_t tdq = tmem + C::kTdQ + buf * C::kDqCols;
+          // contraction over the 128 keys, both operands MN-major
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t cb = ks * 16 / C::kBlk, within = (ks * 16 % C::kBlk) * 2;
-          mma_ss(tmem + C::kTS, smem_desc(sK + cb * C::kKColBlk + within, 16, C::kSbo, C::kSw),
-                 smem_desc(q + cb * C::kQColBlk + within, 16, C::kSbo, C::kSw), idS, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t cb = ks * 16 / C::kBlk, within = (ks * 16 % C::kBlk) * 2;
-          mma_ss(tmem + C::kTdP, smem_desc(sV + cb * C::kKColBlk + within, 16, C::kSbo, C::kSw),
-                 smem_desc(dO + cb * C::kQColBlk + within, 16, C::kSbo, C::kSw), idS, ks > 0);
-        }
-        mma_commit(&bars->s);
-        if (!(ok = mbar_wait(&bars->p, s & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q (A K-major over queries, B MN-major)
-#pragma unroll
-        for (int ks = 0; ks < BQ / 16; ++ks) {
-          const uint32_t aoff = (ks / 4) * C::kPColBlk + (ks % 4) * 32;
-          const uint32_t boff = ks * 16 * C::kRowBytes;
-          const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
-          mma_ss(tmem + C::kTdV, smem_desc(sPT + aoff, 16, 1024, kSwizzle128B),
-                 smem_desc(dO + boff, C::kQColBlk, C::kSbo, C::kSw), idKV, acc);
-          mma_ss(tmem + C::kTdK, smem_desc(sDST + aoff, 16, 1024, kSwizzle128B),
-                 smem_desc(q + boff, C::kQColBlk, C::kSbo, C::kSw), idKV, acc);
-        }
-        if (s > 0 && !(ok = mbar_wait(&bars->dq_free, (s - 1) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        // dQ partial: contraction over the 128 keys, both operands MN-major
-#pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks) {
-          const uint32_t kb_off = ks * 16 * C::kRowBytes;   // 16 key rows of the K tile
-          const uint32_t ds_off = ks * 16 * 128;            // 16 key rows of dS^T
-          if (C::kDqT) {
-            mma_ss(tmem + C::kTdQ, smem_desc(sK + kb_off, C::kKColBlk, C::kSbo, C::kSw),
-                   smem_desc(sDST + ds_off, C::kPColBlk, 1024, kSwizzle128B), idQ, ks > 0);
-          } else {
-            mma_ss(tmem + C::kTdQ, smem_desc(sDST + ds_off, C::kPColBlk, 1024, kSwizzle128B),
-                   smem_desc(sK + kb_off, C::kKColBlk, C::kSbo, C::kSw), idQ, ks > 0);
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            const uint32_t kb_off = (ks * 16 * C::kRowBytes) >> 4;   // 16 key rows of the K tile
+            const uint32_t ds_off = (ks * 16 * 128) >> 4;            // 16 key rows of dS^T
+            if (C::kDqT) mma_ss(tdq, dKm + kb_off, dDSm + ds_off, idQ, ks > 0);
+            else mma_ss(tdq, dDSm + ds_off, dKm + kb_off, idQ, ks > 0);
           }
+          mma_commit(&bars->dq_full[buf]);
+          mma_commit(&bars->pds_free);
+          return true;
+        };
+        const uint64_t dK0 = smem_desc(sK, 16, C::kSbo, C::kSw);
+        const uint64_t dV0 = smem_desc(sV, 16, C::kSbo, C::kSw);
+        const uint64_t dQ0 = smem_desc(sQ, 16, C::kSbo, C::kSw);
+        const uint64_t dO0 = smem_desc(sDO, 16, C::kSbo, C::kSw);
+        for (int s = 0; s < nsteps && ok; ++s) {
+          const int stage = s & 1;
+          if (!(ok = wait(&bars->full[stage], (s >> 1) & 1))) break;
+          if (s > 0 && !(ok = wait(&bars->s_free, (s - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t qoff = (stage * C::kQTile) >> 4;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t cb = ks * 16 / C::kBlk, within = (ks * 16 % C::kBlk) * 2;
+            const uint32_t ko = (cb * C::kKColBlk + within) >> 4, qo = qoff + ((cb * C::kQColBlk + within) >> 4);
+            mma_ss(tmem + C::kTS, dK0 + ko, dQ0 + qo, idS, ks > 0);
+          }
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t cb = ks * 16 / C::kBlk, within = (ks * 16 % C::kBlk) * 2;
+            const uint32_t ko = (cb * C::kKColBlk + within) >> 4, qo = qoff + ((cb * C::kQColBlk + within) >> 4);
+            mma_ss(tmem + C::kTdP, dV0 + ko, dO0 + qo, idS, ks > 0);
+          }
+          mma_commit(&bars->s_full);
+          // dQ of the previous tile: needs its dS^T and a free dQ buffer
+          if (s > 0 && !(ok = issue_dq(s - 1))) break;
         }
-        mma_commit(&bars->dq_full);
-        mma_commit(&bars->empty[stage]);
+        if (ok && nsteps > 0) ok = issue_dq(nsteps - 1);
+      } else {
+        // dV += P^T dO, dK += dS^T Q (A K-major over queries, B MN-major)
+        constexpr uint32_t idKV = idesc_f16(fmt, 0, 1, BK, D);
+        const uint64_t dPT = smem_desc(sPT, 16, 1024, kSwizzle128B);
+        const uint64_t dDST = smem_desc(sDST, 16, 1024, kSwizzle128B);
+        const uint64_t dQm = smem_desc(sQ, C::kQColBlk, C::kSbo, C::kSw);
+        const uint64_t dOm = smem_desc(sDO, C::kQColBlk, C::kSbo, C::kSw);
+        for (int s = 0; s < nsteps && ok; ++s) {
+          const int stage = s & 1;
+          if (!(ok = wait(&bars->pds_full, s & 1))) break;
+          tc_fence_after();
+          const uint32_t qoff = (stage * C::kQTile) >> 4;
+#pragma unroll
+          for (int ks = 0; ks < BQ / 16; ++ks) {
+            const uint32_t aoff = ((ks / 4) * C::kPColBlk + (ks % 4) * 32) >> 4;
+            const uint32_t boff = qoff + ((ks * 16 * C::kRowBytes) >> 4);
+            const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
+            mma_ss(tmem + C::kTdV, dPT + aoff, dOm + boff, idKV, acc);
+            mma_ss(tmem + C::kTdK, dDST + aoff, dQm + boff, idKV, acc);
+          }
+          mma_commit(&bars->pds_free);
+          mma_commit(&bars->empty[stage]);
+        }
+        mma_commit(&bars->kv_done);
       }
-      mma_commit(&bars->kv_done);
       mma_commit(&bars->done);
       mbar_wait_drain(&bars->done, 0);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------ P^T and dS^T, then dV
-    const int r = threadIdx.x & 127;                         // key row == TMEM lane
-    const int key = key0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const float c = p.scale * kLog2e;
-    bool ok = true;
-    for (int s = 0; s < nsteps; ++s) {
-      const int stage = s & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s, s & 1, abort_flag, p.status) &&
-                                       mbar_wait(&bars->full[stage], (s >> 1) & 1, abort_flag, p.status));
-      if (!ok) break;
-      tc_fence_after();
-      const int q0 = (i0 + s) * BQ;
-      const float* lse2 = stat + stage * 2 * BQ;
-      const float* dl = lse2 + BQ;
-      const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
-#pragma unroll 1
-      for (int cc = 0; cc < BQ / 32; ++cc) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tmem + lane_off + C::kTS + cc * 32, sv);
-        tmem_ld32(tmem + lane_off + C::kTdP + cc * 32, dv);
-        tmem_ld_wait();
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pr[2], ds[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = cc * 32 + 2 * e + h;
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h]), c, -lse2[col]));
-            if (need_mask && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
-            pr[h] = pv;
-            ds[h] = pv * (__uint_as_float(dv[2 * e + h]) - dl[col]);
-          }
-          pk[e] = Pack2<T>::pack(pr[0], pr[1]);
-          dk[e] = Pack2<T>::pack(ds[0], ds[1]);
-        }
-        // [key row][query] in 128-byte swizzled rows, 64 queries per column block
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int chunk = cc * 4 + ch;           // 8-query chunk index
-          const uint32_t off = (chunk / 8) * C::kPColBlk + r * 128 + (((chunk % 8) ^ (r & 7)) << 4);
-          st_shared_v4(sPT + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-          st_shared_v4(sDST + off, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->p);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_done, 0, abort_flag, p.status));
-    if (ok) {
-      tc_fence_after();
-      T* dvrow = static_cast<T*>(bp.dv) + (static_cast<long long>(unit) * Lk + key) * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + C::kTdV + cc * 32, o);
-        tmem_ld_wait();
-        if (nsteps == 0) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (key < Lk) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = Pack2<T>::pack(__uint_as_float(o[8 * e + 0]), __uint_as_float(o[8 * e + 1]));
-            w.y = Pack2<T>::pack(__uint_as_float(o[8 * e + 2]), __uint_as_float(o[8 * e + 3]));
-            w.z = Pack2<T>::pack(__uint_as_float(o[8 * e + 4]), __uint_as_float(o[8 * e + 5]));
-            w.w = Pack2<T>::pack(__uint_as_float(o[8 * e + 6]), __uint_as_float(o[8 * e + 7]));
-            *reinterpret_cast<uint4*>(dvrow + cc * 32 + 8 * e) = w;
-          }
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------ dQ drain, then dK
+   } else if (warp < kDqWarp0 + 4) {
+    // ------------------------------------------------ dQ drain
     const int r = threadIdx.x & 127;                          // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* dq_unit = bp.dq_acc + static_cast<long long>(unit) * Lq * D;
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, s & 1, abort_flag, p.status));
+      const int buf = s & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full[buf], (s >> 1) & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
       const int q0 = (i0 + s) * BQ;
+      const uint32_t tdq = tmem + lane_off + C::kTdQ + buf * C::kDqCols;
       if (r == 0) bulk_wait_read0();          // the previous reduce has read the staging tile
       named_bar_sync(1, 128);
       if (C::kDqT) {
@@ -353,7 +339,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll 1
         for (int cc = 0; cc < BQ / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + C::kTdQ + cc * 32, o);
+          tmem_ld32(tdq + cc * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) st_shared_f32(sDQ + ((cc * 32 + e) * D + r) * 4, __uint_as_float(o[e]));
@@ -363,7 +349,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + C::kTdQ + cc * 32, o);
+          tmem_ld32(tdq + cc * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -371,7 +357,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->dq_free);
+      mbar_arrive(&bars->dq_free[buf]);
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (r == 0) {
@@ -381,16 +367,83 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       }
     }
     if (r == 0) bulk_wait0();
+   }
+  } else {
+    regs_inc<kRegsSoftmax>();
+    // ------------------------------------------------ P^T and dS^T, then dV / dK
+    const int half = warp / 4;                                // query columns [half * kHalf, +kHalf)
+    const int r = threadIdx.x & 127;                          // key row == TMEM lane
+    const int key = key0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c = p.scale * kLog2e;
+    constexpr int NH = C::kHalf;
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      const int stage = s & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, abort_flag, p.status) &&
+                                       mbar_wait(&bars->full[stage], (s >> 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[NH], dv[NH];
+#pragma unroll
+      for (int cc = 0; cc < NH / 32; ++cc) {
+        tmem_ld32(tmem + lane_off + C::kTS + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[cc * 32]));
+        tmem_ld32(tmem + lane_off + C::kTdP + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[cc * 32]));
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);               // the next S^T / dP^T may be written
+      const int q0 = (i0 + s) * BQ + half * NH;
+      const uint32_t sl = smem_u32(stat + stage * 2 * BQ + half * NH);   // lse2 of this half
+      const uint32_t sd = sl + BQ * 4;                                     // delta of this half
+      const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
+      uint32_t pk[NH / 2], dk[NH / 2];
+#pragma unroll
+      for (int g = 0; g < NH / 4; ++g) {
+        float l4[4], d4[4];
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(l4[0]), "=f"(l4[1]), "=f"(l4[2]), "=f"(l4[3]) : "r"(sl + g * 16));
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(d4[0]), "=f"(d4[1]), "=f"(d4[2]), "=f"(d4[3]) : "r"(sd + g * 16));
+        float pr[4], ds[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int col = 4 * g + h;
+          float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, -l4[h]));
+          if (need_mask && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
+          pr[h] = pv;
+          ds[h] = pv * (__uint_as_float(dv[col]) - d4[h]);
+        }
+        pk[2 * g] = Pack2<T>::pack(pr[0], pr[1]);
+        pk[2 * g + 1] = Pack2<T>::pack(pr[2], pr[3]);
+        dk[2 * g] = Pack2<T>::pack(ds[0], ds[1]);
+        dk[2 * g + 1] = Pack2<T>::pack(ds[2], ds[3]);
+      }
+      // P^T / dS^T buffers are free once the previous tile's dV, dK, dQ MMAs finished
+      if (s > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_free, (s - 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      // [key row][query] in 128-byte swizzled rows, 64 queries per column block
+#pragma unroll
+      for (int ch = 0; ch < NH / 8; ++ch) {
+        const int chunk = half * (NH / 8) + ch;    // 8-query chunk index within the tile
+        const uint32_t off = (chunk / 8) * C::kPColBlk + r * 128 + (((chunk % 8) ^ (r & 7)) << 4);
+        st_shared_v4(sPT + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        st_shared_v4(sDST + off, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->pds_full);
+    }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_done, 0, abort_flag, p.status));
     if (ok) {
+      // group 0 writes dV, group 1 writes dK = scale * dK_acc
       tc_fence_after();
-      const int key = key0 + r;
-      T* dkrow = static_cast<T*>(bp.dk) + (static_cast<long long>(unit) * Lk + key) * D;
-      const float sc = p.scale;
+      const uint32_t col0 = half == 0 ? C::kTdV : C::kTdK;
+      const float sc = half == 0 ? 1.f : p.scale;
+      T* out = static_cast<T*>(half == 0 ? bp.dv : bp.dk) + (static_cast<long long>(unit) * Lk + key) * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + C::kTdK + cc * 32, o);
+        tmem_ld32(tmem + lane_off + col0 + cc * 32, o);
         tmem_ld_wait();
         if (nsteps == 0) {
 #pragma unroll
@@ -404,7 +457,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             w.y = Pack2<T>::pack(__uint_as_float(o[8 * e + 2]) * sc, __uint_as_float(o[8 * e + 3]) * sc);
             w.z = Pack2<T>::pack(__uint_as_float(o[8 * e + 4]) * sc, __uint_as_float(o[8 * e + 5]) * sc);
             w.w = Pack2<T>::pack(__uint_as_float(o[8 * e + 6]) * sc, __uint_as_float(o[8 * e + 7]) * sc);
-            *reinterpret_cast<uint4*>(dkrow + cc * 32 + 8 * e) = w;
+            *reinterpret_cast<uint4*>(out + cc * 32 + 8 * e) = w;
           }
         }
       }
@@ -413,9 +466,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaSWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(bars->tmem_base, kTmemCols);
   }
 }
 
@@ -429,6 +482,12 @@ cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
   if (dev < 64 && !attr_set[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem);
     if (e != cudaSuccess) return e;
+    // setmaxnreg redistributes the registers the block is launched with; a
+    // split larger than that would wait forever, so refuse to launch instead
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < static_cast<int>(256 * kRegsSoftmax + 256 * kRegsOther)) return cudaErrorInvalidConfiguration;
     attr_set[dev] = 1;
   }
   const Problem& p = bp.f;

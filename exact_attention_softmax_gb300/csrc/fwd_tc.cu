@@ -576,6 +576,12 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
   if (dev < 64 && !attr_set[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
     if (e != cudaSuccess) return e;
+    // setmaxnreg redistributes the registers the block is launched with; a
+    // split larger than that would wait forever, so refuse to launch instead
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * Cfg<D>::kThreads < static_cast<int>(256 * kRegsSoftmax + 128 * kRegsControl)) return cudaErrorInvalidConfiguration;
     attr_set[dev] = 1;
   }
   static int sm_count[64] = {0};
