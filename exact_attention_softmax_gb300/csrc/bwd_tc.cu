@@ -12,8 +12,8 @@
 //   dQ_i partial = dS K   (d = 64: M = query rows)
 //             or  (K^T dS^T)^T (d = 128: M = head dims)       (tcgen05, TMEM)
 //
-// and the dQ partial is added into an fp32 accumulator in global memory with
-// one bulk shared->global reduce per tile. dK = scale * dK_acc and dV are
+// and the dQ partial is added into an fp32 accumulator in global memory (one
+// bulk shared->global reduce per tile at d = 128, vector reductions at d = 64). dK = scale * dK_acc and dV are
 // written at the end; dQ = scale * dQ_acc is rounded by a separate kernel.
 //
 // Warps: 0-3 and 4-7 build P^T / dS^T for the first and second half of the
@@ -48,6 +48,10 @@ struct BCfg {
   static constexpr int BQ = D == 128 ? 64 : 128;            // query rows per step
   static constexpr int kHalf = BQ / 2;                       // query columns per softmax group
   static constexpr bool kDqT = D == 128;                     // dQ computed transposed
+  // Which MMA warp issues the dQ MMAs, so the two warps issue about as many
+  // MMAs per tile: d = 64 -> the S^T/dP^T warp (8 + 8 vs 16), d = 128 -> the
+  // dV/dK warp (16 vs 8 + 8).
+  static constexpr bool kDqOnS = D == 64;
   static constexpr int kBlk = D >= 64 ? 64 : D;
   static constexpr int kNBlk = D / kBlk;
   static constexpr uint32_t kSw = D >= 64 ? kSwizzle128B : kSwizzle64B;
@@ -59,7 +63,6 @@ struct BCfg {
   static constexpr int kQTile = BQ * D * 2;
   static constexpr int kPColBlk = BK * 128;                  // P^T / dS^T: [128 keys][64 queries] blocks
   static constexpr int kPBytes = BK * BQ * 2;
-  static constexpr int kDqBytes = BQ * D * 4;                // fp32 dQ staging tile
   static constexpr int kStages = 2;
   // shared memory map
   static constexpr int kOffK = 0;
@@ -68,6 +71,7 @@ struct BCfg {
   static constexpr int kOffDO = kOffQ + kStages * kQTile;               // kStages dO tiles
   static constexpr int kOffPT = kOffDO + kStages * kQTile;
   static constexpr int kOffDST = kOffPT + kPBytes;
+  static constexpr int kDqBytes = kDqT ? BQ * D * 4 : 0;     // fp32 dQ staging tile (d = 128 only)
   static constexpr int kOffDQ = kOffDST + kPBytes;
   static constexpr int kOffStat = kOffDQ + kDqBytes;                    // kStages x (lse2[BQ], delta[BQ])
   static constexpr int kOffBar = kOffStat + kStages * BQ * 8;
@@ -108,6 +112,9 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void red_add_v4_f32(float* gdst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 
 template <int D, typename T, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -136,7 +143,6 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
   const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
   const uint32_t sPT = smem_u32(smem + C::kOffPT), sDST = smem_u32(smem + C::kOffDST);
-  const uint32_t sDQ = smem_u32(smem + C::kOffDQ);
   float* stat = reinterpret_cast<float*>(smem + C::kOffStat);   // [stage][2][BQ]
 
   if (threadIdx.x == 0) {
@@ -238,32 +244,34 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
       auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort_flag, p.status); };
       bool ok = wait(&bars->kv, 0);
+      // dQ partial of tile t: contraction over the 128 keys, both operands MN-major
+      constexpr uint32_t idQ = C::kDqT ? idesc_f16(fmt, 1, 1, D, BQ)    // dQ^T: M = D, N = queries
+                                       : idesc_f16(fmt, 1, 1, BQ, D);   // dQ: M = queries, N = D
+      const uint64_t dKm = smem_desc(sK, C::kKColBlk, C::kSbo, C::kSw);
+      const uint64_t dDSm = smem_desc(sDST, C::kPColBlk, 1024, kSwizzle128B);
+      auto issue_dq = [&](int t) {
+        if (!wait(&bars->pds_full, t & 1)) return false;
+        const int buf = t & 1;
+        if (t >= 2 && !wait(&bars->dq_free[buf], ((t - 2) >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t tdq = tmem + C::kTdQ + buf * C::kDqCols;
+        // contraction over the 128 keys, both operands MN-major
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks) {
+          const uint32_t kb_off = (ks * 16 * C::kRowBytes) >> 4;   // 16 key rows of the K tile
+          const uint32_t ds_off = (ks * 16 * 128) >> 4;            // 16 key rows of dS^T
+          if (C::kDqT) mma_ss(tdq, dKm + kb_off, dDSm + ds_off, idQ, ks > 0);
+          else mma_ss(tdq, dDSm + ds_off, dKm + kb_off, idQ, ks > 0);
+        }
+        mma_commit(&bars->dq_full[buf]);
+        mma_commit(&bars->pds_free);
+        return true;
+      };
       if (warp == kMmaSWarp) {
         // S^T = K Q^T and dP^T = V dO^T (K-major operands, contraction over D),
         // and the dQ partial of the previous tile
         constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BK, BQ);
-        constexpr uint32_t idQ = C::kDqT ? idesc_f16(fmt, 1, 1, D, BQ)    // dQ^T: M = D, N = queries
-                                         : idesc_f16(fmt, 1, 1, BQ, D);   // dQ: M = queries, N = D
-        const uint64_t dKm = smem_desc(sK, C::kKColBlk, C::kSbo, C::kSw);
-        const uint64_t dDSm = smem_desc(sDST, C::kPColBlk, 1024, kSwizzle128B);
-        auto issue_dq = [&](int t) {
-          if (!wait(&bars->pds_full, t & 1)) return false;
-          const int buf = t & 1;
-          if (t >= 2 && !wait(&bars->dq_free[buf], ((t - 2) >> 1) & 1)) return false;
-          tc_fence_after();
-          const uint32_t tdq = tmem + C::kTdQ + buf * C::kDqCols;
-          // contraction over the 128 keys, both operands MN-major
-#pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) {
-            const uint32_t kb_off = (ks * 16 * C::kRowBytes) >> 4;   // 16 key rows of the K tile
-            const uint32_t ds_off = (ks * 16 * 128) >> 4;            // 16 key rows of dS^T
-            if (C::kDqT) mma_ss(tdq, dKm + kb_off, dDSm + ds_off, idQ, ks > 0);
-            else mma_ss(tdq, dDSm + ds_off, dKm + kb_off, idQ, ks > 0);
-          }
-          mma_commit(&bars->dq_full[buf]);
-          mma_commit(&bars->pds_free);
-          return true;
-        };
+
         const uint64_t dK0 = smem_desc(sK, 16, C::kSbo, C::kSw);
         const uint64_t dV0 = smem_desc(sV, 16, C::kSbo, C::kSw);
         const uint64_t dQ0 = smem_desc(sQ, 16, C::kSbo, C::kSw);
@@ -288,9 +296,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
           }
           mma_commit(&bars->s_full);
           // dQ of the previous tile: needs its dS^T and a free dQ buffer
-          if (s > 0 && !(ok = issue_dq(s - 1))) break;
+          if (C::kDqOnS && s > 0 && !(ok = issue_dq(s - 1))) break;
         }
-        if (ok && nsteps > 0) ok = issue_dq(nsteps - 1);
+        if (C::kDqOnS && ok && nsteps > 0) ok = issue_dq(nsteps - 1);
       } else {
         // dV += P^T dO, dK += dS^T Q (A K-major over queries, B MN-major)
         constexpr uint32_t idKV = idesc_f16(fmt, 0, 1, BK, D);
@@ -313,6 +321,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
           }
           mma_commit(&bars->pds_free);
           mma_commit(&bars->empty[stage]);
+          if (!C::kDqOnS && !(ok = issue_dq(s))) break;
         }
         mma_commit(&bars->kv_done);
       }
@@ -321,21 +330,24 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     }
    } else if (warp < kDqWarp0 + 4) {
     // ------------------------------------------------ dQ drain
+    // d = 128 (lane = head dim, columns = queries): staged as [query][D] in
+    // shared memory and added with one bulk shared->global reduce per tile.
+    // d = 64 (lane = query row): 16-byte vector reductions straight from the
+    // registers, which spares shared memory (the backward is bound by its
+    // bandwidth); with lane = head dim those would be scalar and slower.
     const int r = threadIdx.x & 127;                          // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* dq_unit = bp.dq_acc + static_cast<long long>(unit) * Lq * D;
-    bool ok = true;
+    const uint32_t sDQ = smem_u32(smem + C::kOffDQ);
     for (int s = 0; s < nsteps; ++s) {
       const int buf = s & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full[buf], (s >> 1) & 1, abort_flag, p.status));
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full[buf], (s >> 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
       const int q0 = (i0 + s) * BQ;
       const uint32_t tdq = tmem + lane_off + C::kTdQ + buf * C::kDqCols;
-      if (r == 0) bulk_wait_read0();          // the previous reduce has read the staging tile
-      named_bar_sync(1, 128);
       if (C::kDqT) {
-        // lane r = head dim r; columns = BQ queries -> staging [query][D]
+        if (r == 0) bulk_wait_read0();          // the previous reduce has read the staging tile
+        named_bar_sync(1, 128);
 #pragma unroll 1
         for (int cc = 0; cc < BQ / 32; ++cc) {
           uint32_t o[32];
@@ -344,29 +356,36 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll
           for (int e = 0; e < 32; ++e) st_shared_f32(sDQ + ((cc * 32 + e) * D + r) * 4, __uint_as_float(o[e]));
         }
+        tc_fence_before();
+        mbar_arrive(&bars->dq_free[buf]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (r == 0) {
+          const int rows = min(BQ, Lq - q0);
+          bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0) * D, sDQ, static_cast<uint32_t>(rows * D * 4));
+          bulk_commit();
+        }
       } else {
-        // lane r = query row r; columns = D -> staging [query][D]
+        const int q = q0 + r;
+        float* row = dq_unit + static_cast<long long>(q) * D;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(tdq + cc * 32, o);
           tmem_ld_wait();
+          if (cc == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bars->dq_free[buf]);
+          }
+          if (q < Lq) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            st_shared_v4(sDQ + (r * D + cc * 32 + e * 4) * 4, o[e * 4], o[e * 4 + 1], o[e * 4 + 2], o[e * 4 + 3]);
+            for (int e = 0; e < 8; ++e)
+              red_add_v4_f32(row + cc * 32 + e * 4, o[e * 4], o[e * 4 + 1], o[e * 4 + 2], o[e * 4 + 3]);
+          }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free[buf]);
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (r == 0) {
-        const int rows = min(BQ, Lq - q0);
-        bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0) * D, sDQ, static_cast<uint32_t>(rows * D * 4));
-        bulk_commit();
-      }
     }
-    if (r == 0) bulk_wait0();
+    if (C::kDqT && r == 0) bulk_wait0();
    }
   } else {
     regs_inc<kRegsSoftmax>();
