@@ -42,6 +42,9 @@ HEADLINE = "dense_f16_d32"
 PAGES_TFLOPS = 4.0 * 32 * 32 * 1024 * 1024 * 32 / 2262.901e-6 / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+# ex2 results per clock per SM on GB300, inferred from ncu: the XU pipe is 40 %
+# busy while the d = 32 forward issues 11.7 ex2 per clock per SM.
+EX2_PER_CLK_SM = 32
 
 
 def load_peaks():
@@ -188,6 +191,22 @@ def oracle_sample(w, x, budget_s, max_units=None):
             break
     desc = f"{n} of {len(units)} (unit, head) slices of {w.name}, forward, fp64 NumPy"
     return done_flops, t_total, desc
+
+
+def reduce_max_ms(ms, world, device=None):
+    """Largest value of ``ms`` over all ranks (the slowest replica sets the job time)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_step, steps, max_ms):
+    """Aggregate throughput: every rank processes its own replica of the workload."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
 
 
 def host_cores():
@@ -345,11 +364,7 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     kernel_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(kernel_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_ms(sum(kernel_ms), world, dev)
     ops.sdpa_device_status()
 
     # ---- end to end: pinned host inputs in, outputs out, inside the timed region
@@ -390,21 +405,35 @@ def run_ours(args):
         e2e_step()
     b.record(stream)
     barrier()
-    e2e_ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max_ms(a.elapsed_time(b), world, dev)
 
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, args.steps, total_ms)
     # the end-to-end step always runs the forward (the backward needs its O and LSE)
     e2e_flops = flops + (wl.fwd_flops(w, lengths) if not do_fwd else 0.0)
-    e2e_value = world * e2e_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = whole_job_tflops(world, e2e_flops, e2e_steps, e2e_ms)
     avg_kernel_s = statistics.mean(kernel_ms) * 1e-3
     kern_file = "fwd_tc.cu" if do_fwd and not do_bwd else "bwd_tc.cu"
     kern_name = "fwd_tc_kernel" if kern_file == "fwd_tc.cu" else "bwd_tc_kernel"
     achieved = flops / avg_kernel_s / 1e12
     traffic = profiled_traffic(kern_file, args.workload)
+    # Two ceilings for the dominant kernel: the tensor cores (measured dense
+    # bf16 peak; fp16 has the same rate) and, for the forward, the exponential
+    # unit: one ex2 per score element, 4*d algorithmic flops per score element,
+    # EX2_PER_CLK_SM results per clock per SM.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk_mhz = clk.get("sm_max_mhz") or 2070
+    exp_ceiling = 4.0 * w.d * EX2_PER_CLK_SM * sms * clk_mhz * 1e6 / 1e12
+    if do_fwd and not do_bwd and exp_ceiling < peaks["bf16_tflops"]:
+        roof = {"kernel": kern_name, "bound": "alu", "achieved": round(achieved, 2), "peak": round(exp_ceiling, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / exp_ceiling, 4),
+                "peak_source": f"exponential unit: {EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {clk_mhz} MHz, "
+                               f"{4 * w.d} flop per score element",
+                "tensor_peak": peaks["bf16_tflops"], "tensor_frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic}
+    else:
+        roof = {"kernel": kern_name, "bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": f"{peak_kind} dense bf16 burst (fp16 has the same tensor rate)", "traffic": traffic}
     shape = (f"B={w.B} H={w.H} Lq={w.Lq} Lk={w.Lk} d={w.d}" if not w.varlen else
              f"{w.nseq} packed sequences (max {w.max_len}, total {x['q'].shape[0]}) H={w.H} d={w.d}")
     line = {
@@ -426,11 +455,7 @@ def run_ours(args):
                                f"{'causal' if w.causal else 'non-causal'} {args.passes}",
                    "flops_per_step": flops, "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas x{world} (one independent problem per GPU)"},
-        "roofline": {"kernel": kern_name, "bound": "tensor", "achieved": round(achieved, 2),
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "peak_source": f"{peak_kind} dense bf16 burst (fp16 has the same tensor rate)",
-                     "traffic": traffic},
+        "roofline": roof,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps * launches_per_step,
