@@ -192,9 +192,10 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
   if (!dO || !dq || !dk || !dv) return fail(SDPA_ERR_ARG, "null gradient pointer");
   if (dtype != SDPA_F32 && !(aligned16(dO) && aligned16(dq) && aligned16(dk) && aligned16(dv)))
     return fail(SDPA_ERR_ARG, "fp16/bf16 gradients must be 16-byte aligned");
-  if (cu_seqlens != nullptr) return fail(SDPA_ERR_UNSUPPORTED, "packed (cu_seqlens) backward is not implemented");
   if (dtype != SDPA_F32 && d == 32) return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 backward supports d in {64, 128}");
-  const size_t need = sdpa_bwd_workspace_size(B, H, Lq, d, dtype);
+  const bool packed = cu_seqlens != nullptr;
+  // packed: the row statistics and dQ accumulator cover the `Lq` = total tokens
+  const size_t need = sdpa_bwd_workspace_size(packed ? 1 : B, H, Lq, d, dtype);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace == nullptr ? 0 : workspace_bytes);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(SDPA_ERR_ARG, "workspace must be 256-byte aligned");
@@ -208,7 +209,7 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
-  const size_t rows = static_cast<size_t>(B) * H * Lq;
+  const size_t rows = static_cast<size_t>(packed ? 1 : B) * H * Lq;
   bp.delta = static_cast<float*>(workspace);
   bp.dq_acc = dtype == SDPA_F32 ? nullptr
                                 : reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * 4 + 255) / 256 * 256);
@@ -224,10 +225,11 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
   if (rc != SDPA_OK) return rc;
   BwdMaps maps;
   const uint32_t bq = d == 128 ? 64 : 128;  // query rows per backward step
-  if ((rc = make_operand_map(&maps.q, q, dtype, false, B, H, Lq, d, bq)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.k, k, dtype, false, B, H, Lk, d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.v, v, dtype, false, B, H, Lk, d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.dO, dO, dtype, false, B, H, Lq, d, bq)) != SDPA_OK) return rc;
+  const int rk = packed ? Lq : Lk;   // packed: keys share the token axis of the queries
+  if ((rc = make_operand_map(&maps.q, q, dtype, packed, B, H, Lq, d, bq)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.k, k, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.v, v, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.dO, dO, dtype, packed, B, H, Lq, d, bq)) != SDPA_OK) return rc;
   e = launch_bwd_tc(bp, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward (tensor-core) launch");
   e = launch_dq_convert(bp, dtype, s);

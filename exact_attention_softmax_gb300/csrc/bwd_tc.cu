@@ -116,7 +116,7 @@ __device__ __forceinline__ void red_add_v4_f32(float* gdst, uint32_t a, uint32_t
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int D, typename T, bool CAUSAL>
+template <int D, typename T, bool CAUSAL, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO) {
@@ -131,11 +131,26 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   // Unit-major order: the key blocks of one (batch, head) run side by side and
   // share its Q / dO through L2; under causal masking key block 0 (the most
   // query tiles) goes first.
+  // Packed batches: a unit is (sequence, head), rows cu_seqlens[s] .. +len of
+  // the token axis, and p.Lk bounds every length.
   const int nkb = (p.Lk + BK - 1) / BK;
   const int unit = blockIdx.x / nkb;
   const int kblk = blockIdx.x % nkb;
   const int key0 = kblk * BK;
-  const int Lq = p.Lq, Lk = p.Lk;
+  int Lq = p.Lq, Lk = p.Lk, tok0 = 0, head = 0;
+  if (PACKED) {
+    const int sq = unit / p.H;
+    head = unit % p.H;
+    tok0 = p.cu_seqlens[sq];
+    Lq = Lk = p.cu_seqlens[sq + 1] - tok0;
+    if (Lq > p.Lk && kblk == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+  }
+  if (key0 >= Lk) return;
+  // element offset of row 0 of this unit, stride between rows, and offset of
+  // its row statistics (dense: [B,H,L,d] and [B,H,L]; packed: [total,H,d] and [H,total])
+  const long long row0 = PACKED ? (static_cast<long long>(tok0) * p.H + head) * D : 0;
+  const long long rstride = PACKED ? static_cast<long long>(p.H) * D : D;
+  const long long stat0 = PACKED ? static_cast<long long>(head) * p.Lq + tok0 : static_cast<long long>(unit) * Lq;
   const int nq = (Lq + BQ - 1) / BQ;
   const int i0 = CAUSAL ? min(nq, key0 / BQ) : 0;
   const int nsteps = nq - i0;
@@ -187,13 +202,14 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
       mbar_expect_tx(&bars->kv, 2 * C::kKTile);
+      const int c1 = PACKED ? head : key0, c2 = PACKED ? tok0 + key0 : unit;
       for (int cb = 0; cb < C::kNBlk; ++cb) {
-        tma_load_3d(smem + C::kOffK + cb * C::kKColBlk, &tmK, &bars->kv, cb * C::kBlk, key0, unit);
-        tma_load_3d(smem + C::kOffV + cb * C::kKColBlk, &tmV, &bars->kv, cb * C::kBlk, key0, unit);
+        tma_load_3d(smem + C::kOffK + cb * C::kKColBlk, &tmK, &bars->kv, cb * C::kBlk, c1, c2);
+        tma_load_3d(smem + C::kOffV + cb * C::kKColBlk, &tmV, &bars->kv, cb * C::kBlk, c1, c2);
       }
     }
-    const float* lse = p.lse + static_cast<long long>(unit) * Lq;
-    const float* delta = bp.delta + static_cast<long long>(unit) * Lq;
+    const float* lse = p.lse + stat0;
+    const float* delta = bp.delta + stat0;
     // The row statistics of step s + 1 are fetched into registers while step s
     // is in flight, so their latency hides behind the wait for a free stage.
     constexpr int kPer = BQ / 32;
@@ -218,11 +234,12 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       const int q0 = (i0 + s) * BQ;
       if (lane == 0) {
         mbar_expect_tx_only(&bars->full[stage], 2 * C::kQTile);
+        const int c1 = PACKED ? head : q0, c2 = PACKED ? tok0 + q0 : unit;
         for (int cb = 0; cb < C::kNBlk; ++cb) {
           tma_load_3d(smem + C::kOffQ + stage * C::kQTile + cb * C::kQColBlk, &tmQ, &bars->full[stage],
-                      cb * C::kBlk, q0, unit);
+                      cb * C::kBlk, c1, c2);
           tma_load_3d(smem + C::kOffDO + stage * C::kQTile + cb * C::kQColBlk, &tmDO, &bars->full[stage],
-                      cb * C::kBlk, q0, unit);
+                      cb * C::kBlk, c1, c2);
         }
       }
       float* st = stat + stage * 2 * BQ;
@@ -337,7 +354,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     // bandwidth); with lane = head dim those would be scalar and slower.
     const int r = threadIdx.x & 127;                          // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float* dq_unit = bp.dq_acc + static_cast<long long>(unit) * Lq * D;
+    float* dq_unit = bp.dq_acc + (PACKED ? row0 : static_cast<long long>(unit) * Lq * D);
     const uint32_t sDQ = smem_u32(smem + C::kOffDQ);
     for (int s = 0; s < nsteps; ++s) {
       const int buf = s & 1;
@@ -362,12 +379,18 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         named_bar_sync(1, 128);
         if (r == 0) {
           const int rows = min(BQ, Lq - q0);
-          bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0) * D, sDQ, static_cast<uint32_t>(rows * D * 4));
+          if (!PACKED) {
+            bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0) * D, sDQ, static_cast<uint32_t>(rows * D * 4));
+          } else {
+            // packed rows are H * D apart: one reduce per row
+            for (int q = 0; q < rows; ++q)
+              bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0 + q) * rstride, sDQ + q * D * 4, D * 4);
+          }
           bulk_commit();
         }
       } else {
         const int q = q0 + r;
-        float* row = dq_unit + static_cast<long long>(q) * D;
+        float* row = dq_unit + static_cast<long long>(q) * rstride;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -458,7 +481,8 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       tc_fence_after();
       const uint32_t col0 = half == 0 ? C::kTdV : C::kTdK;
       const float sc = half == 0 ? 1.f : p.scale;
-      T* out = static_cast<T*>(half == 0 ? bp.dv : bp.dk) + (static_cast<long long>(unit) * Lk + key) * D;
+      T* out = static_cast<T*>(half == 0 ? bp.dv : bp.dk) +
+               (PACKED ? row0 + static_cast<long long>(key) * rstride : (static_cast<long long>(unit) * Lk + key) * D);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -491,9 +515,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   }
 }
 
-template <int D, typename T, bool CAUSAL>
+template <int D, typename T, bool CAUSAL, bool PACKED>
 cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
-  auto kern = bwd_tc_kernel<D, T, CAUSAL>;
+  auto kern = bwd_tc_kernel<D, T, CAUSAL, PACKED>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -519,13 +543,14 @@ cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
 
 template <int D, typename T>
 cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
-  return bp.f.causal ? launch_one<D, T, true>(bp, m, s) : launch_one<D, T, false>(bp, m, s);
+  if (bp.f.cu_seqlens != nullptr)
+    return bp.f.causal ? launch_one<D, T, true, true>(bp, m, s) : launch_one<D, T, false, true>(bp, m, s);
+  return bp.f.causal ? launch_one<D, T, true, false>(bp, m, s) : launch_one<D, T, false, false>(bp, m, s);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_tc(const BwdProblem& bp, int dtype, const BwdMaps& m, cudaStream_t s) {
-  if (bp.f.cu_seqlens != nullptr) return cudaErrorNotSupported;
   if (dtype == kF16) {
     if (bp.f.d == 64) return launch_d<64, __half>(bp, m, s);
     if (bp.f.d == 128) return launch_d<128, __half>(bp, m, s);

@@ -98,9 +98,9 @@ size_t sdpa_bwd_workspace_size(int B, int H, int Lq, int d, int dtype);
  *   dq, dk, dv : outputs, layouts of q, k, v; fully overwritten.
  *   workspace : device scratch of at least sdpa_bwd_workspace_size() bytes,
  *               256-byte aligned; its contents on entry do not matter.
- * Other arguments as for sdpa_fwd. Supported: F32 with d <= 128; F16/BF16
- * with d in {64, 128}; packed (cu_seqlens != NULL) batches return
- * SDPA_ERR_UNSUPPORTED in this version.
+ * Other arguments as for sdpa_fwd, dense or packed (cu_seqlens != NULL; the
+ * workspace is then sized with B = 1 and Lq = total). Supported: F32 with
+ * d <= 128; F16/BF16 with d in {64, 128}.
  */
 int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dO, void* dq, void* dk, void* dv,

@@ -75,6 +75,25 @@ def run_fwd_bwd(x, causal, scale):
     return f64(o), f64(lse), f64(dq), f64(dk), f64(dv)
 
 
+def run_fwd_bwd_packed(x, causal, scale):
+    """Packed fwd + bwd through the C ABI; returns (O, LSE, dQ, dK, dV) as float64."""
+    dev = cuda()
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    kw = dict(cu_seqlens=x["cu_seqlens"].to(dev), max_seqlen=max(x["max_seqlen"], 1))
+    o, lse = ops.sdpa_fwd(q, k, v, scale=scale, is_causal=causal, **kw)
+    gb = [guarded_empty(tuple(t.shape), t.dtype, dev) for t in (q, k, v)]
+    dq, dk, dv = ops.sdpa_bwd(q, k, v, o, lse, do, gb[0][1], gb[1][1], gb[2][1], scale=scale, is_causal=causal, **kw)
+    assert ops.sdpa_device_status() == 0
+    for b, _ in gb:
+        check_guard(b)
+    return f64(o), f64(lse), f64(dq), f64(dk), f64(dv)
+
+
+def oracle_bwd_packed(x, causal, scale):
+    q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
+    return attn_bwd_ref(q, k, v, do, scale, causal, x["cu_seqlens"].numpy())
+
+
 def oracle_fwd(x, causal, scale, packed=False):
     q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
     return attn_fwd_ref(q, k, v, scale, causal, x["cu_seqlens"].numpy() if packed else None)

@@ -87,9 +87,11 @@ def test_workspace_size_and_errors(lib):
     assert lib.sdpa_bwd(*args, FAKE, 16, None) == _abi.SDPA_ERR_WORKSPACE
     assert lib.sdpa_bwd(*args, None, 1 << 40, None) == _abi.SDPA_ERR_WORKSPACE
     assert b"workspace" in lib.sdpa_last_error()
-    # packed backward is not in this version
-    args_p = [FAKE] * 9 + [2, H, 100, 64, d, 0.125, 0, FAKE, 1]
-    assert lib.sdpa_bwd(*args_p, FAKE, 1 << 30, None) == _abi.SDPA_ERR_UNSUPPORTED
+    # packed: the workspace covers the Lq = total packed tokens (B = 1 in the size query)
+    total = 700
+    need_p = lib.sdpa_bwd_workspace_size(1, H, total, d, 1)
+    args_p = [FAKE] * 9 + [5, H, total, 300, d, 0.125, 0, FAKE, 1]
+    assert lib.sdpa_bwd(*args_p, FAKE, need_p - 1, None) == _abi.SDPA_ERR_WORKSPACE
 
 
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -53,3 +53,21 @@ def test_d32_backward_is_rejected():
     with pytest.raises(ops.SdpaError) as e:
         ops.sdpa_bwd(q, k, v, o, lse, do)
     assert e.value.code == -2
+
+
+LENGTHS = [1, 0, 130, 7, 256, 300, 129]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_bwd(dtype, d, causal):
+    """Packed (variable-length) batches: rows of a tile that belong to the next
+    sequence must neither contribute nor receive gradients."""
+    from _gpu import (assert_fwd_close, assert_grads_close, oracle_bwd_packed, oracle_fwd,
+                      run_fwd_bwd_packed)
+    x = wl.varlen_inputs(LENGTHS, 3, d, dtype, "normal", seed=12)
+    scale = d ** -0.5
+    o, lse, dq, dk, dv = run_fwd_bwd_packed(x, causal, scale)
+    assert_fwd_close((o, lse), oracle_fwd(x, causal, scale, packed=True), dtype)
+    assert_grads_close((dq, dk, dv), oracle_bwd_packed(x, causal, scale), dtype)

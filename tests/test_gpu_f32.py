@@ -53,3 +53,12 @@ def test_f32_packed_fwd(causal):
     x = wl.varlen_inputs([1, 0, 130, 7, 256], 2, 16, "f32", "normal", seed=5)
     got = run_fwd(x, causal, 0.25, packed=True)
     assert_fwd_close(got, oracle_fwd(x, causal, 0.25, packed=True), "f32")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_packed_fwd_bwd(causal):
+    from _gpu import assert_fwd_close, assert_grads_close, oracle_bwd_packed, oracle_fwd, run_fwd_bwd_packed
+    x = wl.varlen_inputs([1, 0, 130, 7, 256], 2, 16, "f32", "normal", seed=6)
+    o, lse, dq, dk, dv = run_fwd_bwd_packed(x, causal, 0.25)
+    assert_fwd_close((o, lse), oracle_fwd(x, causal, 0.25, packed=True), "f32")
+    assert_grads_close((dq, dk, dv), oracle_bwd_packed(x, causal, 0.25), "f32")
