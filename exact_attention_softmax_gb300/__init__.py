@@ -19,7 +19,8 @@ import math
 from . import _abi
 from ._abi import SdpaError  # noqa: F401
 
-__all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_device_status",
+__all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_bwd_workspace_size",
+           "sdpa_device_status",
            "sdpa_debug_set", "sdpa_last_error", "sdpa_version", "SdpaError"]
 
 
@@ -125,6 +126,76 @@ def sdpa_bwd(q, k, v, o, lse, dO, dq=None, dk=None, dv=None, *, scale=None, is_c
     _abi.check(lib.sdpa_bwd(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
                             B, H, Lq, Lk, d, float(scale), int(bool(is_causal)), _vp(cu_seqlens), code,
                             _vp(workspace), workspace.numel(), _stream(q.device, stream)))
+    return dq, dk, dv
+
+
+def _varlen_geometry(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
+    """(nseq, H, total_q, total_k, max_q, max_k, d) for the cross-attention calls."""
+    import torch
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("varlen q and k must be [total, H, d]")
+    if k.shape[1:] != q.shape[1:]:
+        raise ValueError("q and k must agree in H and d")
+    for name, cu in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if cu.dtype != torch.int32 or cu.device != q.device or cu.dim() != 1 or not cu.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int32 vector on the device of q")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold nseq + 1 offsets")
+    total_q, H, d = q.shape
+    return cu_seqlens_q.numel() - 1, H, total_q, k.shape[0], int(max_seqlen_q), int(max_seqlen_k), d
+
+
+def sdpa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o=None, lse=None, *,
+                    scale=None, is_causal=False, stream=None):
+    """Forward over packed sequences with separate query and key offsets.
+
+    q/o [total_q,H,d], k/v [total_k,H,d]; sequence s owns query rows
+    ``cu_seqlens_q[s]:cu_seqlens_q[s+1]`` and key rows
+    ``cu_seqlens_k[s]:cu_seqlens_k[s+1]``; the max_seqlen bounds cover every
+    length. Returns ``(O, LSE)`` with LSE [H,total_q] fp32. A [B,L,H,d] batch
+    is the case of uniform offsets ``s*L``.
+    """
+    import torch
+    lib = _abi.load()
+    nseq, H, tq, tk, mq, mk, d = _varlen_geometry(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((H, tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensors({"k": k, "v": v, "o": o}, q.device, q.dtype)
+    if v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("v must match k and o must match q")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (H, tq):
+        raise TypeError("lse must be contiguous float32 [H, total_q]")
+    _abi.check(lib.sdpa_fwd_varlen(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), nseq, H, tq, tk, mq, mk, d,
+                                   float(scale), int(bool(is_causal)), _vp(cu_seqlens_q), _vp(cu_seqlens_k),
+                                   _dtype_code(q), _stream(q.device, stream)))
+    return o, lse
+
+
+def sdpa_bwd_varlen(q, k, v, o, lse, dO, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    dq=None, dk=None, dv=None, *, scale=None, is_causal=False, workspace=None, stream=None):
+    """Backward of :func:`sdpa_fwd_varlen`. Returns ``(dQ, dK, dV)``."""
+    import torch
+    lib = _abi.load()
+    nseq, H, tq, tk, mq, mk, d = _varlen_geometry(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_tensors({"k": k, "v": v, "o": o, "dO": dO, "dq": dq, "dk": dk, "dv": dv}, q.device, q.dtype)
+    if v.shape != k.shape or o.shape != q.shape or dO.shape != q.shape or dq.shape != q.shape \
+            or dk.shape != k.shape or dv.shape != k.shape:
+        raise ValueError("gradient and output shapes must match their inputs")
+    code = _dtype_code(q)
+    need = lib.sdpa_bwd_workspace_size(1, H, tq, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _abi.check(lib.sdpa_bwd_varlen(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
+                                   nseq, H, tq, tk, mq, mk, d, float(scale), int(bool(is_causal)),
+                                   _vp(cu_seqlens_q), _vp(cu_seqlens_k), code, _vp(workspace), workspace.numel(),
+                                   _stream(q.device, stream)))
     return dq, dk, dv
 
 

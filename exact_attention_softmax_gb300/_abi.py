@@ -25,9 +25,12 @@ SDPA_STATUS_SEQLEN = 2
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "sdpa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "sdpa_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _i, _vp]),
     "sdpa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "sdpa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                       _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
+    "sdpa_bwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                             _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _i, _vp, _sz, _vp]),
     "sdpa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "sdpa_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),

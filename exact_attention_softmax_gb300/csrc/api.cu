@@ -96,34 +96,6 @@ int make_operand_map(CUtensorMap* m, const void* base, int dtype, bool packed, i
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int Lq,
-                 int Lk, int d, float scale, int is_causal, const int* cu, int dtype, bool* noop) {
-  *noop = false;
-  if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return fail(SDPA_ERR_ARG, "unknown dtype %d", dtype);
-  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d <= 0)
-    return fail(SDPA_ERR_ARG, "sizes must be non-negative and d positive (B=%d H=%d Lq=%d Lk=%d d=%d)", B, H, Lq, Lk, d);
-  if (!std::isfinite(scale)) return fail(SDPA_ERR_ARG, "scale must be finite");
-  if (is_causal != 0 && is_causal != 1) return fail(SDPA_ERR_ARG, "is_causal must be 0 or 1");
-  if (dtype == SDPA_F32) {
-    if (d > 128) return fail(SDPA_ERR_UNSUPPORTED, "float32 path supports d <= 128 (got %d)", d);
-  } else if (d != 32 && d != 64 && d != 128) {
-    return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 path supports d in {32, 64, 128} (got %d)", d);
-  }
-  if (B == 0 || H == 0 || Lq == 0) {
-    *noop = true;
-    return SDPA_OK;
-  }
-  if (cu == nullptr && Lk == 0) return fail(SDPA_ERR_ARG, "Lk = 0 with Lq > 0: softmax over no keys");
-  if (!q || !k || !v || !o || !lse) return fail(SDPA_ERR_ARG, "null tensor pointer");
-  if (dtype != SDPA_F32 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o)))
-    return fail(SDPA_ERR_ARG, "fp16/bf16 tensors must be 16-byte aligned");
-  if (cu != nullptr && Lk == 0) {
-    // every sequence must then be empty; nothing to compute
-    *noop = true;
-  }
-  return SDPA_OK;
-}
-
 }  // namespace
 
 int set_last_error(int code, const char* fmt, ...) {
@@ -140,17 +112,71 @@ int set_last_error(int code, const char* fmt, ...) {
 
 using namespace sdpa;
 
-extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq, int Lk,
-                        int d, float scale, int is_causal, const int* cu_seqlens, int dtype, void* stream) {
+namespace {
+
+// Sizes of one call. Dense: cu_q = cu_k = NULL, [B,H,Lq,d] / [B,H,Lk,d].
+// Packed: B sequences; queries on `total_q` rows through cu_q, keys on
+// `total_k` rows through cu_k; max_q / max_k bound the lengths.
+struct Shape {
+  int B, H, total_q, total_k, max_q, max_k, d;
+  const int* cu_q;
+  const int* cu_k;
+  bool packed() const { return cu_q != nullptr; }
+};
+
+int check_shape(const Shape& sh, float scale, int is_causal, int dtype, bool* noop) {
+  *noop = false;
+  if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return fail(SDPA_ERR_ARG, "unknown dtype %d", dtype);
+  if (sh.B < 0 || sh.H < 0 || sh.total_q < 0 || sh.total_k < 0 || sh.max_q < 0 || sh.max_k < 0 || sh.d <= 0)
+    return fail(SDPA_ERR_ARG, "sizes must be non-negative and d positive (B=%d H=%d Lq=%d Lk=%d d=%d)", sh.B, sh.H,
+                sh.total_q, sh.total_k, sh.d);
+  if (!std::isfinite(scale)) return fail(SDPA_ERR_ARG, "scale must be finite");
+  if (is_causal != 0 && is_causal != 1) return fail(SDPA_ERR_ARG, "is_causal must be 0 or 1");
+  if (dtype == SDPA_F32) {
+    if (sh.d > 128) return fail(SDPA_ERR_UNSUPPORTED, "float32 path supports d <= 128 (got %d)", sh.d);
+  } else if (sh.d != 32 && sh.d != 64 && sh.d != 128) {
+    return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 path supports d in {32, 64, 128} (got %d)", sh.d);
+  }
+  if (sh.packed() && sh.cu_k == nullptr) return fail(SDPA_ERR_ARG, "key offsets missing");
+  if (sh.B == 0 || sh.H == 0 || sh.total_q == 0 || (sh.packed() && sh.max_q == 0)) {
+    *noop = true;  // no query rows
+    return SDPA_OK;
+  }
+  if (sh.max_k == 0 || sh.total_k == 0) return fail(SDPA_ERR_ARG, "no keys for %d query rows: softmax over no keys", sh.total_q);
+  return SDPA_OK;
+}
+
+int check_tensors(const void* q, const void* k, const void* v, const void* o, const float* lse, int dtype) {
+  if (!q || !k || !v || !o || !lse) return fail(SDPA_ERR_ARG, "null tensor pointer");
+  if (dtype != SDPA_F32 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o)))
+    return fail(SDPA_ERR_ARG, "fp16/bf16 tensors must be 16-byte aligned");
+  return SDPA_OK;
+}
+
+void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, const void* v, const void* o,
+                  const float* lse, float scale, int is_causal) {
+  p.q = q; p.k = k; p.v = v; p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
+  p.B = sh.B; p.H = sh.H; p.d = sh.d;
+  p.scale = scale; p.causal = is_causal;
+  p.cu_seqlens = sh.cu_q;
+  p.cu_k = sh.cu_k;
+  p.Lq = sh.total_q;
+  // dense: Lk is the key length of every unit; packed: the bound on it
+  p.Lk = sh.packed() ? sh.max_k : sh.total_k;
+  p.total_k = sh.total_k;
+  p.max_q = sh.packed() ? sh.max_q : sh.total_q;
+  p.debug = g_debug_flags;
+}
+
+int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o, float* lse, float scale,
+            int is_causal, int dtype, void* stream) {
   g_last_error.clear();
   bool noop = false;
-  int rc = check_common(q, k, v, o, lse, B, H, Lq, Lk, d, scale, is_causal, cu_seqlens, dtype, &noop);
+  int rc = check_shape(sh, scale, is_causal, dtype, &noop);
   if (rc != SDPA_OK || noop) return rc;
+  if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
   Problem p{};
-  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
-  p.B = B; p.H = H; p.Lq = Lq; p.Lk = Lk; p.d = d;
-  p.scale = scale; p.causal = is_causal; p.cu_seqlens = cu_seqlens;
-  p.debug = g_debug_flags;
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -162,54 +188,43 @@ extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* o, fl
   }
   rc = get_encoder();
   if (rc != SDPA_OK) return rc;
-  const bool packed = cu_seqlens != nullptr;
+  const bool packed = sh.packed();
   FwdMaps maps;
-  const int rq = Lq, rk = packed ? Lq : Lk;
-  if ((rc = make_operand_map(&maps.q, q, dtype, packed, B, H, rq, d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.k, k, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.v, v, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.q, q, dtype, packed, sh.B, sh.H, sh.total_q, sh.d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.k, k, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
   e = launch_fwd_tc(p, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "forward (tensor-core) launch");
   return SDPA_OK;
 }
 
-extern "C" size_t sdpa_bwd_workspace_size(int B, int H, int Lq, int d, int dtype) {
-  if (B <= 0 || H <= 0 || Lq <= 0 || d <= 0) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * Lq;
-  const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
-  if (dtype == SDPA_F32) return delta;
-  return delta + rows * d * sizeof(float);
-}
-
-extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                        void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
-                        const int* cu_seqlens, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const void* o, const float* lse,
+            const void* dO, void* dq, void* dk, void* dv, float scale, int is_causal, int dtype, void* workspace,
+            size_t workspace_bytes, void* stream) {
   g_last_error.clear();
   bool noop = false;
-  int rc = check_common(q, k, v, o, lse, B, H, Lq, Lk, d, scale, is_causal, cu_seqlens, dtype, &noop);
-  if (rc != SDPA_OK) return rc;
-  if (noop) return SDPA_OK;
+  int rc = check_shape(sh, scale, is_causal, dtype, &noop);
+  if (rc != SDPA_OK || noop) return rc;
+  if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
   if (!dO || !dq || !dk || !dv) return fail(SDPA_ERR_ARG, "null gradient pointer");
   if (dtype != SDPA_F32 && !(aligned16(dO) && aligned16(dq) && aligned16(dk) && aligned16(dv)))
     return fail(SDPA_ERR_ARG, "fp16/bf16 gradients must be 16-byte aligned");
-  if (dtype != SDPA_F32 && d == 32) return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 backward supports d in {64, 128}");
-  const bool packed = cu_seqlens != nullptr;
-  // packed: the row statistics and dQ accumulator cover the `Lq` = total tokens
-  const size_t need = sdpa_bwd_workspace_size(packed ? 1 : B, H, Lq, d, dtype);
+  if (dtype != SDPA_F32 && sh.d == 32) return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 backward supports d in {64, 128}");
+  const bool packed = sh.packed();
+  // packed: the row statistics and dQ accumulator cover the total query rows
+  const int nb = packed ? 1 : sh.B;
+  const size_t need = sdpa_bwd_workspace_size(nb, sh.H, sh.total_q, sh.d, dtype);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace == nullptr ? 0 : workspace_bytes);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(SDPA_ERR_ARG, "workspace must be 256-byte aligned");
 
   BwdProblem bp{};
   Problem& p = bp.f;
-  p.q = q; p.k = k; p.v = v; p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
-  p.B = B; p.H = H; p.Lq = Lq; p.Lk = Lk; p.d = d;
-  p.scale = scale; p.causal = is_causal; p.cu_seqlens = cu_seqlens;
-  p.debug = g_debug_flags;
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
-  const size_t rows = static_cast<size_t>(packed ? 1 : B) * H * Lq;
+  const size_t rows = static_cast<size_t>(nb) * sh.H * sh.total_q;
   bp.delta = static_cast<float*>(workspace);
   bp.dq_acc = dtype == SDPA_F32 ? nullptr
                                 : reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * 4 + 255) / 256 * 256);
@@ -224,17 +239,70 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
   rc = get_encoder();
   if (rc != SDPA_OK) return rc;
   BwdMaps maps;
-  const uint32_t bq = d == 128 ? 64 : 128;  // query rows per backward step
-  const int rk = packed ? Lq : Lk;   // packed: keys share the token axis of the queries
-  if ((rc = make_operand_map(&maps.q, q, dtype, packed, B, H, Lq, d, bq)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.k, k, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.v, v, dtype, packed, B, H, rk, d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.dO, dO, dtype, packed, B, H, Lq, d, bq)) != SDPA_OK) return rc;
+  const uint32_t bq = sh.d == 128 ? 64 : 128;  // query rows per backward step
+  if ((rc = make_operand_map(&maps.q, q, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, bq)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.k, k, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.dO, dO, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, bq)) != SDPA_OK) return rc;
   e = launch_bwd_tc(bp, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward (tensor-core) launch");
   e = launch_dq_convert(bp, dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "dQ convert launch");
   return SDPA_OK;
+}
+
+// Dense, or packed self-attention (one offset array for queries and keys;
+// Lq = total tokens, Lk = max_seqlen).
+Shape self_shape(int B, int H, int Lq, int Lk, int d, const int* cu) {
+  if (cu == nullptr) return Shape{B, H, Lq, Lk, Lq, Lk, d, nullptr, nullptr};
+  return Shape{B, H, Lq, Lq, Lk, Lk, d, cu, cu};
+}
+
+}  // namespace
+
+extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq, int Lk,
+                        int d, float scale, int is_causal, const int* cu_seqlens, int dtype, void* stream) {
+  return run_fwd(self_shape(B, H, Lq, Lk, d, cu_seqlens), q, k, v, o, lse, scale, is_causal, dtype, stream);
+}
+
+extern "C" int sdpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int nseq, int H,
+                               int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, float scale,
+                               int is_causal, const int* cu_seqlens_q, const int* cu_seqlens_k, int dtype,
+                               void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) {
+    g_last_error.clear();
+    return fail(SDPA_ERR_ARG, "sdpa_fwd_varlen needs both offset arrays");
+  }
+  const Shape sh{nseq, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, cu_seqlens_q, cu_seqlens_k};
+  return run_fwd(sh, q, k, v, o, lse, scale, is_causal, dtype, stream);
+}
+
+extern "C" size_t sdpa_bwd_workspace_size(int B, int H, int Lq, int d, int dtype) {
+  if (B <= 0 || H <= 0 || Lq <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Lq;
+  const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
+  if (dtype == SDPA_F32) return delta;
+  return delta + rows * d * sizeof(float);
+}
+
+extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                        const int* cu_seqlens, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_bwd(self_shape(B, H, Lq, Lk, d, cu_seqlens), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
+                 workspace, workspace_bytes, stream);
+}
+
+extern "C" int sdpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dO, void* dq, void* dk, void* dv, int nseq, int H, int total_q, int total_k,
+                               int max_seqlen_q, int max_seqlen_k, int d, float scale, int is_causal,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, int dtype, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) {
+    g_last_error.clear();
+    return fail(SDPA_ERR_ARG, "sdpa_bwd_varlen needs both offset arrays");
+  }
+  const Shape sh{nseq, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, cu_seqlens_q, cu_seqlens_k};
+  return run_bwd(sh, q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype, workspace, workspace_bytes, stream);
 }
 
 extern "C" int sdpa_device_status(void* stream, unsigned* bits) {
@@ -255,7 +323,7 @@ extern "C" int sdpa_device_status(void* stream, unsigned* bits) {
   }
   if (bits) *bits = word;
   if (word & SDPA_STATUS_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", word);
-  if (word & SDPA_STATUS_SEQLEN) return fail(SDPA_ERR_ARG, "a packed sequence is longer than max_seqlen (status 0x%x)", word);
+  if (word & SDPA_STATUS_SEQLEN) return fail(SDPA_ERR_ARG, "a packed sequence is longer than its bound or has queries but no keys (status 0x%x)", word);
   return SDPA_OK;
 }
 

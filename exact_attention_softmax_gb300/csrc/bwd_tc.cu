@@ -131,24 +131,31 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   // Unit-major order: the key blocks of one (batch, head) run side by side and
   // share its Q / dO through L2; under causal masking key block 0 (the most
   // query tiles) goes first.
-  // Packed batches: a unit is (sequence, head), rows cu_seqlens[s] .. +len of
-  // the token axis, and p.Lk bounds every length.
+  // Packed batches: a unit is (sequence, head); its queries are rows
+  // cu_seqlens[s] .. cu_seqlens[s+1]-1 of the query token axis, its keys rows
+  // cu_k[s] .. cu_k[s+1]-1 of the key token axis, and p.Lk bounds every key length.
   const int nkb = (p.Lk + BK - 1) / BK;
   const int unit = blockIdx.x / nkb;
   const int kblk = blockIdx.x % nkb;
   const int key0 = kblk * BK;
-  int Lq = p.Lq, Lk = p.Lk, tok0 = 0, head = 0;
+  int Lq = p.Lq, Lk = p.Lk, tok0 = 0, tok0k = 0, head = 0;
   if (PACKED) {
     const int sq = unit / p.H;
     head = unit % p.H;
     tok0 = p.cu_seqlens[sq];
-    Lq = Lk = p.cu_seqlens[sq + 1] - tok0;
-    if (Lq > p.Lk && kblk == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+    Lq = p.cu_seqlens[sq + 1] - tok0;
+    tok0k = p.cu_k[sq];
+    Lk = p.cu_k[sq + 1] - tok0k;
+    const bool bad = Lq > p.max_q || Lk > p.Lk || (Lq > 0 && Lk <= 0);
+    if (bad && kblk == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+    if (bad) return;  // lengths outside their bounds: reported, nothing written
   }
   if (key0 >= Lk) return;
-  // element offset of row 0 of this unit, stride between rows, and offset of
-  // its row statistics (dense: [B,H,L,d] and [B,H,L]; packed: [total,H,d] and [H,total])
+  // element offset of row 0 of this unit (query side, key side), stride between
+  // rows, and offset of its row statistics (dense: [B,H,L,d] and [B,H,L];
+  // packed: [total,H,d] and [H,total])
   const long long row0 = PACKED ? (static_cast<long long>(tok0) * p.H + head) * D : 0;
+  const long long row0k = PACKED ? (static_cast<long long>(tok0k) * p.H + head) * D : 0;
   const long long rstride = PACKED ? static_cast<long long>(p.H) * D : D;
   const long long stat0 = PACKED ? static_cast<long long>(head) * p.Lq + tok0 : static_cast<long long>(unit) * Lq;
   const int nq = (Lq + BQ - 1) / BQ;
@@ -202,7 +209,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
       mbar_expect_tx(&bars->kv, 2 * C::kKTile);
-      const int c1 = PACKED ? head : key0, c2 = PACKED ? tok0 + key0 : unit;
+      const int c1 = PACKED ? head : key0, c2 = PACKED ? tok0k + key0 : unit;
       for (int cb = 0; cb < C::kNBlk; ++cb) {
         tma_load_3d(smem + C::kOffK + cb * C::kKColBlk, &tmK, &bars->kv, cb * C::kBlk, c1, c2);
         tma_load_3d(smem + C::kOffV + cb * C::kKColBlk, &tmV, &bars->kv, cb * C::kBlk, c1, c2);
@@ -482,7 +489,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       const uint32_t col0 = half == 0 ? C::kTdV : C::kTdK;
       const float sc = half == 0 ? 1.f : p.scale;
       T* out = static_cast<T*>(half == 0 ? bp.dv : bp.dk) +
-               (PACKED ? row0 + static_cast<long long>(key) * rstride : (static_cast<long long>(unit) * Lk + key) * D);
+               (PACKED ? row0k + static_cast<long long>(key) * rstride : (static_cast<long long>(unit) * Lk + key) * D);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];

@@ -18,8 +18,11 @@ constexpr int kDebugDropQArrive = 1;  // forward producer never loads Q: every w
 enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
 // One attention problem as the kernels see it. Dense: q/o [B,H,Lq,d],
-// k/v [B,H,Lk,d], lse [B,H,Lq]. Packed (cu_seqlens != nullptr): q/k/v/o
-// [total,H,d] with total = Lq, lse [H,total], Lk = max sequence length.
+// k/v [B,H,Lk,d], lse [B,H,Lq]. Packed (cu_seqlens != nullptr): B sequences;
+// q/o [Lq = total query tokens, H, d] with sequence s at rows
+// cu_seqlens[s]..cu_seqlens[s+1]; k/v [total_k, H, d] with rows from cu_k
+// (cu_k == cu_seqlens for self-attention); lse [H, Lq]; max_q and Lk bound the
+// query and key lengths of every sequence.
 struct Problem {
   const void* q;
   const void* k;
@@ -30,6 +33,9 @@ struct Problem {
   float scale;
   int causal;
   const int* cu_seqlens;
+  const int* cu_k;
+  int total_k;
+  int max_q;
   unsigned* status;  // device status word (bit flags above)
   int debug;
 };

@@ -142,7 +142,7 @@ __device__ __forceinline__ int tile_blocks(int r, int len_q, int len_k) {
 
 // One work item: 256 query rows (two 128-row tiles) of one (batch|sequence, head).
 struct Item {
-  int unit, h, tok0, len_q, len_k, r0, n0, n1, nmax;
+  int unit, h, tok0, tok0k, len_q, len_k, r0, n0, n1, nmax;
 };
 
 // Items are numbered unit-major, so the items of one (batch|sequence, head) run
@@ -155,13 +155,19 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
   const int ord = idx % npairs;
   const int pair = CAUSAL ? (npairs - 1 - ord) : ord;
   it.h = 0;
-  it.tok0 = 0;
+  it.tok0 = it.tok0k = 0;
   if (PACKED) {
     const int s = it.unit / p.H;
     it.h = it.unit % p.H;
     it.tok0 = p.cu_seqlens[s];
-    it.len_q = it.len_k = p.cu_seqlens[s + 1] - it.tok0;
-    if (it.len_q > p.Lk && ord == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+    it.len_q = p.cu_seqlens[s + 1] - it.tok0;
+    it.tok0k = p.cu_k[s];
+    it.len_k = p.cu_k[s + 1] - it.tok0k;
+    // lengths beyond their bounds, or queries with no keys, are reported
+    // (the item is then skipped: its rows stay unwritten)
+    const bool bad = it.len_q > p.max_q || it.len_k > p.Lk || (it.len_q > 0 && it.len_k <= 0);
+    if (bad && ord == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+    if (bad) it.len_q = 0;
   } else {
     it.len_q = p.Lq;
     it.len_k = p.Lk;
@@ -185,7 +191,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Persistent: CTA b starts with work item b, then claims items dynamically.
-  const int npairs = ((PACKED ? p.Lk : p.Lq) + 2 * BM - 1) / (2 * BM);
+  const int npairs = ((PACKED ? p.max_q : p.Lq) + 2 * BM - 1) / (2 * BM);
   const int nitems = npairs * p.B * p.H;
 
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
@@ -256,7 +262,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         idx = static_cast<int>(atomicAdd(sched, 1u)) + static_cast<int>(gridDim.x);
         if (it.nmax == 0) continue;
         auto c1 = [&](int row) { return PACKED ? it.h : row; };
-        auto c2 = [&](int row) { return PACKED ? it.tok0 + row : it.unit; };
+        auto c2 = [&](int row) { return PACKED ? it.tok0 + row : it.unit; };      // query rows
+        auto c2k = [&](int row) { return PACKED ? it.tok0k + row : it.unit; };    // key rows
         for (int t = 0; t < 2 && ok; ++t) {
           if ((t == 0 ? it.n0 : it.n1) == 0) continue;
           if (qloads[t] > 0 && !(ok = mbar_wait(&bars->q_empty[t], (qloads[t] - 1) & 1, abort_flag, p.status))) break;
@@ -278,7 +285,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             const int row = j * BN;
             for (int cb = 0; cb < C::kNBlk; ++cb)
               tma_load_3d(smem + C::kOffSlots + slot * C::kTileBytes + cb * C::kColBlkBytes, m, &bars->full[slot],
-                          cb * C::kBlk, c1(row), c2(row));
+                          cb * C::kBlk, c1(row), c2k(row));
           }
         }
       }
@@ -590,7 +597,7 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   const int sms = dev < 64 ? sm_count[dev] : 1;
-  const int rows = PACKED ? p.Lk : p.Lq;
+  const int rows = PACKED ? p.max_q : p.Lq;
   const long long npairs = (rows + 2 * BM - 1) / (2 * BM);
   const long long items = npairs * p.B * p.H;
   if (items == 0) return cudaSuccess;

@@ -21,40 +21,43 @@ constexpr int kTile = 32;    // rows of the other operand staged per step
 
 struct Unit {
   int len_q, len_k;   // rows of this (batch|sequence, head)
-  long long base;     // element offset of row 0
+  long long base;     // element offset of query row 0 (q, o, dO, dq)
+  long long kbase;    // element offset of key row 0 (k, v, dk, dv)
   long long stride;   // elements between consecutive rows
   long long stat;     // offset of row 0 in lse / delta
+  bool bad;           // packed lengths outside their bounds
 };
 
 __device__ __forceinline__ Unit unit_of(const Problem& p, int b, int h) {
   Unit u;
+  u.bad = false;
   if (p.cu_seqlens == nullptr) {
     u.len_q = p.Lq;
     u.len_k = p.Lk;
     u.stride = p.d;
     u.base = (static_cast<long long>(b) * p.H + h) * p.Lq * p.d;
+    u.kbase = (static_cast<long long>(b) * p.H + h) * p.Lk * p.d;
     u.stat = (static_cast<long long>(b) * p.H + h) * p.Lq;
   } else {
-    const int s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
-    u.len_q = u.len_k = s1 - s0;
+    const int s0 = p.cu_seqlens[b], t0 = p.cu_k[b];
+    u.len_q = p.cu_seqlens[b + 1] - s0;
+    u.len_k = p.cu_k[b + 1] - t0;
     u.stride = static_cast<long long>(p.H) * p.d;
     u.base = static_cast<long long>(s0) * p.H * p.d + static_cast<long long>(h) * p.d;
+    u.kbase = static_cast<long long>(t0) * p.H * p.d + static_cast<long long>(h) * p.d;
     u.stat = static_cast<long long>(h) * p.Lq + s0;
+    u.bad = u.len_q > p.max_q || u.len_k > p.Lk || (u.len_q > 0 && u.len_k <= 0);
   }
   return u;
-}
-// Dense K/V rows live in their own [B,H,Lk,d] tensor.
-__device__ __forceinline__ long long kv_base(const Problem& p, int b, int h, const Unit& u) {
-  if (p.cu_seqlens == nullptr) return (static_cast<long long>(b) * p.H + h) * p.Lk * p.d;
-  return u.base;
 }
 
 template <int DMAX>
 __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
   const int b = blockIdx.z, h = blockIdx.y;
   const Unit u = unit_of(p, b, h);
-  if (p.cu_seqlens != nullptr && u.len_q > p.Lk) {
+  if (u.bad) {
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+    return;
   }
   const int row0 = blockIdx.x * kRows;
   if (row0 >= u.len_q) return;
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
   const bool live = row < u.len_q;
   const int d = p.d;
   const float* Q = static_cast<const float*>(p.q) + u.base;
-  const long long kvb = kv_base(p, b, h, u);
+  const long long kvb = u.kbase;
   const float* K = static_cast<const float*>(p.k) + kvb;
   const float* V = static_cast<const float*>(p.v) + kvb;
 
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
   const int row = row0 + threadIdx.x;
   const bool live = row < u.len_q;
   const int d = p.d;
-  const long long kvb = kv_base(p, b, h, u);
+  const long long kvb = u.kbase;
   const float* Q = static_cast<const float*>(p.q) + u.base;
   const float* dO = static_cast<const float*>(bp.dO) + u.base;
   const float* K = static_cast<const float*>(p.k) + kvb;
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
   const int key = key0 + threadIdx.x;
   const bool live = key < u.len_k;
   const int d = p.d;
-  const long long kvb = kv_base(p, b, h, u);
+  const long long kvb = u.kbase;
   const float* Q = static_cast<const float*>(p.q) + u.base;
   const float* dO = static_cast<const float*>(bp.dO) + u.base;
   const float* K = static_cast<const float*>(p.k) + kvb;
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
 
 cudaError_t launch_fwd_simt(const Problem& p, cudaStream_t s) {
   const bool packed = p.cu_seqlens != nullptr;
-  const int rows = packed ? p.Lk : p.Lq;  // packed: Lk bounds every sequence length
+  const int rows = packed ? p.max_q : p.Lq;  // packed: max_q bounds every query length
   dim3 grid((rows + kRows - 1) / kRows, p.H, p.B);
   if (grid.x == 0) return cudaSuccess;
   if (p.d <= 32) fwd_f32_kernel<32><<<grid, kRows, 0, s>>>(p);
@@ -270,7 +273,7 @@ cudaError_t launch_fwd_simt(const Problem& p, cudaStream_t s) {
 cudaError_t launch_bwd_simt(const BwdProblem& bp, cudaStream_t s) {
   const Problem& p = bp.f;
   const bool packed = p.cu_seqlens != nullptr;
-  const int rq = packed ? p.Lk : p.Lq;
+  const int rq = packed ? p.max_q : p.Lq;  // packed: bounds on the query and key lengths
   const int rk = p.Lk;
   dim3 gq((rq + kRows - 1) / kRows, p.H, p.B), gk((rk + kRows - 1) / kRows, p.H, p.B);
   if (p.d <= 32) {

@@ -145,6 +145,29 @@ def varlen_inputs(lengths, H, d, dtype="f16", dist="normal", seed=0, with_do=Tru
     return out
 
 
+def varlen_cross_inputs(lengths_q, lengths_k, H, d, dtype="f16", dist="normal", seed=0, with_do=True):
+    """Packed cross-attention inputs: q/dO [total_q, H, d], k/v [total_k, H, d]
+    with their own offsets ``cu_seqlens_q`` / ``cu_seqlens_k`` (int32) and
+    length bounds ``max_seqlen_q`` / ``max_seqlen_k``."""
+    if len(lengths_q) != len(lengths_k):
+        raise ValueError("one key length per query length")
+    g = torch.Generator("cpu").manual_seed(seed)
+    td = _DTYPES[dtype]
+    tq, tk = int(sum(lengths_q)), int(sum(lengths_k))
+    out = {
+        "q": _draw(g, (tq, H, d), dist).to(td),
+        "k": _draw(g, (tk, H, d), dist).to(td),
+        "v": _draw(g, (tk, H, d), dist).to(td),
+        "cu_seqlens_q": cu_seqlens_from(lengths_q),
+        "cu_seqlens_k": cu_seqlens_from(lengths_k),
+        "max_seqlen_q": int(max(lengths_q)) if lengths_q else 0,
+        "max_seqlen_k": int(max(lengths_k)) if lengths_k else 0,
+    }
+    if with_do:
+        out["do"] = _draw(g, (tq, H, d), "normal").to(td)
+    return out
+
+
 def workload_inputs(w: Workload, seed: int = 0, with_do=None):
     """Inputs of a named workload (dO drawn when the workload has a backward)."""
     if with_do is None:

@@ -36,8 +36,16 @@
  *  - Return value: SDPA_OK or a negative sdpa_status. Argument errors are
  *    detected on the host before anything is launched. A nonzero return
  *    leaves a message for sdpa_last_error(). Errors found by a kernel while
- *    it runs (a bounded wait that gave up, a packed sequence longer than Lk)
- *    are recorded in a device status word that sdpa_device_status() reads.
+ *    it runs (a bounded wait that gave up, a packed sequence longer than its
+ *    bound) are recorded in a device status word that sdpa_device_status()
+ *    reads.
+ *  - Packed cross-attention (sdpa_fwd_varlen / sdpa_bwd_varlen): queries and
+ *    keys of sequence s sit on two different token axes, q/o/dO/dq
+ *    [total_q, H, d] at rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 and
+ *    k/v/dk/dv [total_k, H, d] at rows cu_seqlens_k[s] .. cu_seqlens_k[s+1]-1;
+ *    lse is [H, total_q]. Query i of a sequence attends to the keys of the
+ *    same sequence (causal: to its keys j <= i). The same calls cover a
+ *    padded-free [B, L, H, d] batch: pass the uniform offsets s*L.
  */
 #ifndef SDPA_GB300_H
 #define SDPA_GB300_H
@@ -61,7 +69,8 @@ typedef enum {
 
 /* Bits of the device status word (see sdpa_device_status). */
 #define SDPA_STATUS_TIMEOUT 1u   /* an mbarrier wait exceeded its time limit; outputs invalid */
-#define SDPA_STATUS_SEQLEN 2u    /* a packed sequence is longer than Lk (max_seqlen); outputs invalid */
+#define SDPA_STATUS_SEQLEN 2u    /* a packed sequence is longer than its bound (max_seqlen), or has
+                                    queries but no keys; its outputs are left unwritten */
 
 /*
  * Forward: O and LSE.
@@ -79,6 +88,28 @@ typedef enum {
 int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
              const int* cu_seqlens, int dtype, void* stream);
+
+/*
+ * Forward over packed sequences whose queries and keys have their own
+ * offsets (cross-attention over a NestedTensor-style batch; layout rules
+ * above). The tutorial's NestedTensor section runs the op on batches of
+ * unequal lengths; this is that op with the key side indexed separately.
+ *   nseq          : number of sequences; cu_seqlens_q / cu_seqlens_k are
+ *                   device int32 arrays of nseq+1 non-decreasing offsets
+ *                   from 0 to total_q / total_k.
+ *   max_seqlen_q, max_seqlen_k : upper bounds on every sequence's query and
+ *                   key length (sizes the launch; a longer sequence sets
+ *                   SDPA_STATUS_SEQLEN and is left unwritten).
+ *   o, lse        : [total_q, H, d] and [H, total_q] outputs.
+ * A sequence with queries must have at least one key (else
+ * SDPA_STATUS_SEQLEN); total_q == 0 or max_seqlen_q == 0 is a no-op;
+ * max_seqlen_k == 0 or total_k == 0 with queries present is SDPA_ERR_ARG.
+ * dtype / d support as for sdpa_fwd.
+ */
+int sdpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int nseq, int H, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                    int d, float scale, int is_causal,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, int dtype, void* stream);
 
 /*
  * Bytes of device workspace sdpa_bwd needs for these sizes (a float32 row
@@ -107,6 +138,19 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const f
              int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
              const int* cu_seqlens, int dtype,
              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of sdpa_fwd_varlen: dq [total_q, H, d], dk and dv [total_k, H, d],
+ * fully overwritten. Arguments as for sdpa_fwd_varlen plus those of sdpa_bwd;
+ * the workspace is sdpa_bwd_workspace_size(1, H, total_q, d, dtype) bytes.
+ * Supported: F32 with d <= 128; F16/BF16 with d in {64, 128}.
+ */
+int sdpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv,
+                    int nseq, int H, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                    int d, float scale, int is_causal,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass for callers that cannot allocate device memory: it takes the

@@ -34,7 +34,11 @@ Layouts: dense tensors are ``[..., L, d]`` (any leading batch/head dims, the
 tutorial's ``[B, H, L, d]`` and its ``[2, 3, 8]`` example both fit); packed
 variable-length tensors (the tutorial's NestedTensor section) are
 ``[total, H, d]`` with ``cu_seqlens`` of length ``nseq + 1``; the same
-offsets serve queries and keys (self-attention).
+offsets serve queries and keys (self-attention) unless ``cu_seqlens_k`` gives
+the keys their own offsets on their own token axis (cross-attention: k/v
+``[total_k, H, d]``; query i of a sequence sees that sequence's keys, causal
+ones j <= i as in the dense case). A ``[B, L, H, d]`` batch is the packed
+case with offsets ``s * L``.
 """
 from __future__ import annotations
 
@@ -122,14 +126,25 @@ def _check_cu(cu_seqlens, total: int) -> np.ndarray:
     return cu
 
 
-def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None):
+def _packed_spans(cu_seqlens, cu_seqlens_k, total_q: int, total_k: int):
+    """Per sequence: (query rows a:b, key rows c:e)."""
+    cq = _check_cu(cu_seqlens, total_q)
+    ck = cq if cu_seqlens_k is None else _check_cu(cu_seqlens_k, total_k)
+    if ck.size != cq.size:
+        raise ValueError("cu_seqlens and cu_seqlens_k must describe the same number of sequences")
+    return [(int(cq[s]), int(cq[s + 1]), int(ck[s]), int(ck[s + 1])) for s in range(cq.size - 1)]
+
+
+def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None):
     """Forward over a whole batch.
 
     Dense: ``q`` [..., Lq, d], ``k``/``v`` [..., Lk, d] -> ``O`` [..., Lq, d],
     ``LSE`` [..., Lq]. Packed (``cu_seqlens`` given): ``q``/``k``/``v``
     [total, H, d] -> ``O`` [total, H, d], ``LSE`` [H, total]; sequence s owns
     rows ``cu_seqlens[s] : cu_seqlens[s+1]`` of queries and keys (the
-    tutorial's NestedTensor batches without padding).
+    tutorial's NestedTensor batches without padding). With ``cu_seqlens_k``
+    the keys/values are [total_k, H, d] and sequence s owns key rows
+    ``cu_seqlens_k[s] : cu_seqlens_k[s+1]``.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     if cu_seqlens is None:
@@ -141,19 +156,17 @@ def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None
             o[u], lse[u] = attn_fwd_unit(qu[u], ku[u], vu[u], scale, is_causal)
         return o.reshape(lead + o.shape[1:]), lse.reshape(lead + lse.shape[1:])
     total, nh, _ = q.shape
-    cu = _check_cu(cu_seqlens, total)
     o = np.zeros((total, nh, v.shape[-1]))
     lse = np.zeros((nh, total))
-    for s in range(cu.size - 1):
-        a, b = int(cu[s]), int(cu[s + 1])
+    for a, b, c, e in _packed_spans(cu_seqlens, cu_seqlens_k, total, k.shape[0]):
         if b == a:
             continue
         for h in range(nh):
-            o[a:b, h], lse[h, a:b] = attn_fwd_unit(q[a:b, h], k[a:b, h], v[a:b, h], scale, is_causal)
+            o[a:b, h], lse[h, a:b] = attn_fwd_unit(q[a:b, h], k[c:e, h], v[c:e, h], scale, is_causal)
     return o, lse
 
 
-def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=None):
+def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None):
     """Backward over a whole batch; same layouts as :func:`attn_fwd_ref`.
     Returns ``(dQ, dK, dV)`` in float64."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -164,15 +177,13 @@ def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=
             dq[u], dk[u], dv[u] = attn_bwd_unit(qu[u], ku[u], vu[u], du[u], scale, is_causal)
         return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
     total, nh, _ = q.shape
-    cu = _check_cu(cu_seqlens, total)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    for s in range(cu.size - 1):
-        a, b = int(cu[s]), int(cu[s + 1])
+    for a, b, c, e in _packed_spans(cu_seqlens, cu_seqlens_k, total, k.shape[0]):
         if b == a:
             continue
         for h in range(nh):
-            dq[a:b, h], dk[a:b, h], dv[a:b, h] = attn_bwd_unit(
-                q[a:b, h], k[a:b, h], v[a:b, h], do[a:b, h], scale, is_causal)
+            dq[a:b, h], dk[c:e, h], dv[c:e, h] = attn_bwd_unit(
+                q[a:b, h], k[c:e, h], v[c:e, h], do[a:b, h], scale, is_causal)
     return dq, dk, dv
 
 

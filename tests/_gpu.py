@@ -89,6 +89,40 @@ def run_fwd_bwd_packed(x, causal, scale):
     return f64(o), f64(lse), f64(dq), f64(dk), f64(dv)
 
 
+def run_varlen_cross(x, causal, scale, bwd=True):
+    """Cross-attention packed fwd (+ bwd) through sdpa_fwd_varlen / sdpa_bwd_varlen;
+    returns (O, LSE[, dQ, dK, dV]) as float64 after the canary and status checks."""
+    dev = cuda()
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    cq, ck = x["cu_seqlens_q"].to(dev), x["cu_seqlens_k"].to(dev)
+    mq, mk = max(x["max_seqlen_q"], 1), max(x["max_seqlen_k"], 1)
+    ob, o = guarded_empty(tuple(q.shape), q.dtype, dev)
+    lb, lse = guarded_empty((q.shape[1], q.shape[0]), torch.float32, dev)
+    ops.sdpa_fwd_varlen(q, k, v, cq, ck, mq, mk, o, lse, scale=scale, is_causal=causal)
+    out = [o, lse]
+    bufs = [ob, lb]
+    if bwd:
+        do = x["do"].to(dev)
+        gb = [guarded_empty(tuple(t.shape), t.dtype, dev) for t in (q, k, v)]
+        ops.sdpa_bwd_varlen(q, k, v, o, lse, do, cq, ck, mq, mk, gb[0][1], gb[1][1], gb[2][1],
+                            scale=scale, is_causal=causal)
+        out += [g for _, g in gb]
+        bufs += [b for b, _ in gb]
+    assert ops.sdpa_device_status() == 0
+    for b in bufs:
+        check_guard(b)
+    return tuple(f64(t) for t in out)
+
+
+def oracle_varlen_cross(x, causal, scale, bwd=True):
+    q, k, v = (f64(x[n]) for n in ("q", "k", "v"))
+    cq, ck = x["cu_seqlens_q"].numpy(), x["cu_seqlens_k"].numpy()
+    out = attn_fwd_ref(q, k, v, scale, causal, cq, ck)
+    if bwd:
+        out = out + attn_bwd_ref(q, k, v, f64(x["do"]), scale, causal, cq, ck)
+    return out
+
+
 def oracle_bwd_packed(x, causal, scale):
     q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
     return attn_bwd_ref(q, k, v, do, scale, causal, x["cu_seqlens"].numpy())

@@ -94,6 +94,33 @@ def test_workspace_size_and_errors(lib):
     assert lib.sdpa_bwd(*args_p, FAKE, need_p - 1, None) == _abi.SDPA_ERR_WORKSPACE
 
 
+def _fwd_varlen(lib, nseq=2, H=1, tq=8, tk=12, mq=5, mk=7, d=64, causal=0, cu_q=FAKE, cu_k=FAKE, dtype=1, ptr=FAKE):
+    return lib.sdpa_fwd_varlen(ptr, ptr, ptr, ptr, ptr, nseq, H, tq, tk, mq, mk, d, 0.125, causal, cu_q, cu_k,
+                               dtype, None)
+
+
+def test_varlen_cross_argument_errors(lib):
+    assert _fwd_varlen(lib, cu_k=None) == _abi.SDPA_ERR_ARG     # both offset arrays required
+    assert b"offset" in lib.sdpa_last_error()
+    assert _fwd_varlen(lib, cu_q=None) == _abi.SDPA_ERR_ARG
+    assert _fwd_varlen(lib, mk=0) == _abi.SDPA_ERR_ARG          # queries but no keys anywhere
+    assert _fwd_varlen(lib, tk=0) == _abi.SDPA_ERR_ARG
+    assert _fwd_varlen(lib, tk=-1) == _abi.SDPA_ERR_ARG
+    assert _fwd_varlen(lib, d=48) == _abi.SDPA_ERR_UNSUPPORTED
+    assert _fwd_varlen(lib, ptr=ctypes.c_void_p(0x100008)) == _abi.SDPA_ERR_ARG
+    # no query rows: a no-op that touches nothing
+    assert _fwd_varlen(lib, tq=0, ptr=ctypes.c_void_p(0)) == _abi.SDPA_OK
+    assert _fwd_varlen(lib, mq=0, ptr=ctypes.c_void_p(0)) == _abi.SDPA_OK
+    assert _fwd_varlen(lib, nseq=0, ptr=ctypes.c_void_p(0)) == _abi.SDPA_OK
+    # backward: the workspace covers the total query rows
+    H, tq, d = 4, 700, 64
+    need = lib.sdpa_bwd_workspace_size(1, H, tq, d, 1)
+    args = [FAKE] * 9 + [3, H, tq, 900, 300, 400, d, 0.125, 1, FAKE, FAKE, 1]
+    assert lib.sdpa_bwd_varlen(*args, FAKE, need - 1, None) == _abi.SDPA_ERR_WORKSPACE
+    assert lib.sdpa_bwd_varlen(*(args[:19] + [None] + args[20:]), FAKE, need, None) == _abi.SDPA_ERR_ARG
+    assert lib.sdpa_bwd_varlen(*(args[:15] + [32] + args[16:]), FAKE, need, None) == _abi.SDPA_ERR_UNSUPPORTED
+
+
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_abi, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):

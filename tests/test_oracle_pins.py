@@ -183,6 +183,78 @@ def test_packed_equals_dense_per_sequence():
                 np.testing.assert_array_equal(dv[a:b, h], g[2])
 
 
+def _cross_bruteforce(q, k, v, do, cq, ck, scale, causal):
+    """Per-sequence brute force for a packed cross-attention batch, written
+    with explicit row lists so that it shares no slicing with the oracle."""
+    H = q.shape[1]
+    o, lse = np.zeros(q.shape), np.zeros((H, q.shape[0]))
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for s in range(len(cq) - 1):
+        qrows = list(range(cq[s], cq[s + 1]))
+        krows = list(range(ck[s], ck[s + 1]))
+        if not qrows:
+            continue
+        for h in range(H):
+            qs = [q[r, h].tolist() for r in qrows]
+            ks = [k[r, h].tolist() for r in krows]
+            vs = [v[r, h].tolist() for r in krows]
+            ds = [do[r, h].tolist() for r in qrows]
+            ob, lb = fwd_bruteforce(qs, ks, vs, scale, causal)
+            gq, gk, gv = bwd_bruteforce(qs, ks, vs, ds, scale, causal)
+            for i, r in enumerate(qrows):
+                o[r, h], lse[h, r], dq[r, h] = ob[i], lb[i], gq[i]
+            for j, r in enumerate(krows):
+                dk[r, h], dv[r, h] = gk[j], gv[j]
+    return o, lse, dq, dk, dv
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_cross_matches_bruteforce(causal):
+    # queries and keys of unequal lengths on their own token axes, including
+    # a sequence with keys but no queries (its dK, dV must stay zero)
+    lq, lk = [2, 0, 4, 1, 3], [3, 2, 2, 5, 3]
+    x = wl.varlen_cross_inputs(lq, lk, 2, 3, "f32", "normal", seed=11)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    cq, ck = x["cu_seqlens_q"].numpy(), x["cu_seqlens_k"].numpy()
+    o, lse = attn_fwd_ref(q, k, v, 0.6, causal, cq, ck)
+    grads = attn_bwd_ref(q, k, v, do, 0.6, causal, cq, ck)
+    ref = _cross_bruteforce(q, k, v, do, cq.tolist(), ck.tolist(), 0.6, causal)
+    for got, want in zip((o, lse) + tuple(grads), ref):
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-13)
+    assert np.all(grads[1][ck[1]:ck[2]] == 0) and np.all(grads[2][ck[1]:ck[2]] == 0)
+
+
+def test_packed_cross_with_shared_offsets_is_self_attention():
+    lens = [3, 1, 5, 0, 2]
+    x = wl.varlen_inputs(lens, 2, 4, "f32", "normal", seed=3)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    cu = x["cu_seqlens"].numpy()
+    for causal in (False, True):
+        a = attn_fwd_ref(q, k, v, 0.5, causal, cu) + attn_bwd_ref(q, k, v, do, 0.5, causal, cu)
+        b = attn_fwd_ref(q, k, v, 0.5, causal, cu, cu.copy()) + attn_bwd_ref(q, k, v, do, 0.5, causal, cu, cu.copy())
+        for x1, x2 in zip(a, b):
+            np.testing.assert_array_equal(x1, x2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blhd_batch_is_packed_with_uniform_offsets(causal):
+    # a [B, L, H, d] batch read through uniform offsets s*L equals the dense
+    # [B, H, L, d] definition (queries and keys of different lengths)
+    B, Lq, Lk, H, d = 3, 4, 6, 2, 3
+    q, k, v, do = rnd(B, Lq, H, d, seed=1), rnd(B, Lk, H, d, seed=2), rnd(B, Lk, H, d, seed=3), rnd(B, Lq, H, d, seed=4)
+    cq, ck = np.arange(B + 1) * Lq, np.arange(B + 1) * Lk
+    flat = lambda t: t.reshape(-1, H, d)
+    o, lse = attn_fwd_ref(flat(q), flat(k), flat(v), 0.5, causal, cq, ck)
+    dq, dk, dv = attn_bwd_ref(flat(q), flat(k), flat(v), flat(do), 0.5, causal, cq, ck)
+    T = lambda t: t.transpose(0, 2, 1, 3)   # [B, L, H, d] -> [B, H, L, d]
+    od, lsed = attn_fwd_ref(T(q), T(k), T(v), 0.5, causal)
+    gd = attn_bwd_ref(T(q), T(k), T(v), T(do), 0.5, causal)
+    np.testing.assert_allclose(o.reshape(B, Lq, H, d), T(od), atol=1e-14)
+    np.testing.assert_allclose(lse.reshape(H, B, Lq).transpose(1, 0, 2), lsed, atol=1e-14)
+    for g, r, L in zip((dq, dk, dv), gd, (Lq, Lk, Lk)):
+        np.testing.assert_allclose(g.reshape(B, L, H, d), T(r), atol=1e-14)
+
+
 def test_rows_helper_matches_full_unit():
     q, k, v = rnd(10, 4, seed=1), rnd(10, 4, seed=2), rnd(10, 4, seed=3)
     rows = np.array([0, 3, 9])
@@ -288,6 +360,20 @@ def _bwd_mut(kind):
 @pytest.mark.parametrize("kind", ["D_sign", "D_axis", "no_scale", "dv_transpose"])
 def test_finite_differences_catch_planted_backward_mistakes(kind):
     assert _fd_check(_bwd_mut(kind), causal=True) > 1e-3
+
+
+def test_cross_bruteforce_catches_keys_read_at_query_offsets():
+    # a packed cross-attention oracle that slices keys with the query offsets
+    lq, lk = [2, 3], [4, 1]
+    x = wl.varlen_cross_inputs(lq, lk, 1, 3, "f32", "normal", seed=5)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    cq, ck = x["cu_seqlens_q"].numpy().tolist(), x["cu_seqlens_k"].numpy().tolist()
+    wrong = np.zeros(q.shape)
+    for s in range(2):
+        a, b = cq[s], cq[s + 1]
+        wrong[a:b, 0], _ = attn_fwd_unit(q[a:b, 0], k[a:b, 0], v[a:b, 0], 0.5, False)
+    ob = _cross_bruteforce(q, k, v, do, cq, ck, 0.5, False)[0]
+    assert np.max(np.abs(wrong - ob)) > 1e-3
 
 
 def test_bruteforce_catches_planted_mask_mistake():
