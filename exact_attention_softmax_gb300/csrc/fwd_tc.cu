@@ -8,21 +8,26 @@
 // for an A100) is prior art; here each CTA owns 256 query rows (two 128-row
 // tiles) of one (batch|sequence, head) and streams K/V blocks past them:
 //
-//   warp 8      TMA producer: Q tiles once, then K_j, V_j into a ring of slots
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j as
-//               tcgen05.mma, accumulators in TMEM
+//   warp 8      TMA producer: Q tiles, then K_j, V_j into a ring of slots,
+//               streaming from one work item into the next
+//   warps 9-10  MMA issuers (one thread each; one warp per Q tile for d <= 64,
+//               warp 9 alone for d = 128): S_t = Q_t K_j^T and O_t += P_t V_j
+//               as tcgen05.mma with fp32 accumulators in TMEM
 //   warps 0-3   softmax for tile 0: one thread per query row reads its S row
 //   warps 4-7   softmax for tile 1    from TMEM, masks, updates the running max
-//               m and sum l, writes P (fp16/bf16) to shared memory, rescales
-//               its O row in TMEM when m grew, and finally writes O = O/l and
-//               LSE = (m + log2 l) ln 2.
+//               m and sum l, writes P (fp16/bf16) back to TMEM, rescales its
+//               O row in TMEM when m grew past a threshold, and finally
+//               writes O = O/l and LSE = (m + log2 l) ln 2.
 //
-// The two tiles alternate on the tensor cores: while one softmax group works
-// on its tile, the MMAs of the other tile run. A softmax group releases S_t as
-// soon as it holds the row in registers, so Q_t K_{j+1}^T runs under its
-// exponentials; P is double-buffered in shared memory for d <= 64, and O is
-// rescaled only when a row maximum grows past a threshold. TMEM columns:
-// S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+// A softmax group releases S_t as soon as it holds the row in registers, so
+// Q_t K_{j+1}^T runs under its exponentials, and P.V reads P straight from
+// TMEM. For d <= 64 each CTA is persistent and takes work items from a
+// dynamic queue: Q is double-buffered, the next item's first S_t is issued
+// while the current item's last block is still in its softmax, and the
+// current item's epilogue is deferred into the next item's first block, so
+// consecutive items overlap instead of draining the pipeline.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0, O_1 (d each) and P_0, P_1
+// (64 columns each) after them; at d = 128 P_t overlays the upper half of S_t.
 #include <atomic>
 #include <type_traits>
 
@@ -65,9 +70,12 @@ struct Cfg {
   static constexpr int kSbo = 8 * kRowBytes;                  // 8-row group stride
   static constexpr int kColBlkBytes = 128 * kRowBytes;        // one column block of a 128-row tile
   static constexpr int kTileBytes = 128 * D * 2;              // a Q, K or V tile
-  static constexpr int kSlots = D == 128 ? 5 : (D == 64 ? 12 : 16);
+  // Q tiles are double-buffered where each CTA runs many work items (d <= 64),
+  // so the next item's Q and K/V stream in while the current item finishes.
+  static constexpr int kQBufs = D == 128 ? 1 : 2;
+  static constexpr int kSlots = D == 128 ? 5 : (D == 64 ? 10 : 16);
   static constexpr int kOffQ = 0;
-  static constexpr int kOffSlots = 2 * kTileBytes;
+  static constexpr int kOffSlots = 2 * kQBufs * kTileBytes;
   static constexpr int kOffBar = kOffSlots + kSlots * kTileBytes;
   static constexpr int kSmem = kOffBar + 512 + 1024;          // barriers + alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -91,8 +99,8 @@ struct Cfg {
 };
 
 struct __align__(8) Bars {
-  uint64_t q_full[2];     // Q_t loaded for the current work item
-  uint64_t q_empty[2];    // last S_t = Q_t K^T of a work item finished: Q_t may be reloaded
+  uint64_t q_full[4];     // Q_t loaded into buffer b ([t * kQBufs + b])
+  uint64_t q_empty[4];    // last S_t = Q_t K^T of a work item finished: buffer b may be reloaded
   uint64_t full[16];
   uint64_t empty[16];
   uint64_t s_full[2];     // S_t written by the tensor cores
@@ -202,9 +210,11 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       mbar_init(&bars->full[i], 1);
       mbar_init(&bars->empty[i], C::kMmaWarps);
     }
+    for (int i = 0; i < 2 * C::kQBufs; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->q_full[t], 1);
-      mbar_init(&bars->q_empty[t], 1);
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->s_free[t], BM);
       mbar_init(&bars->p_full[t], BM);
@@ -266,13 +276,15 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         auto c2k = [&](int row) { return PACKED ? it.tok0k + row : it.unit; };    // key rows
         for (int t = 0; t < 2 && ok; ++t) {
           if ((t == 0 ? it.n0 : it.n1) == 0) continue;
-          if (qloads[t] > 0 && !(ok = mbar_wait(&bars->q_empty[t], (qloads[t] - 1) & 1, abort_flag, p.status))) break;
+          // buffer qb of tile t was last used kQBufs loads ago
+          const int qb = t * C::kQBufs + qloads[t] % C::kQBufs, use = qloads[t] / C::kQBufs;
+          if (use > 0 && !(ok = mbar_wait(&bars->q_empty[qb], (use - 1) & 1, abort_flag, p.status))) break;
           ++qloads[t];
           if (p.debug & kDebugDropQArrive) continue;
-          mbar_expect_tx(&bars->q_full[t], C::kTileBytes);
+          mbar_expect_tx(&bars->q_full[qb], C::kTileBytes);
           const int row = it.r0 + t * BM;
           for (int cb = 0; cb < C::kNBlk; ++cb)
-            tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[t],
+            tma_load_3d(smem + C::kOffQ + qb * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[qb],
                         cb * C::kBlk, c1(row), c2(row));
         }
         for (int j = 0; j < it.nmax && ok; ++j) {
@@ -299,7 +311,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         for (int f = max(0, fill - C::kSlots); f < fill; ++f)
           mbar_wait_drain(&bars->full[f % C::kSlots], (f / C::kSlots) & 1);
         for (int t = 0; t < 2; ++t)
-          if (qloads[t] > 0 && !(p.debug & kDebugDropQArrive)) mbar_wait_drain(&bars->q_full[t], (qloads[t] - 1) & 1);
+          for (int n = max(0, qloads[t] - C::kQBufs); n < qloads[t]; ++n)
+            if (!(p.debug & kDebugDropQArrive))
+              mbar_wait_drain(&bars->q_full[t * C::kQBufs + n % C::kQBufs], (n / C::kQBufs) & 1);
       }
     }
   } else if (warp >= kMmaWarp && warp < kMmaWarp + C::kMmaWarps) {
@@ -317,8 +331,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       const uint64_t dQ = smem_desc(sQ, 16, C::kSbo, C::kSw);
       const uint64_t dSlot0K = smem_desc(sSlots, 16, C::kSbo, C::kSw);
       const uint64_t dSlot0V = smem_desc(sSlots, C::kColBlkBytes, C::kSbo, C::kSw);
-      auto issue_qk = [&](int t, int slot) {
-        const uint64_t a = dQ + ((t * C::kTileBytes) >> 4);
+      auto issue_qk = [&](int t, int qb, int slot) {
+        const uint64_t a = dQ + ((qb * C::kTileBytes) >> 4);
         const uint64_t b = dSlot0K + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -336,38 +350,55 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort_flag, p.status); };
       auto full_wait = [&](int pos) { return wait(&bars->full[pos % C::kSlots], (pos / C::kSlots) & 1); };
-      int fill = 0;
+      // Work items come from the producer's queue; the next one is read ahead
+      // so that its first S_t can be issued before the current item's last P.V.
+      int k = 0;                 // queue index of the current item
+      int next_idx = -2;         // queue entry k + 1 once read (-2: not yet)
+      auto take = [&](int kk, int& idx) {
+        const int q = kk % kItemQueue;
+        if (!wait(&bars->item_full[q], (kk / kItemQueue) & 1)) return false;
+        idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
+        mbar_arrive(&bars->item_empty[q]);
+        return true;
+      };
+      int fill = 0;              // ring position of the current item's K_0
       int qloads[2] = {0, 0};    // Q tiles consumed per tile slot
       int blocks[2] = {0, 0};    // K/V blocks processed per tile slot (barrier phases)
       int items[2] = {0, 0};     // work items finished per tile slot
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int q = k % kItemQueue;
-        if (!(ok = wait(&bars->item_full[q], (k / kItemQueue) & 1))) break;
-        const int idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
-        mbar_arrive(&bars->item_empty[q]);
-        if (idx < 0) break;
-        const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
-        if (it.nmax == 0) continue;
-        // first S_t of the item
-        for (int t = t_lo; t < t_hi && ok; ++t) {
-          if ((t == 0 ? it.n0 : it.n1) == 0) continue;
-          if (!(ok = wait(&bars->q_full[t], qloads[t] & 1))) break;
-          ++qloads[t];
-          // the previous item's last S_t must have been read (P overlaying S is
-          // ordered behind the last P.V on the tensor cores instead)
-          if (!C::kPAlias && blocks[t] > 0 && !(ok = wait(&bars->s_free[t], (blocks[t] - 1) & 1))) break;
-        }
-        if (!ok || !(ok = full_wait(fill))) break;
+      bool pre[2] = {false, false};   // first S_t of the current item already issued
+      // first S_t = Q_t K_0^T of item `x` whose K_0 sits at ring position `xfill`
+      auto first_qk = [&](const Item& x, int t, int xfill) {
+        const int nt = t == 0 ? x.n0 : x.n1;
+        const int qb = t * C::kQBufs + qloads[t] % C::kQBufs;
+        if (!wait(&bars->q_full[qb], (qloads[t] / C::kQBufs) & 1)) return false;
+        ++qloads[t];
+        // the tile's previous S_t must have been read (P overlaying S is
+        // ordered behind the last P.V on the tensor cores instead)
+        if (!C::kPAlias && blocks[t] > 0 && !wait(&bars->s_free[t], (blocks[t] - 1) & 1)) return false;
+        if (!full_wait(xfill)) return false;
         tc_fence_after();
-        for (int t = t_lo; t < t_hi; ++t) {
-          const int nt = t == 0 ? it.n0 : it.n1;
-          if (nt == 0) continue;
-          issue_qk(t, fill % C::kSlots);
-          mma_commit(&bars->s_full[t]);
-          if (nt == 1) mma_commit(&bars->q_empty[t]);
+        issue_qk(t, qb, xfill % C::kSlots);
+        mma_commit(&bars->s_full[t]);
+        if (nt == 1) mma_commit(&bars->q_empty[qb]);
+        return true;
+      };
+      bool ok = true;
+      int idx = -1;
+      ok = take(0, idx);
+      while (ok && idx >= 0) {
+        const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
+        int qbuf[2];             // Q buffer of this item per tile
+        for (int t = t_lo; t < t_hi; ++t) qbuf[t] = t * C::kQBufs + (qloads[t] - (pre[t] ? 1 : 0)) % C::kQBufs;
+        if (it.nmax > 0) {
+          for (int t = t_lo; t < t_hi && ok; ++t) {
+            if ((t == 0 ? it.n0 : it.n1) == 0 || pre[t]) continue;
+            qbuf[t] = t * C::kQBufs + qloads[t] % C::kQBufs;
+            ok = first_qk(it, t, fill);
+          }
+          if (!ok) break;
+          mma_commit(&bars->empty[fill % C::kSlots]);
         }
-        mma_commit(&bars->empty[fill % C::kSlots]);
+        pre[0] = pre[1] = false;   // from here on pre[] is about the next item
         for (int j = 0; j < it.nmax && ok; ++j) {
           // K_{j+1} sits at ring position fill + 2j + 2, V_j at fill + 2j + 1
           const bool has_next = j + 1 < it.nmax;
@@ -383,9 +414,23 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               // S_t may be overwritten once its softmax group holds it in registers
               if (!(ok = wait(&bars->s_free[t], g & 1))) break;
               tc_fence_after();
-              issue_qk(t, kpos % C::kSlots);
+              issue_qk(t, qbuf[t], kpos % C::kSlots);
               mma_commit(&bars->s_full[t]);
-              if (j + 2 == nt) mma_commit(&bars->q_empty[t]);
+              if (j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
+            } else if (!C::kPAlias && j + 1 == nt) {
+              // last block of this tile: read the next work item and issue its
+              // first S_t now, under this block's softmax
+              if (next_idx == -2 && !(ok = take(k + 1, next_idx))) break;
+              if (next_idx >= 0) {
+                const Item nx = decode_item<CAUSAL, PACKED>(p, next_idx, npairs);
+                if (nx.nmax > 0 && (t == 0 ? nx.n0 : nx.n1) > 0) {
+                  blocks[t] += nt;            // the phases of S_t continue into the next item
+                  ok = first_qk(nx, t, fill + 2 * it.nmax);
+                  blocks[t] -= nt;
+                  if (!ok) break;
+                  pre[t] = true;
+                }
+              }
             }
             if (!(ok = wait(&bars->p_full[t], g & 1))) break;
             // O_t is overwritten by the item's first P.V: the previous item's
@@ -396,20 +441,28 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             mma_commit(&bars->pv_done[t]);
             if (C::kPAlias && j + 1 < nt) {
               // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
-              issue_qk(t, kpos % C::kSlots);
+              issue_qk(t, qbuf[t], kpos % C::kSlots);
               mma_commit(&bars->s_full[t]);
-              if (j + 2 == nt) mma_commit(&bars->q_empty[t]);
+              if (j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
             }
           }
           mma_commit(&bars->empty[vpos % C::kSlots]);
           if (has_next) mma_commit(&bars->empty[kpos % C::kSlots]);
         }
+        if (!ok) break;
         for (int t = t_lo; t < t_hi; ++t) {
           const int nt = t == 0 ? it.n0 : it.n1;
           blocks[t] += nt;
           if (nt > 0) ++items[t];
         }
         fill += 2 * it.nmax;
+        ++k;
+        if (next_idx != -2) {
+          idx = next_idx;
+          next_idx = -2;
+        } else {
+          ok = take(k, idx);
+        }
       }
       mma_commit(&bars->done);
       mbar_wait_drain(&bars->done, 0);
@@ -430,6 +483,40 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.status));
     };
     int blocks = 0;   // K/V blocks processed by this tile slot so far (barrier phases)
+    // Epilogue of a finished work item: O = O / l rounded once, LSE = (m + log2 l) ln 2.
+    // Where a CTA runs many items (d <= 64) it is deferred into the next item's
+    // first block, after that block's P has been handed to the tensor cores, so
+    // the wait for the item's last P.V overlaps the next item's exponentials.
+    constexpr bool kDefer = !C::kPAlias;
+    struct Pending {
+      bool on;
+      float m, l;
+      long long orow, li;     // output row offset (elements) and LSE index; orow < 0: row past the end
+    } pend{false, 0.f, 0.f, -1, 0};
+    auto epilogue = [&](const Pending& e) {
+      tc_fence_after();
+      const float inv = __frcp_rn(e.l);
+      uint32_t ov[D / 2];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          ov[cc * 16 + x] = Pack2<T>::pack(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+      }
+      // O_t has been read out: the next item's first P.V may overwrite it
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+      if (e.orow >= 0) {
+        T* orow = static_cast<T*>(p.o) + e.orow;
+#pragma unroll
+        for (int x = 0; x < D / 8; ++x)
+          *reinterpret_cast<uint4*>(orow + 8 * x) = make_uint4(ov[4 * x], ov[4 * x + 1], ov[4 * x + 2], ov[4 * x + 3]);
+        p.lse[e.li] = (e.m + __log2f(e.l)) * kLn2;
+      }
+    };
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int q = k % kItemQueue;
@@ -461,11 +548,10 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         float* x = reinterpret_cast<float*>(sr);
         const int kbase = j * BN;
         if ((kbase + BN > it.len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
+          // keys kbase + i with i >= lim are past the end or (causal) after the row
+          const int lim = (CAUSAL ? min(it.len_k, row + 1) : it.len_k) - kbase;
 #pragma unroll
-          for (int i = 0; i < BN; ++i) {
-            const int key = kbase + i;
-            if (key >= it.len_k || (CAUSAL && key > row)) x[i] = -INFINITY;
-          }
+          for (int i = 0; i < BN; ++i) x[i] = i < lim ? x[i] : -INFINITY;
         }
         // row maximum: four independent chains of three-input max
         float mx0 = max3f(x[0], x[1], x[2]), mx1 = max3f(x[3], x[4], x[5]);
@@ -507,9 +593,10 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int u = 0; u < 4; ++u) pk[chunk * 4 + u] = Pack2<T>::pack(e[2 * u], e[2 * u + 1]);
           }
-          // P_t's columns are free once O_t += P_{j-1} V_{j-1} has finished (at d = 128
-          // they overlay S_t, already in registers, and that MMA finished before S_j)
-          if (half == 0 && !C::kPAlias && j > 0) ok = wait_all(&bars->pv_done[t], (g - 1) & 1);
+          // P_t's columns are free once the previous P.V on this tile (possibly
+          // the last one of the previous item) has finished; at d = 128 they
+          // overlay S_t, already in registers, and that MMA finished before S_j
+          if (half == 0 && !C::kPAlias && (j > 0 || pend.on)) ok = wait_all(&bars->pv_done[t], (g - 1) & 1);
           if (!ok) break;
           tmem_st32(tP + half * 32, pk);
         }
@@ -532,37 +619,29 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
+        if (kDefer && j == 0 && pend.on) {
+          // the previous item's last P.V was waited for above
+          epilogue(pend);
+          pend.on = false;
+        }
       }
-      if (!ok || !(ok = wait_all(&bars->pv_done[t], (blocks + nt - 1) & 1))) break;
+      if (!ok) break;
       blocks += nt;
-      // epilogue: O = O / l rounded once, LSE = (m + log2 l) ln 2. O_t is read
-      // into packed registers first and released to the next item's first P.V.
-      tc_fence_after();
-      const float inv = 1.f / l;
-      uint32_t ov[D / 2];
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tO + cc * 32, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          ov[cc * 16 + e] = Pack2<T>::pack(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->o_free[t]);
-      if (row < it.len_q) {
-        T* orow = static_cast<T*>(p.o) +
-                  (PACKED ? (static_cast<long long>(it.tok0 + row) * p.H + it.h) * D
-                          : (static_cast<long long>(it.unit) * it.len_q + row) * D);
-#pragma unroll
-        for (int e = 0; e < D / 8; ++e)
-          *reinterpret_cast<uint4*>(orow + 8 * e) = make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
-        const long long li = PACKED ? static_cast<long long>(it.h) * p.Lq + it.tok0 + row
-                                    : static_cast<long long>(it.unit) * it.len_q + row;
-        p.lse[li] = (m_run + __log2f(l)) * kLn2;
+      pend.on = true;
+      pend.m = m_run;
+      pend.l = l;
+      pend.orow = row < it.len_q ? (PACKED ? (static_cast<long long>(it.tok0 + row) * p.H + it.h) * D
+                                           : (static_cast<long long>(it.unit) * it.len_q + row) * D)
+                                 : -1;
+      pend.li = PACKED ? static_cast<long long>(it.h) * p.Lq + it.tok0 + row
+                       : static_cast<long long>(it.unit) * it.len_q + row;
+      if (!kDefer) {
+        if (!(ok = wait_all(&bars->pv_done[t], (blocks - 1) & 1))) break;
+        epilogue(pend);
+        pend.on = false;
       }
     }
+    if (ok && pend.on && wait_all(&bars->pv_done[t], (blocks - 1) & 1)) epilogue(pend);
   }
 
   tc_fence_before();
