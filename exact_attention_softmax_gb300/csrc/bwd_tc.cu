@@ -24,6 +24,8 @@
 // buffers so its drain overlaps the next tile.
 #include <type_traits>
 
+#include <algorithm>
+
 #include "ptx.cuh"
 
 namespace sdpa {
@@ -128,15 +130,19 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   BBars* bars = reinterpret_cast<BBars*>(smem + C::kOffBar);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  // Unit-major order: the key blocks of one (batch, head) run side by side and
-  // share its Q / dO through L2; under causal masking key block 0 (the most
-  // query tiles) goes first.
   // Packed batches: a unit is (sequence, head); its queries are rows
   // cu_seqlens[s] .. cu_seqlens[s+1]-1 of the query token axis, its keys rows
   // cu_k[s] .. cu_k[s+1]-1 of the key token axis, and p.Lk bounds every key length.
   const int nkb = (p.Lk + BK - 1) / BK;
-  const int unit = blockIdx.x / nkb;
-  const int kblk = blockIdx.x % nkb;
+  // CTAs go out in groups of bp.group units; inside a group key block 0 of
+  // every unit comes first, then key block 1, and so on. Under causal masking
+  // low key blocks see the most query rows, so the longest CTAs start first,
+  // while a group's Q, dO and dQ accumulator stay small enough for L2.
+  const int per_group = bp.group * nkb;
+  const int grp = blockIdx.x / per_group, rg = blockIdx.x % per_group;
+  const int gunits = min(bp.group, p.B * p.H - grp * bp.group);
+  const int unit = grp * bp.group + rg % gunits;
+  const int kblk = rg / gunits;
   const int key0 = kblk * BK;
   int Lq = p.Lq, Lk = p.Lk, tok0 = 0, tok0k = 0, head = 0;
   if (PACKED) {
@@ -541,10 +547,18 @@ cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
     attr_set[dev] = 1;
   }
   const Problem& p = bp.f;
-  const long long blocks = static_cast<long long>((p.Lk + BK - 1) / BK) * p.B * p.H;
+  const long long units = static_cast<long long>(p.B) * p.H;
+  const long long blocks = static_cast<long long>((p.Lk + BK - 1) / BK) * units;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), kThreads, BCfg<D>::kSmem, s>>>(bp, m.q, m.k, m.v, m.dO);
+  BwdProblem g = bp;
+  // causal: as many units per group as keep their Q, dO (2 bytes per element)
+  // and dQ accumulator (4) within kL2Budget; without masking every CTA has
+  // the same work and the units simply go one after another
+  constexpr long long kL2Budget = 48ll << 20;
+  const long long unit_bytes = static_cast<long long>(p.cu_seqlens ? p.max_q : p.Lq) * D * 8;
+  g.group = p.causal ? static_cast<int>(std::max(1ll, std::min(units, kL2Budget / std::max(1ll, unit_bytes)))) : 1;
+  kern<<<static_cast<unsigned>(blocks), kThreads, BCfg<D>::kSmem, s>>>(g, m.q, m.k, m.v, m.dO);
   return cudaGetLastError();
 }
 

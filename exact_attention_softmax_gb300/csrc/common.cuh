@@ -48,6 +48,7 @@ struct BwdProblem {
   void* dv;
   float* delta;       // [rows] fp32 workspace: rowsum(dO * O)
   float* dq_acc;      // [rows, d] fp32 workspace (tensor-core path only)
+  int group;          // tensor-core kernel: units per scheduling group (set by its launcher)
 };
 
 // Tensor maps for the tensor-core kernels (built on the host by the C-ABI layer).

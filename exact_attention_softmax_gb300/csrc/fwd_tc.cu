@@ -159,8 +159,13 @@ struct Item {
 template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npairs) {
   Item it;
-  it.unit = idx / npairs;
-  const int ord = idx % npairs;
+  // Causal items get shorter with their query position, so they are handed
+  // out longest first across all units (ord-major), which keeps the last
+  // CTAs to finish from starting long items late; without masking every item
+  // costs the same and the units are taken one after another.
+  const int units = p.B * p.H;
+  it.unit = CAUSAL ? idx % units : idx / npairs;
+  const int ord = CAUSAL ? idx / units : idx % npairs;
   const int pair = CAUSAL ? (npairs - 1 - ord) : ord;
   it.h = 0;
   it.tok0 = it.tok0k = 0;
