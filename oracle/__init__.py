@@ -10,5 +10,6 @@ from .attention import (  # noqa: F401
     attn_fwd_ref,
     attn_fwd_rows,
     attn_fwd_unit,
+    expand_block_mask,
 )
 from .bruteforce import bwd_bruteforce, fwd_bruteforce  # noqa: F401

@@ -30,6 +30,13 @@ causal masking is top-left aligned (key j is visible to query i iff j <= i);
 shape ``[B, H, Lq]`` dense and ``[H, total]`` packed; a unit with Lq = 0
 yields empty outputs; Lk = 0 with Lq > 0 is an error.
 
+Block-sparse attention (the FlashAttention article's "block-sparse
+FlashAttention", section "FlashAttention", which it only names): the
+attention of the plain definition restricted to the (query block, key block)
+tiles a 0/1 block mask keeps; every other score is excluded like a causally
+masked one. Reading taken where the article is silent: a query row left with
+no visible key gets O = 0 and LSE = -inf (and no gradient).
+
 Layouts: dense tensors are ``[..., L, d]`` (any leading batch/head dims, the
 tutorial's ``[B, H, L, d]`` and its ``[2, 3, 8]`` example both fit); packed
 variable-length tensors (the tutorial's NestedTensor section) are
@@ -51,6 +58,7 @@ __all__ = [
     "attn_fwd_ref",
     "attn_bwd_ref",
     "attn_fwd_rows",
+    "expand_block_mask",
 ]
 
 
@@ -58,10 +66,13 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def _scores(q: np.ndarray, k: np.ndarray, scale: float, is_causal: bool) -> np.ndarray:
+def _scores(q: np.ndarray, k: np.ndarray, scale: float, is_causal: bool, visible=None) -> np.ndarray:
     """S = scale * Q K^T with masked entries set to -inf (SDPA tutorial, "Overview";
-    causal mask: "Causal Self Attention")."""
+    causal mask: "Causal Self Attention"; ``visible``: an extra [Lq, Lk] boolean
+    mask, e.g. a block-sparse pattern)."""
     s = float(scale) * (q @ k.T)
+    if visible is not None:
+        s = np.where(visible, s, -np.inf)
     if is_causal:
         lq, lk = s.shape
         i = np.arange(lq)[:, None]
@@ -70,12 +81,13 @@ def _scores(q: np.ndarray, k: np.ndarray, scale: float, is_causal: bool) -> np.n
     return s
 
 
-def attention_probs(q, k, scale: float, is_causal: bool = False):
+def attention_probs(q, k, scale: float, is_causal: bool = False, visible=None):
     """P = softmax_j(S_ij) and LSE_i for one (batch, head) unit.
 
     ``q``: [Lq, d], ``k``: [Lk, d]. Returns ``(P [Lq, Lk], LSE [Lq])`` in float64.
     The row maximum is subtracted before exponentiating (a rounding measure
-    only; softmax is shift invariant).
+    only; softmax is shift invariant). ``visible`` ([Lq, Lk] bool, optional)
+    excludes further scores; a row it leaves empty gets P = 0, LSE = -inf.
     """
     q, k = _f64(q), _f64(k)
     lq, lk = q.shape[0], k.shape[0]
@@ -83,29 +95,33 @@ def attention_probs(q, k, scale: float, is_causal: bool = False):
         return np.zeros((0, lk)), np.zeros((0,))
     if lk == 0:
         raise ValueError("softmax over an empty key set is undefined (Lk = 0 with Lq > 0)")
-    s = _scores(q, k, scale, is_causal)
+    s = _scores(q, k, scale, is_causal, visible)
     m = np.max(s, axis=1, keepdims=True)
+    empty = ~np.isfinite(m[:, 0])
+    m = np.where(np.isfinite(m), m, 0.0)
     e = np.exp(s - m)
     z = np.sum(e, axis=1, keepdims=True)
-    p = e / z
-    lse = (m + np.log(z))[:, 0]
+    p = e / np.where(z > 0, z, 1.0)
+    with np.errstate(divide="ignore"):
+        lse = (m + np.log(z))[:, 0]
+    lse[empty] = -np.inf
     return p, lse
 
 
-def attn_fwd_unit(q, k, v, scale: float, is_causal: bool = False):
+def attn_fwd_unit(q, k, v, scale: float, is_causal: bool = False, visible=None):
     """O = P V and LSE for one unit. ``v``: [Lk, dv]. Returns (O [Lq, dv], LSE [Lq])."""
     v = _f64(v)
-    p, lse = attention_probs(q, k, scale, is_causal)
+    p, lse = attention_probs(q, k, scale, is_causal, visible)
     return p @ v, lse
 
 
-def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False):
+def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False, visible=None):
     """Gradients of sum(dO * O) w.r.t. Q, K, V for one unit (chain rule through
     the softmax; the pages only say the backward recomputes attention)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     if q.shape[0] == 0:
         return np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    p, _ = attention_probs(q, k, scale, is_causal)
+    p, _ = attention_probs(q, k, scale, is_causal, visible)
     dv = p.T @ do
     dp = do @ v.T
     dsum = np.sum(p * dp, axis=1, keepdims=True)
@@ -117,6 +133,27 @@ def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False):
 
 def _units_dense(x: np.ndarray) -> np.ndarray:
     return x.reshape((-1,) + x.shape[-2:])
+
+
+def expand_block_mask(block_mask, lq: int, lk: int, block: int = 128) -> np.ndarray:
+    """[..., ceil(Lq/block), ceil(Lk/block)] 0/1 block mask -> [..., Lq, Lk]
+    booleans: score (i, j) is kept iff its tile (i // block, j // block) is."""
+    bm = np.asarray(block_mask) != 0
+    nq, nk = -(-lq // block), -(-lk // block)
+    if bm.shape[-2:] != (nq, nk):
+        raise ValueError(f"block mask must end in ({nq}, {nk}) for Lq={lq}, Lk={lk}, block={block}")
+    rows = np.arange(lq) // block
+    cols = np.arange(lk) // block
+    return bm[..., rows, :][..., :, cols]
+
+
+def _unit_masks(block_mask, lead, lq, lk, block):
+    """Per-unit [Lq, Lk] masks for a dense batch with leading dims ``lead``."""
+    if block_mask is None:
+        return None
+    full = expand_block_mask(block_mask, lq, lk, block)
+    full = np.broadcast_to(full, tuple(lead) + (lq, lk))
+    return full.reshape((-1, lq, lk))
 
 
 def _check_cu(cu_seqlens, total: int) -> np.ndarray:
@@ -135,7 +172,8 @@ def _packed_spans(cu_seqlens, cu_seqlens_k, total_q: int, total_k: int):
     return [(int(cq[s]), int(cq[s + 1]), int(ck[s]), int(ck[s + 1])) for s in range(cq.size - 1)]
 
 
-def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None):
+def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None,
+                 block_mask=None, block_size: int = 128):
     """Forward over a whole batch.
 
     Dense: ``q`` [..., Lq, d], ``k``/``v`` [..., Lk, d] -> ``O`` [..., Lq, d],
@@ -145,16 +183,21 @@ def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None
     tutorial's NestedTensor batches without padding). With ``cu_seqlens_k``
     the keys/values are [total_k, H, d] and sequence s owns key rows
     ``cu_seqlens_k[s] : cu_seqlens_k[s+1]``.
+    Dense only: ``block_mask`` [..., ceil(Lq/block_size), ceil(Lk/block_size)]
+    (broadcast over the leading dims) keeps or drops whole score tiles.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     if cu_seqlens is None:
         lead = q.shape[:-2]
         qu, ku, vu = _units_dense(q), _units_dense(k), _units_dense(v)
+        vis = _unit_masks(block_mask, lead, q.shape[-2], k.shape[-2], block_size)
         o = np.empty(qu.shape[:2] + (vu.shape[-1],))
         lse = np.empty(qu.shape[:2])
         for u in range(qu.shape[0]):
-            o[u], lse[u] = attn_fwd_unit(qu[u], ku[u], vu[u], scale, is_causal)
+            o[u], lse[u] = attn_fwd_unit(qu[u], ku[u], vu[u], scale, is_causal, None if vis is None else vis[u])
         return o.reshape(lead + o.shape[1:]), lse.reshape(lead + lse.shape[1:])
+    if block_mask is not None:
+        raise ValueError("block masks apply to dense batches only")
     total, nh, _ = q.shape
     o = np.zeros((total, nh, v.shape[-1]))
     lse = np.zeros((nh, total))
@@ -166,16 +209,21 @@ def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None
     return o, lse
 
 
-def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None):
+def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None,
+                 block_mask=None, block_size: int = 128):
     """Backward over a whole batch; same layouts as :func:`attn_fwd_ref`.
     Returns ``(dQ, dK, dV)`` in float64."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     if cu_seqlens is None:
         qu, ku, vu, du = (_units_dense(x) for x in (q, k, v, do))
+        vis = _unit_masks(block_mask, q.shape[:-2], q.shape[-2], k.shape[-2], block_size)
         dq, dk, dv = np.empty_like(qu), np.empty_like(ku), np.empty_like(vu)
         for u in range(qu.shape[0]):
-            dq[u], dk[u], dv[u] = attn_bwd_unit(qu[u], ku[u], vu[u], du[u], scale, is_causal)
+            dq[u], dk[u], dv[u] = attn_bwd_unit(qu[u], ku[u], vu[u], du[u], scale, is_causal,
+                                                None if vis is None else vis[u])
         return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
+    if block_mask is not None:
+        raise ValueError("block masks apply to dense batches only")
     total, nh, _ = q.shape
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     for a, b, c, e in _packed_spans(cu_seqlens, cu_seqlens_k, total, k.shape[0]):

@@ -18,11 +18,15 @@ import math
 __all__ = ["fwd_bruteforce", "bwd_bruteforce"]
 
 
-def _visible(i: int, j: int, is_causal: bool) -> bool:
+def _visible(i: int, j: int, is_causal: bool, allowed=None) -> bool:
+    """Key j is visible to query i: causal (top-left) and, when given, the
+    explicit set ``allowed`` of (i, j) pairs (block-sparse attention)."""
+    if allowed is not None and (i, j) not in allowed:
+        return False
     return (not is_causal) or j <= i
 
 
-def _probs(q, k, scale, is_causal):
+def _probs(q, k, scale, is_causal, allowed=None):
     lq, lk, d = len(q), len(k), len(q[0]) if q else 0
     p = [[0.0] * lk for _ in range(lq)]
     lse = [0.0] * lq
@@ -30,30 +34,36 @@ def _probs(q, k, scale, is_causal):
         w = [0.0] * lk
         z = 0.0
         for j in range(lk):
-            if _visible(i, j, is_causal):
+            if _visible(i, j, is_causal, allowed):
                 dot = 0.0
                 for c in range(d):
                     dot += q[i][c] * k[j][c]
                 w[j] = math.exp(scale * dot)
                 z += w[j]
+        if z == 0.0:
+            # no visible key (possible only with `allowed`): the row's
+            # probabilities are all zero and its log-sum-exp is -inf
+            lse[i] = -math.inf
+            continue
         for j in range(lk):
             p[i][j] = w[j] / z
         lse[i] = math.log(z)
     return p, lse
 
 
-def fwd_bruteforce(q, k, v, scale, is_causal=False):
-    """q: list[Lq][d], k: list[Lk][d], v: list[Lk][dv] -> (O list[Lq][dv], LSE list[Lq])."""
-    p, lse = _probs(q, k, scale, is_causal)
+def fwd_bruteforce(q, k, v, scale, is_causal=False, allowed=None):
+    """q: list[Lq][d], k: list[Lk][d], v: list[Lk][dv] -> (O list[Lq][dv], LSE list[Lq]).
+    ``allowed``: optional set of visible (query, key) index pairs."""
+    p, lse = _probs(q, k, scale, is_causal, allowed)
     dv = len(v[0])
     o = [[sum(p[i][j] * v[j][c] for j in range(len(k))) for c in range(dv)] for i in range(len(q))]
     return o, lse
 
 
-def bwd_bruteforce(q, k, v, do, scale, is_causal=False):
+def bwd_bruteforce(q, k, v, do, scale, is_causal=False, allowed=None):
     """Gradients of sum(dO * O) by the explicit softmax Jacobian."""
     lq, lk, d, dv_ = len(q), len(k), len(q[0]), len(v[0])
-    p, _ = _probs(q, k, scale, is_causal)
+    p, _ = _probs(q, k, scale, is_causal, allowed)
     # dL/dP_ij = sum_c dO_ic V_jc
     gp = [[sum(do[i][c] * v[j][c] for c in range(dv_)) for j in range(lk)] for i in range(lq)]
     # dL/dS_ik = sum_j gp_ij * P_ij * (delta_jk - P_ik)

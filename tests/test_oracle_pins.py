@@ -18,7 +18,7 @@ import pytest
 import torch
 
 from oracle import (attention_probs, attn_bwd_ref, attn_bwd_unit, attn_fwd_ref,
-                    attn_fwd_rows, attn_fwd_unit, bwd_bruteforce, fwd_bruteforce)
+                    attn_fwd_rows, attn_fwd_unit, bwd_bruteforce, expand_block_mask, fwd_bruteforce)
 from exact_attention_softmax_gb300 import workloads as wl
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -255,6 +255,101 @@ def test_blhd_batch_is_packed_with_uniform_offsets(causal):
         np.testing.assert_allclose(g.reshape(B, L, H, d), T(r), atol=1e-14)
 
 
+# ------------------------------------------------------------- block-sparse
+
+def _allowed_pairs(bm, lq, lk, block):
+    """Visible (i, j) pairs of a block mask, enumerated with plain loops."""
+    out = set()
+    for i in range(lq):
+        for j in range(lk):
+            if bm[i // block][j // block]:
+                out.add((i, j))
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_matches_bruteforce(causal):
+    # tiles of 2 on a 7 x 9 score matrix (ragged last tiles); row block 1 keeps
+    # nothing, so its rows must come out empty
+    lq, lk, d, blk = 7, 9, 3, 2
+    bm = np.array([[1, 0, 1, 0, 1], [0, 0, 0, 0, 0], [0, 1, 1, 0, 0], [1, 0, 0, 1, 1]])
+    q, k, v, do = rnd(lq, d, seed=31), rnd(lk, d, seed=32), rnd(lk, d, seed=33), rnd(lq, d, seed=34)
+    o, lse = attn_fwd_ref(q[None], k[None], v[None], 0.7, causal, block_mask=bm, block_size=blk)
+    grads = attn_bwd_ref(q[None], k[None], v[None], do[None], 0.7, causal, block_mask=bm, block_size=blk)
+    allowed = _allowed_pairs(bm, lq, lk, blk)
+    ob, lb = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.7, causal, allowed)
+    gb = bwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), do.tolist(), 0.7, causal, allowed)
+    np.testing.assert_allclose(o[0], np.array(ob), rtol=0, atol=1e-13)
+    np.testing.assert_array_equal(np.isinf(lse[0]), np.isinf(np.array(lb)))
+    fin = np.isfinite(lse[0])
+    np.testing.assert_allclose(lse[0][fin], np.array(lb)[fin], rtol=0, atol=1e-13)
+    for g, r in zip(grads, gb):
+        np.testing.assert_allclose(g[0], np.array(r), rtol=0, atol=1e-13)
+    # rows 2 and 3 (row block 1) see nothing: O = 0, LSE = -inf, no gradient
+    assert np.all(o[0][2:4] == 0) and np.all(np.isneginf(lse[0][2:4])) and np.all(grads[0][0][2:4] == 0)
+
+
+def test_block_mask_of_ones_is_plain_attention():
+    q, k, v, do = rnd(2, 3, 10, 4, seed=1), rnd(2, 3, 6, 4, seed=2), rnd(2, 3, 6, 4, seed=3), rnd(2, 3, 10, 4, seed=4)
+    for causal in (False, True):
+        a = attn_fwd_ref(q, k, v, 0.5, causal) + attn_bwd_ref(q, k, v, do, 0.5, causal)
+        b = (attn_fwd_ref(q, k, v, 0.5, causal, block_mask=np.ones((4, 2)), block_size=3)
+             + attn_bwd_ref(q, k, v, do, 0.5, causal, block_mask=np.ones((4, 2)), block_size=3))
+        for x1, x2 in zip(a, b):
+            np.testing.assert_array_equal(x1, x2)
+
+
+def test_block_diagonal_mask_is_independent_blocks():
+    # a block-diagonal mask splits the sequence into independent pieces: each
+    # equals plain attention over its own slice
+    n, blk, d = 3, 4, 5
+    q, k, v, do = (rnd(1, 2, n * blk, d, seed=s) for s in (5, 6, 7, 8))
+    o, lse = attn_fwd_ref(q, k, v, 0.4, False, block_mask=np.eye(n), block_size=blk)
+    dq, dk, dv = attn_bwd_ref(q, k, v, do, 0.4, False, block_mask=np.eye(n), block_size=blk)
+    for h in range(2):
+        for b in range(n):
+            sl = slice(b * blk, (b + 1) * blk)
+            od, ld = attn_fwd_unit(q[0, h, sl], k[0, h, sl], v[0, h, sl], 0.4)
+            gd = attn_bwd_unit(q[0, h, sl], k[0, h, sl], v[0, h, sl], do[0, h, sl], 0.4)
+            np.testing.assert_allclose(o[0, h, sl], od, atol=1e-14)
+            np.testing.assert_allclose(lse[0, h, sl], ld, atol=1e-14)
+            for g, r in zip((dq, dk, dv), gd):
+                np.testing.assert_allclose(g[0, h, sl], r, atol=1e-14)
+
+
+def test_block_sparse_backward_finite_differences():
+    lq, lk, d, blk = 5, 6, 3, 2
+    bm = np.array([[1, 1, 0], [0, 1, 1], [1, 0, 1]])
+    q, k, v, do = rnd(lq, d, seed=41), rnd(lk, d, seed=42), rnd(lk, d, seed=43), rnd(lq, d, seed=44)
+    dq, dk, dv = attn_bwd_ref(q, k, v, do, 0.6, True, block_mask=bm, block_size=blk)
+
+    def loss(qq, kk, vv):
+        o, _ = attn_fwd_ref(qq, kk, vv, 0.6, True, block_mask=bm, block_size=blk)
+        return float(np.sum(do * o))
+    h = 1e-6
+    for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which], args_m[which] = xp, xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert np.max(np.abs(num - g)) <= 1e-7 * max(1.0, np.max(np.abs(g)))
+
+
+def test_expand_block_mask_shapes():
+    bm = np.array([[1, 0], [0, 1], [1, 1]])
+    full = expand_block_mask(bm, 5, 3, 2)
+    assert full.shape == (5, 3)
+    assert full[0].tolist() == [True, True, False] and full[2].tolist() == [False, False, True]
+    assert full[4].tolist() == [True, True, True]
+    with pytest.raises(ValueError):
+        expand_block_mask(bm, 7, 3, 2)
+
+
 def test_rows_helper_matches_full_unit():
     q, k, v = rnd(10, 4, seed=1), rnd(10, 4, seed=2), rnd(10, 4, seed=3)
     rows = np.array([0, 3, 9])
@@ -374,6 +469,16 @@ def test_cross_bruteforce_catches_keys_read_at_query_offsets():
         wrong[a:b, 0], _ = attn_fwd_unit(q[a:b, 0], k[a:b, 0], v[a:b, 0], 0.5, False)
     ob = _cross_bruteforce(q, k, v, do, cq, ck, 0.5, False)[0]
     assert np.max(np.abs(wrong - ob)) > 1e-3
+
+
+def test_bruteforce_catches_transposed_block_mask():
+    # an oracle that applied the block mask transposed (key blocks as rows)
+    lq = lk = 6
+    bm = np.array([[1, 0, 0], [1, 1, 0], [0, 1, 1]])
+    q, k, v = rnd(lq, 3, seed=51), rnd(lk, 3, seed=52), rnd(lk, 3, seed=53)
+    wrong, _ = attn_fwd_ref(q[None], k[None], v[None], 0.5, False, block_mask=bm.T, block_size=2)
+    ob, _ = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.5, False, _allowed_pairs(bm, lq, lk, 2))
+    assert np.max(np.abs(wrong[0] - np.array(ob))) > 1e-3
 
 
 def test_bruteforce_catches_planted_mask_mistake():
