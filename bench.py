@@ -303,6 +303,62 @@ def per_workload_results(dev, flush, peaks, peak_kind):
     return out
 
 
+def extra_results(dev, flush, peaks):
+    """Timings of the layouts and masks added beyond the five workloads:
+    block-sparse attention and packed cross-attention (N = 1 only)."""
+    import torch
+    import exact_attention_softmax_gb300 as ops
+    from exact_attention_softmax_gb300 import workloads as wl
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(name, fwd, bwd, ff, bf, desc):
+        for _ in range(3):
+            fwd()
+            bwd()
+        torch.cuda.synchronize()
+        tf = time_calls(fwd, 20, flush, stream)
+        tb = time_calls(bwd, 20, flush, stream)
+        res = {"config": desc, "fwd_us": 1e3 * statistics.median(tf), "bwd_us": 1e3 * statistics.median(tb)}
+        res["fwd_tflops"] = ff / (res["fwd_us"] * 1e-6) / 1e12
+        res["bwd_tflops"] = bf / (res["bwd_us"] * 1e-6) / 1e12
+        res["fwd_frac_of_peak"] = res["fwd_tflops"] / peaks["bf16_tflops"]
+        out[name] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in res.items()}
+
+    # block-sparse: half of the 128 x 128 score tiles kept (seeded), flops counted on kept tiles
+    B, H, L, d = 4, 16, 4096, 64
+    x = wl.dense_inputs(B, H, L, L, d, "f16", "normal", seed=0)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    mask = wl.block_mask((B, H, L // 128, L // 128), 0.5, seed=0).to(dev)
+    kept = float(mask.sum().item()) * 128 * 128
+    o, lse = ops.sdpa_fwd_blocksparse(q, k, v, mask)
+    ws = torch.empty(ops.sdpa_bwd_workspace_size(B, H, L, d, 1), dtype=torch.uint8, device=dev)
+    g = [torch.empty_like(t) for t in (q, k, v)]
+    timed("blocksparse_f16_d64", lambda: ops.sdpa_fwd_blocksparse(q, k, v, mask, o, lse),
+          lambda: ops.sdpa_bwd_blocksparse(q, k, v, o, lse, do, mask, *g, workspace=ws),
+          4 * d * kept, 2.5 * 4 * d * kept,
+          f"B={B} H={H} L={L} d={d} f16 non-causal, 50 % of 128x128 tiles kept (seeded)")
+    del q, k, v, do, o, lse, g, ws, x
+
+    # packed cross-attention: 32 sequences, queries around 256 long, keys around 512
+    lq = wl.varlen_lengths(32, 512, 0.5, 0)
+    lk = wl.varlen_lengths(32, 1024, 0.5, 1)
+    x = wl.varlen_cross_inputs(lq, lk, 8, 64, "f16", "normal", seed=0)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    cq, ck = x["cu_seqlens_q"].to(dev), x["cu_seqlens_k"].to(dev)
+    mq, mk = x["max_seqlen_q"], x["max_seqlen_k"]
+    o, lse = ops.sdpa_fwd_varlen(q, k, v, cq, ck, mq, mk)
+    ws = torch.empty(ops.sdpa_bwd_workspace_size(1, 8, q.shape[0], 64, 1), dtype=torch.uint8, device=dev)
+    g = [torch.empty_like(t) for t in (q, k, v)]
+    pairs = float(sum(a * b for a, b in zip(lq, lk)))
+    timed("cross_varlen_f16_d64", lambda: ops.sdpa_fwd_varlen(q, k, v, cq, ck, mq, mk, o, lse),
+          lambda: ops.sdpa_bwd_varlen(q, k, v, o, lse, do, cq, ck, mq, mk, *g, workspace=ws),
+          4 * 8 * 64 * pairs, 2.5 * 4 * 8 * 64 * pairs,
+          f"32 sequences, query lengths sum {sum(lq)} (max {mq}), key lengths sum {sum(lk)} (max {mk}), H=8 d=64 f16")
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -467,6 +523,7 @@ def run_ours(args):
                                 "kind": "oracle", "sample": desc + f", {s:.1f} s"}
     if rank == 0 and world == 1 and not args.no_extras:
         line["per_workload"] = per_workload_results(dev, flush, peaks, peak_kind)
+        line["extras"] = extra_results(dev, flush, peaks)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

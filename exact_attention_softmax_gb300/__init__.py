@@ -19,7 +19,8 @@ import math
 from . import _abi
 from ._abi import SdpaError  # noqa: F401
 
-__all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_bwd_workspace_size",
+__all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_fwd_blocksparse",
+           "sdpa_bwd_blocksparse", "sdpa_bwd_workspace_size",
            "sdpa_device_status",
            "sdpa_debug_set", "sdpa_last_error", "sdpa_version", "SdpaError"]
 
@@ -196,6 +197,76 @@ def sdpa_bwd_varlen(q, k, v, o, lse, dO, cu_seqlens_q, cu_seqlens_k, max_seqlen_
                                    nseq, H, tq, tk, mq, mk, d, float(scale), int(bool(is_causal)),
                                    _vp(cu_seqlens_q), _vp(cu_seqlens_k), code, _vp(workspace), workspace.numel(),
                                    _stream(q.device, stream)))
+    return dq, dk, dv
+
+
+MASK_BLOCK = 128   # rows and keys per tile of a block-sparse mask
+
+
+def _mask_args(block_mask, B, H, Lq, Lk, dev):
+    """(pointer, stride_b, stride_h, stride_row) of a uint8 block mask of shape
+    [nqb, nkb], [H, nqb, nkb] or [B, H, nqb, nkb] (size-1 or expanded dims broadcast)."""
+    import torch
+    nq, nk = -(-Lq // MASK_BLOCK), -(-Lk // MASK_BLOCK)
+    if block_mask.dtype not in (torch.uint8, torch.bool) or block_mask.device != dev:
+        raise TypeError("block_mask must be uint8 or bool on the device of q")
+    m = block_mask
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    if m.dim() != 4 or tuple(m.shape[-2:]) != (nq, nk):
+        raise ValueError(f"block_mask must end in ({nq}, {nk}) for Lq={Lq}, Lk={Lk}")
+    if m.stride(-1) != 1:
+        raise ValueError("block_mask rows must be contiguous")
+    sb = 0 if m.shape[0] == 1 else m.stride(0)
+    sh = 0 if m.shape[1] == 1 else m.stride(1)
+    if m.shape[0] not in (1, B) or m.shape[1] not in (1, H):
+        raise ValueError("block_mask batch / head dims must be 1 or match q")
+    return ctypes.c_void_p(m.data_ptr()), sb, sh, m.stride(2)
+
+
+def sdpa_fwd_blocksparse(q, k, v, block_mask, o=None, lse=None, *, scale=None, is_causal=False, stream=None):
+    """Block-sparse forward: exact attention over the 128x128 score tiles
+    ``block_mask`` keeps (uint8/bool, [..., ceil(Lq/128), ceil(Lk/128)]).
+    Dense [B,H,L,d] layout. Rows with no visible key get O = 0, LSE = -inf."""
+    import torch
+    lib = _abi.load()
+    if q.dim() != 4:
+        raise ValueError("block-sparse q must be [B, H, L, d]")
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensors({"k": k, "v": v, "o": o}, q.device, q.dtype)
+    mp, sb, sh, sq = _mask_args(block_mask, B, H, Lq, Lk, q.device)
+    _abi.check(lib.sdpa_fwd_blocksparse(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), B, H, Lq, Lk, d, float(scale),
+                                        int(bool(is_causal)), mp, sb, sh, sq, _dtype_code(q),
+                                        _stream(q.device, stream)))
+    return o, lse
+
+
+def sdpa_bwd_blocksparse(q, k, v, o, lse, dO, block_mask, dq=None, dk=None, dv=None, *, scale=None,
+                         is_causal=False, workspace=None, stream=None):
+    """Backward of :func:`sdpa_fwd_blocksparse`. Returns ``(dQ, dK, dV)``."""
+    import torch
+    lib = _abi.load()
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_tensors({"k": k, "v": v, "o": o, "dO": dO, "dq": dq, "dk": dk, "dv": dv}, q.device, q.dtype)
+    code = _dtype_code(q)
+    need = lib.sdpa_bwd_workspace_size(B, H, Lq, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    mp, sb, sh, sq = _mask_args(block_mask, B, H, Lq, Lk, q.device)
+    _abi.check(lib.sdpa_bwd_blocksparse(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
+                                        B, H, Lq, Lk, d, float(scale), int(bool(is_causal)), mp, sb, sh, sq, code,
+                                        _vp(workspace), workspace.numel(), _stream(q.device, stream)))
     return dq, dk, dv
 
 

@@ -124,6 +124,29 @@ struct Shape {
   bool packed() const { return cu_q != nullptr; }
 };
 
+// Block-sparse mask (dense layout only): 0/1 per (128-query, 128-key) tile.
+struct BlockMask {
+  const unsigned char* m;
+  long long sb, sh;
+  int sq;
+};
+
+// Longest query axis a block-sparse backward accepts: its CTAs list their
+// active query steps (up to 2048 of 64 or 128 rows) in shared memory.
+constexpr int kMaxSparseLq = 131072;
+
+int check_mask(const Shape& sh, const BlockMask& bm, bool backward) {
+  if (bm.m == nullptr) return fail(SDPA_ERR_ARG, "block mask pointer is NULL");
+  if (sh.packed()) return fail(SDPA_ERR_UNSUPPORTED, "block masks apply to the dense layout only");
+  const int nkb = (sh.total_k + kMaskBlock - 1) / kMaskBlock;
+  if (bm.sb < 0 || bm.sh < 0 || bm.sq < nkb)
+    return fail(SDPA_ERR_ARG, "block mask strides must be non-negative and the row stride at least %d (got %lld, %lld, %d)",
+                nkb, bm.sb, bm.sh, bm.sq);
+  if (backward && sh.total_q > kMaxSparseLq)
+    return fail(SDPA_ERR_UNSUPPORTED, "block-sparse backward supports Lq <= %d (got %d)", kMaxSparseLq, sh.total_q);
+  return SDPA_OK;
+}
+
 int check_shape(const Shape& sh, float scale, int is_causal, int dtype, bool* noop) {
   *noop = false;
   if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return fail(SDPA_ERR_ARG, "unknown dtype %d", dtype);
@@ -154,7 +177,11 @@ int check_tensors(const void* q, const void* k, const void* v, const void* o, co
 }
 
 void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, const void* v, const void* o,
-                  const float* lse, float scale, int is_causal) {
+                  const float* lse, float scale, int is_causal, const BlockMask& bm) {
+  p.bmask = bm.m;
+  p.bm_sb = bm.sb;
+  p.bm_sh = bm.sh;
+  p.bm_sq = bm.sq;
   p.q = q; p.k = k; p.v = v; p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
   p.B = sh.B; p.H = sh.H; p.d = sh.d;
   p.scale = scale; p.causal = is_causal;
@@ -169,14 +196,15 @@ void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, con
 }
 
 int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o, float* lse, float scale,
-            int is_causal, int dtype, void* stream) {
+            int is_causal, int dtype, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0}, bool sparse = false) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
   if (rc != SDPA_OK || noop) return rc;
   if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
+  if (sparse && (rc = check_mask(sh, bm, false)) != SDPA_OK) return rc;
   Problem p{};
-  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal);
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -200,12 +228,14 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
 
 int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const void* o, const float* lse,
             const void* dO, void* dq, void* dk, void* dv, float scale, int is_causal, int dtype, void* workspace,
-            size_t workspace_bytes, void* stream) {
+            size_t workspace_bytes, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0},
+            bool sparse = false) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
   if (rc != SDPA_OK || noop) return rc;
   if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
+  if (sparse && (rc = check_mask(sh, bm, true)) != SDPA_OK) return rc;
   if (!dO || !dq || !dk || !dv) return fail(SDPA_ERR_ARG, "null gradient pointer");
   if (dtype != SDPA_F32 && !(aligned16(dO) && aligned16(dq) && aligned16(dk) && aligned16(dv)))
     return fail(SDPA_ERR_ARG, "fp16/bf16 gradients must be 16-byte aligned");
@@ -220,7 +250,7 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
 
   BwdProblem bp{};
   Problem& p = bp.f;
-  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal);
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
@@ -303,6 +333,24 @@ extern "C" int sdpa_bwd_varlen(const void* q, const void* k, const void* v, cons
   }
   const Shape sh{nseq, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, cu_seqlens_q, cu_seqlens_k};
   return run_bwd(sh, q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" int sdpa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                    int Lq, int Lk, int d, float scale, int is_causal,
+                                    const unsigned char* block_mask, long long mask_stride_b,
+                                    long long mask_stride_h, int mask_stride_row, int dtype, void* stream) {
+  const BlockMask bm{block_mask, mask_stride_b, mask_stride_h, mask_stride_row};
+  return run_fwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, scale, is_causal, dtype, stream, bm, true);
+}
+
+extern "C" int sdpa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+                                    float scale, int is_causal, const unsigned char* block_mask,
+                                    long long mask_stride_b, long long mask_stride_h, int mask_stride_row,
+                                    int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  const BlockMask bm{block_mask, mask_stride_b, mask_stride_h, mask_stride_row};
+  return run_bwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
+                 workspace, workspace_bytes, stream, bm, true);
 }
 
 extern "C" int sdpa_device_status(void* stream, unsigned* bits) {

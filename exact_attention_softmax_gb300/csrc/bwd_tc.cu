@@ -76,7 +76,10 @@ struct BCfg {
   static constexpr int kDqBytes = kDqT ? BQ * D * 4 : 0;     // fp32 dQ staging tile (d = 128 only)
   static constexpr int kOffDQ = kOffDST + kPBytes;
   static constexpr int kOffStat = kOffDQ + kDqBytes;                    // kStages x (lse2[BQ], delta[BQ])
-  static constexpr int kOffBar = kOffStat + kStages * BQ * 8;
+  // block-sparse: the CTA's active query steps (uint16 indices)
+  static constexpr int kMaxSteps = 2048;
+  static constexpr int kOffList = kOffStat + kStages * BQ * 8;
+  static constexpr int kOffBar = kOffList + kMaxSteps * 2;
   static constexpr int kSmem = kOffBar + 256 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   // TMEM columns: S^T, dP^T, dV, dK, two dQ buffers
@@ -99,6 +102,7 @@ struct __align__(8) BBars {
   uint64_t done;
   uint32_t tmem_base;
   uint32_t abort_flag;
+  int nsteps;          // block-sparse: number of active query steps
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -118,7 +122,8 @@ __device__ __forceinline__ void red_add_v4_f32(float* gdst, uint32_t a, uint32_t
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int D, typename T, bool CAUSAL, bool PACKED>
+// SPARSE (dense layout only): block-sparse attention, p.bmask set.
+template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO) {
@@ -166,7 +171,10 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   const long long stat0 = PACKED ? static_cast<long long>(head) * p.Lq + tok0 : static_cast<long long>(unit) * Lq;
   const int nq = (Lq + BQ - 1) / BQ;
   const int i0 = CAUSAL ? min(nq, key0 / BQ) : 0;
-  const int nsteps = nq - i0;
+  // Block-sparse (dense layout): only the query steps whose 128-row mask
+  // block keeps this key block run; one warp lists them before the roles start.
+  constexpr bool sparse = SPARSE;
+  uint16_t* slist = reinterpret_cast<uint16_t*>(smem + C::kOffList);
 
   const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
   const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
@@ -190,6 +198,19 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     bars->abort_flag = 0;
     fence_mbar_init();
   }
+  if (sparse && warp == 1) {
+    const unsigned char* mcol = p.bmask + (unit / p.H) * p.bm_sb + (unit % p.H) * p.bm_sh + kblk;
+    int cnt = 0;
+    for (int base = i0; base < nq; base += 32) {
+      const int qi = base + lane;
+      const bool act = qi < nq && mcol[static_cast<long long>(qi * BQ / kMaskBlock) * p.bm_sq] != 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, act);
+      const int at = cnt + __popc(bal & ((1u << lane) - 1u));
+      if (act && at < C::kMaxSteps) slist[at] = static_cast<uint16_t>(qi);
+      cnt += __popc(bal);
+    }
+    if (lane == 0) bars->nsteps = min(cnt, C::kMaxSteps);
+  }
   if (warp == kMmaSWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -198,6 +219,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   __syncthreads();
   tc_fence_after();
   volatile uint32_t* abort_flag = &bars->abort_flag;
+  const int nsteps = sparse ? bars->nsteps : nq - i0;
+  // query step (in BQ rows) of the CTA's s-th step
+  auto qstep = [&](int st) { return sparse ? (st < nsteps ? static_cast<int>(slist[st]) : nq) : i0 + st; };
   // All 512 columns are allocated, so the allocation starts at column 0.
   constexpr uint32_t tmem = 0;
   if (bars->tmem_base != 0u) {
@@ -228,7 +252,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     constexpr int kPer = BQ / 32;
     float nl[kPer], nd[kPer];
     auto fetch = [&](int step) {
-      const int q0 = (i0 + step) * BQ;
+      const int q0 = qstep(step) * BQ;
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int q = q0 + lane + 32 * u;
@@ -244,7 +268,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       bool ok = !*abort_flag;
       if (ok && lane == 0 && round > 0) ok = mbar_wait(&bars->empty[stage], (round - 1) & 1, abort_flag, p.status);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      const int q0 = (i0 + s) * BQ;
+      const int q0 = qstep(s) * BQ;
       if (lane == 0) {
         mbar_expect_tx_only(&bars->full[stage], 2 * C::kQTile);
         const int c1 = PACKED ? head : q0, c2 = PACKED ? tok0 + q0 : unit;
@@ -373,7 +397,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       const int buf = s & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full[buf], (s >> 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      const int q0 = (i0 + s) * BQ;
+      const int q0 = qstep(s) * BQ;
       const uint32_t tdq = tmem + lane_off + C::kTdQ + buf * C::kDqCols;
       if (C::kDqT) {
         if (r == 0) bulk_wait_read0();          // the previous reduce has read the staging tile
@@ -448,7 +472,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars->s_free);               // the next S^T / dP^T may be written
-      const int q0 = (i0 + s) * BQ + half * NH;
+      const int q0 = qstep(s) * BQ + half * NH;
       const uint32_t sl = smem_u32(stat + stage * 2 * BQ + half * NH);   // lse2 of this half
       const uint32_t sd = sl + BQ * 4;                                     // delta of this half
       const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
@@ -528,9 +552,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   }
 }
 
-template <int D, typename T, bool CAUSAL, bool PACKED>
+template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
 cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
-  auto kern = bwd_tc_kernel<D, T, CAUSAL, PACKED>;
+  auto kern = bwd_tc_kernel<D, T, CAUSAL, PACKED, SPARSE>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -564,9 +588,11 @@ cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
 
 template <int D, typename T>
 cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
+  if (bp.f.bmask != nullptr)
+    return bp.f.causal ? launch_one<D, T, true, false, true>(bp, m, s) : launch_one<D, T, false, false, true>(bp, m, s);
   if (bp.f.cu_seqlens != nullptr)
-    return bp.f.causal ? launch_one<D, T, true, true>(bp, m, s) : launch_one<D, T, false, true>(bp, m, s);
-  return bp.f.causal ? launch_one<D, T, true, false>(bp, m, s) : launch_one<D, T, false, false>(bp, m, s);
+    return bp.f.causal ? launch_one<D, T, true, true, false>(bp, m, s) : launch_one<D, T, false, true, false>(bp, m, s);
+  return bp.f.causal ? launch_one<D, T, true, false, false>(bp, m, s) : launch_one<D, T, false, false, false>(bp, m, s);
 }
 
 }  // namespace

@@ -38,7 +38,15 @@ struct Problem {
   int max_q;
   unsigned* status;  // device status word (bit flags above)
   int debug;
+  // Block-sparse attention (dense layout only): 0/1 per (128-query block,
+  // 128-key block) at bmask[b * bm_sb + h * bm_sh + qb * bm_sq + kb], or NULL.
+  const unsigned char* bmask;
+  long long bm_sb, bm_sh;
+  int bm_sq;
 };
+
+// Rows and keys per block of a block-sparse mask.
+constexpr int kMaskBlock = 128;
 
 struct BwdProblem {
   Problem f;          // q, k, v, o, lse as in the forward

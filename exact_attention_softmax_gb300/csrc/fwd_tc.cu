@@ -151,12 +151,30 @@ __device__ __forceinline__ int tile_blocks(int r, int len_q, int len_k) {
 // One work item: 256 query rows (two 128-row tiles) of one (batch|sequence, head).
 struct Item {
   int unit, h, tok0, tok0k, len_q, len_k, r0, n0, n1, nmax;
+  // block-sparse: the two tiles' mask rows and their key-block limits (causal
+  // and length); n0, n1, nmax then count the loaded key blocks
+  const unsigned char* m0;
+  const unsigned char* m1;
+  int lim0, lim1;
 };
+
+// Block-sparse: a key block is loaded for an item when either tile keeps it
+// (within that tile's limit); each tile then processes every loaded block
+// below its limit, masking the blocks its own row of the mask drops.
+__device__ __forceinline__ bool loaded_block(const Item& it, int j) {
+  return (j < it.lim0 && it.m0[j]) || (j < it.lim1 && it.m1[j]);
+}
+// First loaded key block at or after j.
+__device__ __forceinline__ int next_loaded(const Item& it, int j) {
+  const int lim = max(it.lim0, it.lim1);
+  while (j < lim && !loaded_block(it, j)) ++j;
+  return j;
+}
 
 // Items are numbered unit-major, so the items of one (batch|sequence, head) run
 // side by side and share its K/V through L2; under causal masking the longest
 // rows of each unit come first.
-template <bool CAUSAL, bool PACKED>
+template <bool CAUSAL, bool PACKED, bool SPARSE>
 __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npairs) {
   Item it;
   // Causal items get shorter with their query position, so they are handed
@@ -188,11 +206,35 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
   it.r0 = pair * 2 * BM;
   it.n0 = tile_blocks<CAUSAL>(it.r0, it.len_q, it.len_k);
   it.n1 = tile_blocks<CAUSAL>(it.r0 + BM, it.len_q, it.len_k);
+  it.m0 = it.m1 = nullptr;
+  it.lim0 = it.lim1 = 0;
+  if (SPARSE) {
+    const unsigned char* mu = p.bmask + (it.unit / p.H) * p.bm_sb + (it.unit % p.H) * p.bm_sh;
+    const int qb = it.r0 / kMaskBlock;
+    it.m0 = mu + static_cast<long long>(qb) * p.bm_sq;
+    it.m1 = mu + static_cast<long long>(qb + 1) * p.bm_sq;
+    // a tile that keeps no block of its range is skipped (its rows are
+    // written as empty by the softmax group)
+    bool any0 = false, any1 = false;
+    for (int j = 0; j < it.n0 && !any0; ++j) any0 = it.m0[j] != 0;
+    for (int j = 0; j < it.n1 && !any1; ++j) any1 = it.m1[j] != 0;
+    it.lim0 = any0 ? it.n0 : 0;
+    it.lim1 = any1 ? it.n1 : 0;
+    int c0 = 0, c1 = 0;
+    for (int j = 0; j < max(it.lim0, it.lim1); ++j) {
+      if (!loaded_block(it, j)) continue;
+      c0 += j < it.lim0;
+      c1 += j < it.lim1;
+    }
+    it.n0 = c0;
+    it.n1 = c1;
+  }
   it.nmax = max(it.n0, it.n1);
   return it;
 }
 
-template <int D, typename T, bool CAUSAL, bool PACKED>
+// SPARSE (dense layout only): block-sparse attention, p.bmask set.
+template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -273,7 +315,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         bars->item[q] = idx;
         mbar_arrive(&bars->item_full[q]);
         if (idx < 0) break;
-        const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
+        const Item it = decode_item<CAUSAL, PACKED, SPARSE>(p, idx, npairs);
         idx = static_cast<int>(atomicAdd(sched, 1u)) + static_cast<int>(gridDim.x);
         if (it.nmax == 0) continue;
         auto c1 = [&](int row) { return PACKED ? it.h : row; };
@@ -292,14 +334,17 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             tma_load_3d(smem + C::kOffQ + qb * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[qb],
                         cb * C::kBlk, c1(row), c2(row));
         }
+        constexpr bool sparse = SPARSE;
+        int jk = -1;               // key block of the current loaded block
         for (int j = 0; j < it.nmax && ok; ++j) {
+          jk = sparse ? next_loaded(it, jk + 1) : j;
           for (int kv = 0; kv < 2; ++kv, ++fill) {
             const int slot = fill % C::kSlots;
             const int round = fill / C::kSlots;
             if (round > 0 && !(ok = mbar_wait(&bars->empty[slot], (round - 1) & 1, abort_flag, p.status))) break;
             mbar_expect_tx(&bars->full[slot], C::kTileBytes);
             const CUtensorMap* m = kv ? &tmV : &tmK;
-            const int row = j * BN;
+            const int row = jk * BN;
             for (int cb = 0; cb < C::kNBlk; ++cb)
               tma_load_3d(smem + C::kOffSlots + slot * C::kTileBytes + cb * C::kColBlkBytes, m, &bars->full[slot],
                           cb * C::kBlk, c1(row), c2k(row));
@@ -391,7 +436,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       int idx = -1;
       ok = take(0, idx);
       while (ok && idx >= 0) {
-        const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
+        const Item it = decode_item<CAUSAL, PACKED, SPARSE>(p, idx, npairs);
         int qbuf[2];             // Q buffer of this item per tile
         for (int t = t_lo; t < t_hi; ++t) qbuf[t] = t * C::kQBufs + (qloads[t] - (pre[t] ? 1 : 0)) % C::kQBufs;
         if (it.nmax > 0) {
@@ -427,7 +472,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               // first S_t now, under this block's softmax
               if (next_idx == -2 && !(ok = take(k + 1, next_idx))) break;
               if (next_idx >= 0) {
-                const Item nx = decode_item<CAUSAL, PACKED>(p, next_idx, npairs);
+                const Item nx = decode_item<CAUSAL, PACKED, SPARSE>(p, next_idx, npairs);
                 if (nx.nmax > 0 && (t == 0 ? nx.n0 : nx.n1) > 0) {
                   blocks[t] += nt;            // the phases of S_t continue into the next item
                   ok = first_qk(nx, t, fill + 2 * it.nmax);
@@ -500,7 +545,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     } pend{false, 0.f, 0.f, -1, 0};
     auto epilogue = [&](const Pending& e) {
       tc_fence_after();
-      const float inv = __frcp_rn(e.l);
+      // l = 0 only for a row with no visible key (block-sparse): O = 0, LSE = -inf
+      const float inv = e.l > 0.f ? __frcp_rn(e.l) : 0.f;
       uint32_t ov[D / 2];
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -519,7 +565,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int x = 0; x < D / 8; ++x)
           *reinterpret_cast<uint4*>(orow + 8 * x) = make_uint4(ov[4 * x], ov[4 * x + 1], ov[4 * x + 2], ov[4 * x + 3]);
-        p.lse[e.li] = (e.m + __log2f(e.l)) * kLn2;
+        p.lse[e.li] = e.l > 0.f ? (e.m + __log2f(e.l)) * kLn2 : -INFINITY;
       }
     };
     bool ok = true;
@@ -530,11 +576,24 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[q]);
       if (idx < 0) break;
-      const Item it = decode_item<CAUSAL, PACKED>(p, idx, npairs);
+      const Item it = decode_item<CAUSAL, PACKED, SPARSE>(p, idx, npairs);
       const int nt = t == 0 ? it.n0 : it.n1;
-      if (nt == 0) continue;
       const int rt = it.r0 + t * BM;
       const int row = rt + rl;                // row within the unit
+      if (nt == 0) {
+        // block-sparse: a tile whose mask row keeps nothing has no visible key:
+        // O = 0, LSE = -inf
+        if (SPARSE && row < it.len_q) {
+          T* orow = static_cast<T*>(p.o) + (static_cast<long long>(it.unit) * it.len_q + row) * D;
+#pragma unroll
+          for (int x = 0; x < D / 8; ++x) *reinterpret_cast<uint4*>(orow + 8 * x) = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[static_cast<long long>(it.unit) * it.len_q + row] = -INFINITY;
+        }
+        continue;
+      }
+      constexpr bool sparse = SPARSE;
+      const unsigned char* mine = t == 0 ? it.m0 : it.m1;
+      int jk = -1;                           // key block of the current loaded block
       float m_run = -INFINITY, l = 0.f;      // maximum used in the exponent (base 2), running sum
       for (int j = 0; j < nt; ++j) {
         const int g = blocks + j;
@@ -551,10 +610,13 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           mbar_arrive(&bars->s_free[t]);
         }
         float* x = reinterpret_cast<float*>(sr);
-        const int kbase = j * BN;
-        if ((kbase + BN > it.len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
+        jk = sparse ? next_loaded(it, jk + 1) : j;
+        const int kbase = jk * BN;
+        // block-sparse: a loaded block this tile's mask row drops is masked whole
+        const bool drop = sparse && !mine[jk];
+        if (drop || (kbase + BN > it.len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
           // keys kbase + i with i >= lim are past the end or (causal) after the row
-          const int lim = (CAUSAL ? min(it.len_k, row + 1) : it.len_k) - kbase;
+          const int lim = drop ? 0 : (CAUSAL ? min(it.len_k, row + 1) : it.len_k) - kbase;
 #pragma unroll
           for (int i = 0; i < BN; ++i) x[i] = i < lim ? x[i] : -INFINITY;
         }
@@ -657,9 +719,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   }
 }
 
-template <int D, typename T, bool CAUSAL, bool PACKED>
+template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
 cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
-  auto kern = fwd_tc_kernel<D, T, CAUSAL, PACKED>;
+  auto kern = fwd_tc_kernel<D, T, CAUSAL, PACKED, SPARSE>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -709,8 +771,11 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
 template <int D, typename T>
 cudaError_t launch_d(const Problem& p, const FwdMaps& m, cudaStream_t s) {
   const bool packed = p.cu_seqlens != nullptr;
-  if (p.causal) return packed ? launch_one<D, T, true, true>(p, m, s) : launch_one<D, T, true, false>(p, m, s);
-  return packed ? launch_one<D, T, false, true>(p, m, s) : launch_one<D, T, false, false>(p, m, s);
+  if (p.bmask != nullptr)
+    return p.causal ? launch_one<D, T, true, false, true>(p, m, s) : launch_one<D, T, false, false, true>(p, m, s);
+  if (p.causal)
+    return packed ? launch_one<D, T, true, true, false>(p, m, s) : launch_one<D, T, true, false, false>(p, m, s);
+  return packed ? launch_one<D, T, false, true, false>(p, m, s) : launch_one<D, T, false, false, false>(p, m, s);
 }
 
 }  // namespace

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
     acc[c] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
+  const unsigned char* mrow = p.bmask ? p.bmask + b * p.bm_sb + h * p.bm_sh + (row / kMaskBlock) * p.bm_sq : nullptr;
   int kend = u.len_k;
   if (p.causal) kend = min(kend, min(row0 + kRows, u.len_q));
   for (int kb = 0; kb < kend; kb += kTile) {
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
     for (int jj = 0; jj < kTile; ++jj) {
       const int key = kb + jj;
       if (key >= u.len_k || (p.causal && key > row)) break;
+      if (mrow && !mrow[key / kMaskBlock]) continue;
       float s = 0.f;
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) s = fmaf(qr[c], sk[jj][c], s);
@@ -113,11 +115,12 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
   }
   if (!live) return;
   float* O = static_cast<float*>(p.o) + u.base;
-  const float inv = 1.f / l;
+  // a row with no visible key (block-sparse only) gets O = 0 and LSE = -inf
+  const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int c = 0; c < DMAX; ++c)
     if (c < d) O[row * u.stride + c] = acc[c] * inv;
-  p.lse[u.stat + row] = m + logf(l);
+  p.lse[u.stat + row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 // dQ_i = scale * sum_j P_ij (dO_i.v_j - D_i) k_j
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
   }
   const float lse = live ? p.lse[u.stat + row] : 0.f;
   const float D = live ? bp.delta[u.stat + row] : 0.f;
+  const unsigned char* mrow = p.bmask ? p.bmask + b * p.bm_sb + h * p.bm_sh + (row / kMaskBlock) * p.bm_sq : nullptr;
   int kend = u.len_k;
   if (p.causal) kend = min(kend, min(row0 + kRows, u.len_q));
   for (int kb = 0; kb < kend; kb += kTile) {
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
     for (int jj = 0; jj < kTile; ++jj) {
       const int key = kb + jj;
       if (key >= u.len_k || (p.causal && key > row)) break;
+      if (mrow && !mrow[key / kMaskBlock]) continue;
       float s = 0.f, dp = 0.f;
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) {
@@ -230,6 +235,7 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
       const int qi = qb + ii;
       if (qi >= u.len_q) break;
       if (p.causal && key > qi) continue;
+      if (p.bmask && !p.bmask[b * p.bm_sb + h * p.bm_sh + (qi / kMaskBlock) * p.bm_sq + key / kMaskBlock]) continue;
       float s = 0.f, dp = 0.f;
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) {

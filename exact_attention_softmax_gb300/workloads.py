@@ -168,6 +168,17 @@ def varlen_cross_inputs(lengths_q, lengths_k, H, d, dtype="f16", dist="normal", 
     return out
 
 
+def block_mask(shape, density: float = 0.5, seed: int = 0, empty_rows=()) -> torch.Tensor:
+    """Seeded 0/1 block mask (uint8) of ``shape`` [..., nqb, nkb] for block-sparse
+    attention: each tile kept with probability ``density``; the query blocks
+    listed in ``empty_rows`` keep nothing."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    m = (torch.rand(shape, generator=g) < density).to(torch.uint8)
+    for r in empty_rows:
+        m[..., r, :] = 0
+    return m
+
+
 def workload_inputs(w: Workload, seed: int = 0, with_do=None):
     """Inputs of a named workload (dO drawn when the workload has a backward)."""
     if with_do is None:

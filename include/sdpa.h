@@ -153,6 +153,40 @@ int sdpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Block-sparse attention (the FlashAttention news article, QbitAI repost,
+ * section "FlashAttention", names "block-sparse FlashAttention" without
+ * defining it): exact attention restricted to the score tiles that a 0/1
+ * block mask keeps, with every other score excluded like a causally masked
+ * one; the kernels skip the dropped tiles. Dense layout only.
+ *   block_mask : device uint8 array; tile (qb, kb) of head (b, h), covering
+ *                query rows [128 qb, 128 qb + 128) and keys [128 kb, 128 kb + 128),
+ *                is kept iff block_mask[b * mask_stride_b + h * mask_stride_h
+ *                + qb * mask_stride_row + kb] != 0, for qb < ceil(Lq / 128),
+ *                kb < ceil(Lk / 128). Strides are in elements; 0 broadcasts a
+ *                mask over the batch or the heads; mask_stride_row must be at
+ *                least ceil(Lk / 128).
+ *   A query row with no visible key (all its tiles dropped, or dropped and
+ *   causally masked) gets O = 0 and LSE = -inf, and no gradient.
+ * Other arguments, support and errors as for sdpa_fwd with cu_seqlens = NULL.
+ */
+int sdpa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                         const unsigned char* block_mask, long long mask_stride_b,
+                         long long mask_stride_h, int mask_stride_row, int dtype, void* stream);
+
+/*
+ * Backward of sdpa_fwd_blocksparse (same mask; o and lse as that call wrote
+ * them). Arguments, workspace and support as for sdpa_bwd with
+ * cu_seqlens = NULL; Lq is limited to 131072 (SDPA_ERR_UNSUPPORTED above).
+ */
+int sdpa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv,
+                         int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                         const unsigned char* block_mask, long long mask_stride_b,
+                         long long mask_stride_h, int mask_stride_row, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward pass for callers that cannot allocate device memory: it takes the
  * same arguments as sdpa_bwd except the workspace and cu_seqlens (dense
  * layout only), and uses a scratch array of 16 MiB compiled into the library
