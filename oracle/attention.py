@@ -37,6 +37,11 @@ tiles a 0/1 block mask keeps; every other score is excluded like a causally
 masked one. Reading taken where the article is silent: a query row left with
 no visible key gets O = 0 and LSE = -inf (and no gradient).
 
+Additive mask (the SDPA tutorial's ``attn_mask`` argument, section "Causal
+Self Attention", which passes ``None``): a float matrix M added to the scaled
+scores, ``softmax(scale * Q K^T + M)``; -inf entries exclude a score, and a
+row left with no finite score is empty as above.
+
 Layouts: dense tensors are ``[..., L, d]`` (any leading batch/head dims, the
 tutorial's ``[B, H, L, d]`` and its ``[2, 3, 8]`` example both fit); packed
 variable-length tensors (the tutorial's NestedTensor section) are
@@ -66,11 +71,14 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def _scores(q: np.ndarray, k: np.ndarray, scale: float, is_causal: bool, visible=None) -> np.ndarray:
-    """S = scale * Q K^T with masked entries set to -inf (SDPA tutorial, "Overview";
-    causal mask: "Causal Self Attention"; ``visible``: an extra [Lq, Lk] boolean
-    mask, e.g. a block-sparse pattern)."""
+def _scores(q: np.ndarray, k: np.ndarray, scale: float, is_causal: bool, visible=None, bias=None) -> np.ndarray:
+    """S = scale * Q K^T [+ bias] with masked entries set to -inf (SDPA tutorial,
+    "Overview"; causal mask: "Causal Self Attention"; ``visible``: an extra
+    [Lq, Lk] boolean mask, e.g. a block-sparse pattern; ``bias``: an additive
+    [Lq, Lk] mask)."""
     s = float(scale) * (q @ k.T)
+    if bias is not None:
+        s = s + _f64(bias)
     if visible is not None:
         s = np.where(visible, s, -np.inf)
     if is_causal:
@@ -81,7 +89,7 @@ def _scores(q: np.ndarray, k: np.ndarray, scale: float, is_causal: bool, visible
     return s
 
 
-def attention_probs(q, k, scale: float, is_causal: bool = False, visible=None):
+def attention_probs(q, k, scale: float, is_causal: bool = False, visible=None, bias=None):
     """P = softmax_j(S_ij) and LSE_i for one (batch, head) unit.
 
     ``q``: [Lq, d], ``k``: [Lk, d]. Returns ``(P [Lq, Lk], LSE [Lq])`` in float64.
@@ -95,7 +103,7 @@ def attention_probs(q, k, scale: float, is_causal: bool = False, visible=None):
         return np.zeros((0, lk)), np.zeros((0,))
     if lk == 0:
         raise ValueError("softmax over an empty key set is undefined (Lk = 0 with Lq > 0)")
-    s = _scores(q, k, scale, is_causal, visible)
+    s = _scores(q, k, scale, is_causal, visible, bias)
     m = np.max(s, axis=1, keepdims=True)
     empty = ~np.isfinite(m[:, 0])
     m = np.where(np.isfinite(m), m, 0.0)
@@ -108,20 +116,20 @@ def attention_probs(q, k, scale: float, is_causal: bool = False, visible=None):
     return p, lse
 
 
-def attn_fwd_unit(q, k, v, scale: float, is_causal: bool = False, visible=None):
+def attn_fwd_unit(q, k, v, scale: float, is_causal: bool = False, visible=None, bias=None):
     """O = P V and LSE for one unit. ``v``: [Lk, dv]. Returns (O [Lq, dv], LSE [Lq])."""
     v = _f64(v)
-    p, lse = attention_probs(q, k, scale, is_causal, visible)
+    p, lse = attention_probs(q, k, scale, is_causal, visible, bias)
     return p @ v, lse
 
 
-def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False, visible=None):
+def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False, visible=None, bias=None):
     """Gradients of sum(dO * O) w.r.t. Q, K, V for one unit (chain rule through
     the softmax; the pages only say the backward recomputes attention)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     if q.shape[0] == 0:
         return np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    p, _ = attention_probs(q, k, scale, is_causal, visible)
+    p, _ = attention_probs(q, k, scale, is_causal, visible, bias)
     dv = p.T @ do
     dp = do @ v.T
     dsum = np.sum(p * dp, axis=1, keepdims=True)
@@ -172,8 +180,16 @@ def _packed_spans(cu_seqlens, cu_seqlens_k, total_q: int, total_k: int):
     return [(int(cq[s]), int(cq[s + 1]), int(ck[s]), int(ck[s + 1])) for s in range(cq.size - 1)]
 
 
+def _unit_bias(attn_mask, lead, lq, lk):
+    """Per-unit [Lq, Lk] additive masks for a dense batch with leading dims ``lead``."""
+    if attn_mask is None:
+        return None
+    m = np.broadcast_to(_f64(attn_mask), tuple(lead) + (lq, lk))
+    return m.reshape((-1, lq, lk))
+
+
 def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None,
-                 block_mask=None, block_size: int = 128):
+                 block_mask=None, block_size: int = 128, attn_mask=None):
     """Forward over a whole batch.
 
     Dense: ``q`` [..., Lq, d], ``k``/``v`` [..., Lk, d] -> ``O`` [..., Lq, d],
@@ -184,20 +200,23 @@ def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None
     the keys/values are [total_k, H, d] and sequence s owns key rows
     ``cu_seqlens_k[s] : cu_seqlens_k[s+1]``.
     Dense only: ``block_mask`` [..., ceil(Lq/block_size), ceil(Lk/block_size)]
-    (broadcast over the leading dims) keeps or drops whole score tiles.
+    (broadcast over the leading dims) keeps or drops whole score tiles;
+    ``attn_mask`` [..., Lq, Lk] (broadcast likewise) is added to the scores.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     if cu_seqlens is None:
         lead = q.shape[:-2]
         qu, ku, vu = _units_dense(q), _units_dense(k), _units_dense(v)
         vis = _unit_masks(block_mask, lead, q.shape[-2], k.shape[-2], block_size)
+        bias = _unit_bias(attn_mask, lead, q.shape[-2], k.shape[-2])
         o = np.empty(qu.shape[:2] + (vu.shape[-1],))
         lse = np.empty(qu.shape[:2])
         for u in range(qu.shape[0]):
-            o[u], lse[u] = attn_fwd_unit(qu[u], ku[u], vu[u], scale, is_causal, None if vis is None else vis[u])
+            o[u], lse[u] = attn_fwd_unit(qu[u], ku[u], vu[u], scale, is_causal, None if vis is None else vis[u],
+                                         None if bias is None else bias[u])
         return o.reshape(lead + o.shape[1:]), lse.reshape(lead + lse.shape[1:])
-    if block_mask is not None:
-        raise ValueError("block masks apply to dense batches only")
+    if block_mask is not None or attn_mask is not None:
+        raise ValueError("block masks and additive masks apply to dense batches only")
     total, nh, _ = q.shape
     o = np.zeros((total, nh, v.shape[-1]))
     lse = np.zeros((nh, total))
@@ -210,20 +229,21 @@ def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None
 
 
 def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None,
-                 block_mask=None, block_size: int = 128):
+                 block_mask=None, block_size: int = 128, attn_mask=None):
     """Backward over a whole batch; same layouts as :func:`attn_fwd_ref`.
     Returns ``(dQ, dK, dV)`` in float64."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     if cu_seqlens is None:
         qu, ku, vu, du = (_units_dense(x) for x in (q, k, v, do))
         vis = _unit_masks(block_mask, q.shape[:-2], q.shape[-2], k.shape[-2], block_size)
+        bias = _unit_bias(attn_mask, q.shape[:-2], q.shape[-2], k.shape[-2])
         dq, dk, dv = np.empty_like(qu), np.empty_like(ku), np.empty_like(vu)
         for u in range(qu.shape[0]):
             dq[u], dk[u], dv[u] = attn_bwd_unit(qu[u], ku[u], vu[u], du[u], scale, is_causal,
-                                                None if vis is None else vis[u])
+                                                None if vis is None else vis[u], None if bias is None else bias[u])
         return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
-    if block_mask is not None:
-        raise ValueError("block masks apply to dense batches only")
+    if block_mask is not None or attn_mask is not None:
+        raise ValueError("block masks and additive masks apply to dense batches only")
     total, nh, _ = q.shape
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     for a, b, c, e in _packed_spans(cu_seqlens, cu_seqlens_k, total, k.shape[0]):

@@ -26,7 +26,7 @@ def _visible(i: int, j: int, is_causal: bool, allowed=None) -> bool:
     return (not is_causal) or j <= i
 
 
-def _probs(q, k, scale, is_causal, allowed=None):
+def _probs(q, k, scale, is_causal, allowed=None, bias=None):
     lq, lk, d = len(q), len(k), len(q[0]) if q else 0
     p = [[0.0] * lk for _ in range(lq)]
     lse = [0.0] * lq
@@ -38,7 +38,8 @@ def _probs(q, k, scale, is_causal, allowed=None):
                 dot = 0.0
                 for c in range(d):
                     dot += q[i][c] * k[j][c]
-                w[j] = math.exp(scale * dot)
+                sc = scale * dot + (0.0 if bias is None else bias[i][j])
+                w[j] = 0.0 if sc == -math.inf else math.exp(sc)
                 z += w[j]
         if z == 0.0:
             # no visible key (possible only with `allowed`): the row's
@@ -51,19 +52,20 @@ def _probs(q, k, scale, is_causal, allowed=None):
     return p, lse
 
 
-def fwd_bruteforce(q, k, v, scale, is_causal=False, allowed=None):
+def fwd_bruteforce(q, k, v, scale, is_causal=False, allowed=None, bias=None):
     """q: list[Lq][d], k: list[Lk][d], v: list[Lk][dv] -> (O list[Lq][dv], LSE list[Lq]).
-    ``allowed``: optional set of visible (query, key) index pairs."""
-    p, lse = _probs(q, k, scale, is_causal, allowed)
+    ``allowed``: optional set of visible (query, key) index pairs; ``bias``:
+    optional list[Lq][Lk] added to every score (-inf excludes it)."""
+    p, lse = _probs(q, k, scale, is_causal, allowed, bias)
     dv = len(v[0])
     o = [[sum(p[i][j] * v[j][c] for j in range(len(k))) for c in range(dv)] for i in range(len(q))]
     return o, lse
 
 
-def bwd_bruteforce(q, k, v, do, scale, is_causal=False, allowed=None):
+def bwd_bruteforce(q, k, v, do, scale, is_causal=False, allowed=None, bias=None):
     """Gradients of sum(dO * O) by the explicit softmax Jacobian."""
     lq, lk, d, dv_ = len(q), len(k), len(q[0]), len(v[0])
-    p, _ = _probs(q, k, scale, is_causal, allowed)
+    p, _ = _probs(q, k, scale, is_causal, allowed, bias)
     # dL/dP_ij = sum_c dO_ic V_jc
     gp = [[sum(do[i][c] * v[j][c] for c in range(dv_)) for j in range(lk)] for i in range(lq)]
     # dL/dS_ik = sum_j gp_ij * P_ij * (delta_jk - P_ik)

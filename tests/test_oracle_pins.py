@@ -350,6 +350,80 @@ def test_expand_block_mask_shapes():
         expand_block_mask(bm, 7, 3, 2)
 
 
+# ------------------------------------------------------------ additive mask
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_additive_mask_matches_bruteforce(causal):
+    lq, lk, d = 5, 7, 3
+    q, k, v, do = rnd(lq, d, seed=61), rnd(lk, d, seed=62), rnd(lk, d, seed=63), rnd(lq, d, seed=64)
+    m = rnd(lq, lk, seed=65)
+    m[1, :] = -np.inf              # an empty row
+    m[3, [0, 4]] = -np.inf         # scattered exclusions
+    o, lse = attn_fwd_ref(q[None], k[None], v[None], 0.8, causal, attn_mask=m)
+    grads = attn_bwd_ref(q[None], k[None], v[None], do[None], 0.8, causal, attn_mask=m)
+    ob, lb = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.8, causal, bias=m.tolist())
+    gb = bwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), do.tolist(), 0.8, causal, bias=m.tolist())
+    np.testing.assert_allclose(o[0], np.array(ob), rtol=0, atol=1e-13)
+    fin = np.isfinite(np.array(lb))
+    np.testing.assert_array_equal(np.isneginf(lse[0]), ~fin)
+    np.testing.assert_allclose(lse[0][fin], np.array(lb)[fin], rtol=0, atol=1e-13)
+    for g, r in zip(grads, gb):
+        np.testing.assert_allclose(g[0], np.array(r), rtol=0, atol=1e-13)
+    assert np.all(o[0][1] == 0) and np.isneginf(lse[0][1])
+
+
+def test_additive_mask_special_cases():
+    q, k, v, do = rnd(2, 3, 6, 4, seed=71), rnd(2, 3, 6, 4, seed=72), rnd(2, 3, 6, 4, seed=73), rnd(2, 3, 6, 4, seed=74)
+    plain = attn_fwd_ref(q, k, v, 0.5, False) + attn_bwd_ref(q, k, v, do, 0.5, False)
+    # a zero mask changes nothing
+    zero = attn_fwd_ref(q, k, v, 0.5, False, attn_mask=np.zeros((6, 6))) + attn_bwd_ref(
+        q, k, v, do, 0.5, False, attn_mask=np.zeros((6, 6)))
+    for a, b in zip(plain, zero):
+        np.testing.assert_array_equal(a, b)
+    # -inf above the diagonal is the causal mask
+    tri = np.where(np.arange(6)[None, :] > np.arange(6)[:, None], -np.inf, 0.0)
+    caus = attn_fwd_ref(q, k, v, 0.5, True) + attn_bwd_ref(q, k, v, do, 0.5, True)
+    viam = attn_fwd_ref(q, k, v, 0.5, False, attn_mask=tri) + attn_bwd_ref(q, k, v, do, 0.5, False, attn_mask=tri)
+    for a, b in zip(caus, viam):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+    # a constant shifts LSE by that constant and leaves O and the gradients alone
+    sh = attn_fwd_ref(q, k, v, 0.5, False, attn_mask=np.full((6, 6), 2.5)) + attn_bwd_ref(
+        q, k, v, do, 0.5, False, attn_mask=np.full((6, 6), 2.5))
+    np.testing.assert_allclose(sh[0], plain[0], atol=1e-13)
+    np.testing.assert_allclose(sh[1], plain[1] + 2.5, atol=1e-13)
+    for a, b in zip(plain[2:], sh[2:]):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+    # -inf on the last keys (padding) is attention over the first keys only
+    pad = np.zeros((6, 6))
+    pad[:, 4:] = -np.inf
+    o, lse = attn_fwd_ref(q, k, v, 0.5, False, attn_mask=pad)
+    o2, lse2 = attn_fwd_ref(q, k[..., :4, :], v[..., :4, :], 0.5, False)
+    np.testing.assert_allclose(o, o2, atol=1e-14)
+    np.testing.assert_allclose(lse, lse2, atol=1e-14)
+
+
+def test_additive_mask_backward_finite_differences():
+    lq, lk, d = 4, 5, 3
+    q, k, v, do = rnd(lq, d, seed=81), rnd(lk, d, seed=82), rnd(lk, d, seed=83), rnd(lq, d, seed=84)
+    m = rnd(lq, lk, seed=85)
+    dq, dk, dv = attn_bwd_ref(q, k, v, do, 0.6, False, attn_mask=m)
+
+    def loss(qq, kk, vv):
+        o, _ = attn_fwd_ref(qq, kk, vv, 0.6, False, attn_mask=m)
+        return float(np.sum(do * o))
+    h = 1e-6
+    for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            ap, am = [q, k, v], [q, k, v]
+            ap[which], am[which] = xp, xm
+            num[idx] = (loss(*ap) - loss(*am)) / (2 * h)
+        assert np.max(np.abs(num - g)) <= 1e-7 * max(1.0, np.max(np.abs(g)))
+
+
 def test_rows_helper_matches_full_unit():
     q, k, v = rnd(10, 4, seed=1), rnd(10, 4, seed=2), rnd(10, 4, seed=3)
     rows = np.array([0, 3, 9])
@@ -479,6 +553,15 @@ def test_bruteforce_catches_transposed_block_mask():
     wrong, _ = attn_fwd_ref(q[None], k[None], v[None], 0.5, False, block_mask=bm.T, block_size=2)
     ob, _ = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.5, False, _allowed_pairs(bm, lq, lk, 2))
     assert np.max(np.abs(wrong[0] - np.array(ob))) > 1e-3
+
+
+def test_bruteforce_catches_mask_added_before_the_scale():
+    # an oracle that scaled the mask along with Q K^T
+    q, k, v = rnd(4, 3, seed=91), rnd(5, 3, seed=92), rnd(5, 3, seed=93)
+    m = rnd(4, 5, seed=94)
+    wrong, _ = attn_fwd_unit(q, k, v, 0.3, False, bias=m * 0.3)
+    ob, _ = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.3, False, bias=m.tolist())
+    assert np.max(np.abs(wrong - np.array(ob))) > 1e-3
 
 
 def test_bruteforce_catches_planted_mask_mistake():
