@@ -20,7 +20,7 @@ from . import _abi
 from ._abi import SdpaError  # noqa: F401
 
 __all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_fwd_blocksparse",
-           "sdpa_bwd_blocksparse", "sdpa_bwd_workspace_size",
+           "sdpa_bwd_blocksparse", "sdpa_fwd_masked", "sdpa_bwd_masked", "sdpa_bwd_workspace_size",
            "sdpa_device_status",
            "sdpa_debug_set", "sdpa_last_error", "sdpa_version", "SdpaError"]
 
@@ -267,6 +267,70 @@ def sdpa_bwd_blocksparse(q, k, v, o, lse, dO, block_mask, dq=None, dk=None, dv=N
     _abi.check(lib.sdpa_bwd_blocksparse(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
                                         B, H, Lq, Lk, d, float(scale), int(bool(is_causal)), mp, sb, sh, sq, code,
                                         _vp(workspace), workspace.numel(), _stream(q.device, stream)))
+    return dq, dk, dv
+
+
+def _attn_mask_args(attn_mask, q, Lq, Lk):
+    """(pointer, stride_b, stride_h, stride_row) of an additive mask [..., Lq, Lk]
+    in q's dtype, keys contiguous; size-1 or expanded leading dims broadcast."""
+    m = attn_mask
+    if m.dtype != q.dtype or m.device != q.device:
+        raise TypeError("attn_mask must have the dtype and device of q")
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    if m.dim() != 4 or tuple(m.shape[-2:]) != (Lq, Lk) or m.stride(-1) != 1:
+        raise ValueError(f"attn_mask must be [..., {Lq}, {Lk}] with contiguous keys")
+    B, H = q.shape[0], q.shape[1]
+    if m.shape[0] not in (1, B) or m.shape[1] not in (1, H):
+        raise ValueError("attn_mask batch / head dims must be 1 or match q")
+    sb = 0 if m.shape[0] == 1 else m.stride(0)
+    sh = 0 if m.shape[1] == 1 else m.stride(1)
+    return ctypes.c_void_p(m.data_ptr()), sb, sh, m.stride(2)
+
+
+def sdpa_fwd_masked(q, k, v, attn_mask, o=None, lse=None, *, scale=None, is_causal=False, stream=None):
+    """Forward with an additive mask: ``softmax(scale * Q K^T + attn_mask) V``
+    (dense [B,H,L,d]; -inf entries exclude a score). For fp16/bf16 the mask's
+    row stride must be a multiple of 8 elements and at least Lk rounded up to
+    8 (pad the key axis). Rows with no visible key get O = 0, LSE = -inf."""
+    import torch
+    lib = _abi.load()
+    if q.dim() != 4:
+        raise ValueError("masked q must be [B, H, L, d]")
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensors({"k": k, "v": v, "o": o}, q.device, q.dtype)
+    mp, sb, sh, sq = _attn_mask_args(attn_mask, q, Lq, Lk)
+    _abi.check(lib.sdpa_fwd_masked(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), B, H, Lq, Lk, d, float(scale),
+                                   int(bool(is_causal)), mp, sb, sh, sq, _dtype_code(q), _stream(q.device, stream)))
+    return o, lse
+
+
+def sdpa_bwd_masked(q, k, v, o, lse, dO, attn_mask, dq=None, dk=None, dv=None, *, scale=None, is_causal=False,
+                    workspace=None, stream=None):
+    """Backward of :func:`sdpa_fwd_masked` (gradients for q, k, v)."""
+    import torch
+    lib = _abi.load()
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_tensors({"k": k, "v": v, "o": o, "dO": dO, "dq": dq, "dk": dk, "dv": dv}, q.device, q.dtype)
+    code = _dtype_code(q)
+    need = lib.sdpa_bwd_workspace_size(B, H, Lq, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    mp, sb, sh, sq = _attn_mask_args(attn_mask, q, Lq, Lk)
+    _abi.check(lib.sdpa_bwd_masked(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
+                                   B, H, Lq, Lk, d, float(scale), int(bool(is_causal)), mp, sb, sh, sq, code,
+                                   _vp(workspace), workspace.numel(), _stream(q.device, stream)))
     return dq, dk, dv
 
 

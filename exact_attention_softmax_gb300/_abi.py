@@ -35,6 +35,10 @@ SIGNATURES = {
                                   _vp, ctypes.c_longlong, ctypes.c_longlong, _i, _i, _vp]),
     "sdpa_bwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
                                   _vp, ctypes.c_longlong, ctypes.c_longlong, _i, _i, _vp, _sz, _vp]),
+    "sdpa_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
+                             _vp, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong, _i, _vp]),
+    "sdpa_bwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
+                             _vp, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong, _i, _vp, _sz, _vp]),
     "sdpa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "sdpa_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),

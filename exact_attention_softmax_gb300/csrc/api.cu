@@ -131,6 +131,26 @@ struct BlockMask {
   int sq;
 };
 
+// Additive mask (dense layout only), in the input dtype, keys contiguous.
+struct AddMask {
+  const void* m;
+  long long sb, sh, sq;
+};
+
+int check_addmask(const Shape& sh, const AddMask& am, int dtype) {
+  if (am.m == nullptr) return fail(SDPA_ERR_ARG, "attention mask pointer is NULL");
+  if (am.sb < 0 || am.sh < 0 || am.sq < sh.total_k)
+    return fail(SDPA_ERR_ARG, "attention mask strides must be non-negative and the row stride at least Lk = %d", sh.total_k);
+  if (dtype != SDPA_F32) {
+    // rows are read 8 entries (16 bytes) at a time
+    const long long lk8 = (sh.total_k + 7) / 8 * 8;
+    if (!aligned16(am.m) || am.sq % 8 != 0 || am.sb % 8 != 0 || am.sh % 8 != 0 || am.sq < lk8)
+      return fail(SDPA_ERR_ARG, "fp16/bf16 attention masks need a 16-byte aligned base, strides that are multiples of 8 "
+                                "elements and a row stride of at least %lld", lk8);
+  }
+  return SDPA_OK;
+}
+
 // Longest query axis a block-sparse backward accepts: its CTAs list their
 // active query steps (up to 2048 of 64 or 128 rows) in shared memory.
 constexpr int kMaxSparseLq = 131072;
@@ -177,7 +197,12 @@ int check_tensors(const void* q, const void* k, const void* v, const void* o, co
 }
 
 void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, const void* v, const void* o,
-                  const float* lse, float scale, int is_causal, const BlockMask& bm) {
+                  const float* lse, float scale, int is_causal, const BlockMask& bm,
+                  const AddMask& am = AddMask{nullptr, 0, 0, 0}) {
+  p.amask = am.m;
+  p.am_sb = am.sb;
+  p.am_sh = am.sh;
+  p.am_sq = am.sq;
   p.bmask = bm.m;
   p.bm_sb = bm.sb;
   p.bm_sh = bm.sh;
@@ -196,15 +221,17 @@ void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, con
 }
 
 int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o, float* lse, float scale,
-            int is_causal, int dtype, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0}, bool sparse = false) {
+            int is_causal, int dtype, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0}, bool sparse = false,
+            const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
   if (rc != SDPA_OK || noop) return rc;
   if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
   if (sparse && (rc = check_mask(sh, bm, false)) != SDPA_OK) return rc;
+  if (masked && (rc = check_addmask(sh, am, dtype)) != SDPA_OK) return rc;
   Problem p{};
-  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm);
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -229,13 +256,14 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
 int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const void* o, const float* lse,
             const void* dO, void* dq, void* dk, void* dv, float scale, int is_causal, int dtype, void* workspace,
             size_t workspace_bytes, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0},
-            bool sparse = false) {
+            bool sparse = false, const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
   if (rc != SDPA_OK || noop) return rc;
   if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
   if (sparse && (rc = check_mask(sh, bm, true)) != SDPA_OK) return rc;
+  if (masked && (rc = check_addmask(sh, am, dtype)) != SDPA_OK) return rc;
   if (!dO || !dq || !dk || !dv) return fail(SDPA_ERR_ARG, "null gradient pointer");
   if (dtype != SDPA_F32 && !(aligned16(dO) && aligned16(dq) && aligned16(dk) && aligned16(dv)))
     return fail(SDPA_ERR_ARG, "fp16/bf16 gradients must be 16-byte aligned");
@@ -250,7 +278,7 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
 
   BwdProblem bp{};
   Problem& p = bp.f;
-  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm);
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
@@ -351,6 +379,25 @@ extern "C" int sdpa_bwd_blocksparse(const void* q, const void* k, const void* v,
   const BlockMask bm{block_mask, mask_stride_b, mask_stride_h, mask_stride_row};
   return run_bwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
                  workspace, workspace_bytes, stream, bm, true);
+}
+
+extern "C" int sdpa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
+                               int Lk, int d, float scale, int is_causal, const void* attn_mask,
+                               long long mask_stride_b, long long mask_stride_h, long long mask_stride_row, int dtype,
+                               void* stream) {
+  const AddMask am{attn_mask, mask_stride_b, mask_stride_h, mask_stride_row};
+  return run_fwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, scale, is_causal, dtype, stream,
+                 BlockMask{nullptr, 0, 0, 0}, false, am, true);
+}
+
+extern "C" int sdpa_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dO, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+                               float scale, int is_causal, const void* attn_mask, long long mask_stride_b,
+                               long long mask_stride_h, long long mask_stride_row, int dtype, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  const AddMask am{attn_mask, mask_stride_b, mask_stride_h, mask_stride_row};
+  return run_bwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
+                 workspace, workspace_bytes, stream, BlockMask{nullptr, 0, 0, 0}, false, am, true);
 }
 
 extern "C" int sdpa_device_status(void* stream, unsigned* bits) {

@@ -122,12 +122,13 @@ __device__ __forceinline__ void red_add_v4_f32(float* gdst, uint32_t a, uint32_t
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// SPARSE (dense layout only): block-sparse attention, p.bmask set.
-template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
+// EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask (p.amask).
+template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO) {
   using C = BCfg<D>;
+  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2;
   constexpr int BQ = C::BQ;
   const Problem& p = bp.f;
   extern __shared__ uint8_t smem_raw[];
@@ -257,7 +258,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       for (int u = 0; u < kPer; ++u) {
         const int q = q0 + lane + 32 * u;
         const bool in = step < nsteps && q < Lq;
-        nl[u] = in ? lse[q] * kLog2e : INFINITY;
+        // a row with no visible key (LSE = -inf) gets +inf, so all its P are 0
+        const float lq = in ? lse[q] : INFINITY;
+        nl[u] = lq == -INFINITY ? INFINITY : lq * kLog2e;
         nd[u] = in ? delta[q] : 0.f;
       }
     };
@@ -459,6 +462,22 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
       const int stage = s & 1;
+      // additive mask: M[q][key] for this group's query columns, loaded before
+      // the waits so the loads overlap them (a warp reads 32 adjacent keys)
+      uint32_t amk[BIAS ? NH / 2 : 1];
+      if (BIAS) {
+        const int qa = qstep(s) * BQ + half * NH;
+        const T* mcol = static_cast<const T*>(p.amask) + (unit / p.H) * p.am_sb + (unit % p.H) * p.am_sh + key;
+#pragma unroll
+        for (int cpair = 0; cpair < NH / 2; ++cpair) {
+          unsigned short lo = 0, hi = 0;
+          const int qa0 = qa + 2 * cpair;
+          if (key < Lk && qa0 < Lq) lo = *reinterpret_cast<const unsigned short*>(mcol + static_cast<long long>(qa0) * p.am_sq);
+          if (key < Lk && qa0 + 1 < Lq)
+            hi = *reinterpret_cast<const unsigned short*>(mcol + static_cast<long long>(qa0 + 1) * p.am_sq);
+          amk[cpair] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, abort_flag, p.status) &&
                                        mbar_wait(&bars->full[stage], (s >> 1) & 1, abort_flag, p.status));
       if (!ok) break;
@@ -488,7 +507,12 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const int col = 4 * g + h;
-          float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, -l4[h]));
+          float bias2 = 0.f;        // additive mask in base 2
+          if (BIAS) {
+            const float2 mf = Pack2<T>::unpack(amk[col / 2]);
+            bias2 = ((col & 1) ? mf.y : mf.x) * kLog2e;
+          }
+          float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, bias2 - l4[h]));
           if (need_mask && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
           pr[h] = pv;
           ds[h] = pv * (__uint_as_float(dv[col]) - d4[h]);
@@ -552,9 +576,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   }
 }
 
-template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
+template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
-  auto kern = bwd_tc_kernel<D, T, CAUSAL, PACKED, SPARSE>;
+  auto kern = bwd_tc_kernel<D, T, CAUSAL, PACKED, EXT>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -589,10 +613,12 @@ cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
 template <int D, typename T>
 cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
   if (bp.f.bmask != nullptr)
-    return bp.f.causal ? launch_one<D, T, true, false, true>(bp, m, s) : launch_one<D, T, false, false, true>(bp, m, s);
+    return bp.f.causal ? launch_one<D, T, true, false, 1>(bp, m, s) : launch_one<D, T, false, false, 1>(bp, m, s);
+  if (bp.f.amask != nullptr)
+    return bp.f.causal ? launch_one<D, T, true, false, 2>(bp, m, s) : launch_one<D, T, false, false, 2>(bp, m, s);
   if (bp.f.cu_seqlens != nullptr)
-    return bp.f.causal ? launch_one<D, T, true, true, false>(bp, m, s) : launch_one<D, T, false, true, false>(bp, m, s);
-  return bp.f.causal ? launch_one<D, T, true, false, false>(bp, m, s) : launch_one<D, T, false, false, false>(bp, m, s);
+    return bp.f.causal ? launch_one<D, T, true, true, 0>(bp, m, s) : launch_one<D, T, false, true, 0>(bp, m, s);
+  return bp.f.causal ? launch_one<D, T, true, false, 0>(bp, m, s) : launch_one<D, T, false, false, 0>(bp, m, s);
 }
 
 }  // namespace

@@ -43,6 +43,10 @@ struct Problem {
   const unsigned char* bmask;
   long long bm_sb, bm_sh;
   int bm_sq;
+  // Additive mask (dense layout only): element (b, h, i, j) at
+  // amask[b * am_sb + h * am_sh + i * am_sq + j], in the input dtype, or NULL.
+  const void* amask;
+  long long am_sb, am_sh, am_sq;
 };
 
 // Rows and keys per block of a block-sparse mask.

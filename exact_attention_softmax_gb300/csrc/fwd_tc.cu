@@ -233,13 +233,14 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
   return it;
 }
 
-// SPARSE (dense layout only): block-sparse attention, p.bmask set.
-template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
+// EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask (p.amask).
+template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               unsigned* sched) {
   using C = Cfg<D>;
+  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
@@ -597,6 +598,20 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       float m_run = -INFINITY, l = 0.f;      // maximum used in the exponent (base 2), running sum
       for (int j = 0; j < nt; ++j) {
         const int g = blocks + j;
+        jk = sparse ? next_loaded(it, jk + 1) : j;
+        const int kbase = jk * BN;
+        // additive mask: this row's BN entries, loaded before the S wait so the
+        // load overlaps it (rows of 8 entries; the row stride is padded to 8, so
+        // a chunk that starts before len_k stays inside the row)
+        uint4 am[BIAS ? BN / 8 : 1];
+        if (BIAS) {
+          const T* mrow = static_cast<const T*>(p.amask) + (it.unit / p.H) * p.am_sb + (it.unit % p.H) * p.am_sh +
+                          static_cast<long long>(row) * p.am_sq + kbase;
+#pragma unroll
+          for (int u = 0; u < BN / 8; ++u)
+            am[u] = (row < it.len_q && kbase + 8 * u < it.len_k) ? *reinterpret_cast<const uint4*>(mrow + 8 * u)
+                                                                 : make_uint4(0u, 0u, 0u, 0u);
+        }
         if (!(ok = wait_all(&bars->s_full[t], g & 1))) break;
         tc_fence_after();
         uint32_t sr[BN];
@@ -610,8 +625,19 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           mbar_arrive(&bars->s_free[t]);
         }
         float* x = reinterpret_cast<float*>(sr);
-        jk = sparse ? next_loaded(it, jk + 1) : j;
-        const int kbase = jk * BN;
+        if (BIAS) {
+          // x = S * scale * log2(e) + M * log2(e): the exponent in base 2
+#pragma unroll
+          for (int u = 0; u < BN / 8; ++u) {
+            const uint32_t w[4] = {am[u].x, am[u].y, am[u].z, am[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 mf = Pack2<T>::unpack(w[e]);
+              x[8 * u + 2 * e] = fmaf(x[8 * u + 2 * e], c, mf.x * kLog2e);
+              x[8 * u + 2 * e + 1] = fmaf(x[8 * u + 2 * e + 1], c, mf.y * kLog2e);
+            }
+          }
+        }
         // block-sparse: a loaded block this tile's mask row drops is masked whole
         const bool drop = sparse && !mine[jk];
         if (drop || (kbase + BN > it.len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
@@ -632,7 +658,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         }
         mx0 = max3f(mx0, x[BN - 4], x[BN - 3]);
         mx1 = max3f(mx1, x[BN - 2], x[BN - 1]);
-        const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * c;
+        const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * (BIAS ? 1.f : c);
         const bool grow = mx > m_run + kRescaleThreshold;
         const float m_new = grow ? mx : m_run;
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
@@ -649,7 +675,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             float e[8];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], c, -m_use);
+              fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], BIAS ? 1.f : c, -m_use);
               e[2 * u] = ex2_approx(e[2 * u]);
               e[2 * u + 1] = ex2_approx(e[2 * u + 1]);
             }
@@ -719,9 +745,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   }
 }
 
-template <int D, typename T, bool CAUSAL, bool PACKED, bool SPARSE>
+template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
-  auto kern = fwd_tc_kernel<D, T, CAUSAL, PACKED, SPARSE>;
+  auto kern = fwd_tc_kernel<D, T, CAUSAL, PACKED, EXT>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -772,10 +798,12 @@ template <int D, typename T>
 cudaError_t launch_d(const Problem& p, const FwdMaps& m, cudaStream_t s) {
   const bool packed = p.cu_seqlens != nullptr;
   if (p.bmask != nullptr)
-    return p.causal ? launch_one<D, T, true, false, true>(p, m, s) : launch_one<D, T, false, false, true>(p, m, s);
+    return p.causal ? launch_one<D, T, true, false, 1>(p, m, s) : launch_one<D, T, false, false, 1>(p, m, s);
+  if (p.amask != nullptr)
+    return p.causal ? launch_one<D, T, true, false, 2>(p, m, s) : launch_one<D, T, false, false, 2>(p, m, s);
   if (p.causal)
-    return packed ? launch_one<D, T, true, true, false>(p, m, s) : launch_one<D, T, true, false, false>(p, m, s);
-  return packed ? launch_one<D, T, false, true, false>(p, m, s) : launch_one<D, T, false, false, false>(p, m, s);
+    return packed ? launch_one<D, T, true, true, 0>(p, m, s) : launch_one<D, T, true, false, 0>(p, m, s);
+  return packed ? launch_one<D, T, false, true, 0>(p, m, s) : launch_one<D, T, false, false, 0>(p, m, s);
 }
 
 }  // namespace

@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
   }
   float m = -INFINITY, l = 0.f;
   const unsigned char* mrow = p.bmask ? p.bmask + b * p.bm_sb + h * p.bm_sh + (row / kMaskBlock) * p.bm_sq : nullptr;
+  const float* arow = p.amask ? static_cast<const float*>(p.amask) + b * p.am_sb + h * p.am_sh + row * p.am_sq : nullptr;
   int kend = u.len_k;
   if (p.causal) kend = min(kend, min(row0 + kRows, u.len_q));
   for (int kb = 0; kb < kend; kb += kTile) {
@@ -96,10 +97,12 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
       const int key = kb + jj;
       if (key >= u.len_k || (p.causal && key > row)) break;
       if (mrow && !mrow[key / kMaskBlock]) continue;
+      const float bias = arow ? arow[key] : 0.f;
+      if (bias == -INFINITY) continue;
       float s = 0.f;
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) s = fmaf(qr[c], sk[jj][c], s);
-      s *= p.scale;
+      s = s * p.scale + bias;
       if (s > m) {
         const float corr = expf(m - s);
         l *= corr;
@@ -152,6 +155,7 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
   const float lse = live ? p.lse[u.stat + row] : 0.f;
   const float D = live ? bp.delta[u.stat + row] : 0.f;
   const unsigned char* mrow = p.bmask ? p.bmask + b * p.bm_sb + h * p.bm_sh + (row / kMaskBlock) * p.bm_sq : nullptr;
+  const float* arow = p.amask ? static_cast<const float*>(p.amask) + b * p.am_sb + h * p.am_sh + row * p.am_sq : nullptr;
   int kend = u.len_k;
   if (p.causal) kend = min(kend, min(row0 + kRows, u.len_q));
   for (int kb = 0; kb < kend; kb += kTile) {
@@ -168,13 +172,15 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
       const int key = kb + jj;
       if (key >= u.len_k || (p.causal && key > row)) break;
       if (mrow && !mrow[key / kMaskBlock]) continue;
+      const float bias = arow ? arow[key] : 0.f;
+      if (bias == -INFINITY) continue;
       float s = 0.f, dp = 0.f;
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) {
         s = fmaf(qr[c], sk[jj][c], s);
         dp = fmaf(dor[c], sv[jj][c], dp);
       }
-      const float pr = expf(s * p.scale - lse);
+      const float pr = expf(s * p.scale + bias - lse);
       const float ds = pr * (dp - D);
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) dq[c] = fmaf(ds, sk[jj][c], dq[c]);
@@ -236,13 +242,16 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
       if (qi >= u.len_q) break;
       if (p.causal && key > qi) continue;
       if (p.bmask && !p.bmask[b * p.bm_sb + h * p.bm_sh + (qi / kMaskBlock) * p.bm_sq + key / kMaskBlock]) continue;
+      const float bias =
+          p.amask ? static_cast<const float*>(p.amask)[b * p.am_sb + h * p.am_sh + qi * p.am_sq + key] : 0.f;
+      if (bias == -INFINITY) continue;
       float s = 0.f, dp = 0.f;
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) {
         s = fmaf(sq[ii][c], kr[c], s);
         dp = fmaf(sdo[ii][c], vr[c], dp);
       }
-      const float pr = expf(s * p.scale - slse[ii]);
+      const float pr = expf(s * p.scale + bias - slse[ii]);
       const float ds = pr * (dp - sD[ii]);
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) {

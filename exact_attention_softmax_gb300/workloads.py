@@ -179,6 +179,23 @@ def block_mask(shape, density: float = 0.5, seed: int = 0, empty_rows=()) -> tor
     return m
 
 
+def attn_mask(shape, dtype="f16", seed: int = 0, neg_inf: float = 0.1, empty_rows=(), pad_to: int = 8):
+    """Seeded additive mask [..., Lq, Lk]: N(0,1) entries, a fraction
+    ``neg_inf`` of them -inf, the rows in ``empty_rows`` entirely -inf. Returned
+    with the key axis padded to a multiple of ``pad_to`` ([..., Lq, Lk_padded];
+    take ``[..., :Lk]`` after moving it to the device to keep the padded row
+    stride the fp16/bf16 kernels read 8 entries at a time from)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    *lead, lq, lk = shape
+    lkp = (lk + pad_to - 1) // pad_to * pad_to
+    full = torch.randn(tuple(lead) + (lq, lkp), generator=g)
+    drop = torch.rand(tuple(lead) + (lq, lkp), generator=g) < neg_inf
+    full[drop] = float("-inf")
+    for r in empty_rows:
+        full[..., r, :] = float("-inf")
+    return full.to(_DTYPES[dtype])
+
+
 def workload_inputs(w: Workload, seed: int = 0, with_do=None):
     """Inputs of a named workload (dO drawn when the workload has a backward)."""
     if with_do is None:

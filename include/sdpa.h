@@ -187,6 +187,40 @@ int sdpa_bwd_blocksparse(const void* q, const void* k, const void* v, const void
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Attention with an additive mask (the SDPA tutorial's attn_mask argument,
+ * section "Causal Self Attention"): O = softmax(scale * Q K^T + M) V, with
+ * the causal mask on top when is_causal = 1. Dense layout only.
+ *   attn_mask : device array in the input dtype; M(b, h, i, j) =
+ *               attn_mask[b * mask_stride_b + h * mask_stride_h
+ *               + i * mask_stride_row + j] for i < Lq, j < Lk (keys
+ *               contiguous). Strides are in elements; 0 broadcasts over the
+ *               batch or the heads. Entries are finite or -inf (-inf excludes
+ *               the score). fp16/bf16: the base must be 16-byte aligned, the
+ *               strides multiples of 8 and mask_stride_row at least Lk rounded
+ *               up to 8 (rows are read 8 entries at a time); fp32: row stride
+ *               at least Lk.
+ *   A query row with no visible key gets O = 0 and LSE = -inf, and no gradient.
+ * LSE is the log-sum-exp of the masked scores. Other arguments, support and
+ * errors as for sdpa_fwd with cu_seqlens = NULL.
+ */
+int sdpa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                    const void* attn_mask, long long mask_stride_b, long long mask_stride_h,
+                    long long mask_stride_row, int dtype, void* stream);
+
+/*
+ * Backward of sdpa_fwd_masked (same mask; o and lse as that call wrote them).
+ * Gradients for q, k and v only (none for the mask). Arguments, workspace and
+ * support as for sdpa_bwd with cu_seqlens = NULL.
+ */
+int sdpa_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv,
+                    int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                    const void* attn_mask, long long mask_stride_b, long long mask_stride_h,
+                    long long mask_stride_row, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward pass for callers that cannot allocate device memory: it takes the
  * same arguments as sdpa_bwd except the workspace and cu_seqlens (dense
  * layout only), and uses a scratch array of 16 MiB compiled into the library

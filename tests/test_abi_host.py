@@ -121,6 +121,26 @@ def test_varlen_cross_argument_errors(lib):
     assert lib.sdpa_bwd_varlen(*(args[:15] + [32] + args[16:]), FAKE, need, None) == _abi.SDPA_ERR_UNSUPPORTED
 
 
+def test_masked_and_blocksparse_argument_errors(lib):
+    def fwdm(ptr=FAKE, mask=FAKE, sb=0, sh=0, sq=64, dtype=1, lk=60):
+        return lib.sdpa_fwd_masked(ptr, ptr, ptr, ptr, ptr, 1, 1, 4, lk, 64, 0.125, 0, mask, sb, sh, sq, dtype, None)
+    assert fwdm(mask=None) == _abi.SDPA_ERR_ARG
+    assert fwdm(sq=59) == _abi.SDPA_ERR_ARG                # row stride below Lk
+    assert fwdm(sq=60) == _abi.SDPA_ERR_ARG                # fp16: not a multiple of 8
+    assert fwdm(sq=64, sb=4) == _abi.SDPA_ERR_ARG          # fp16: batch stride not a multiple of 8
+    assert fwdm(mask=ctypes.c_void_p(0x100008)) == _abi.SDPA_ERR_ARG   # fp16: unaligned base
+    assert fwdm(sh=-8) == _abi.SDPA_ERR_ARG
+    assert b"mask" in lib.sdpa_last_error()
+
+    def fwdb(mask=FAKE, sq=2, lk=256):
+        return lib.sdpa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, lk, 64, 0.125, 0, mask, 0, 0, sq, 1, None)
+    assert fwdb(mask=None) == _abi.SDPA_ERR_ARG
+    assert fwdb(sq=1) == _abi.SDPA_ERR_ARG                 # fewer than ceil(Lk / 128) key blocks per row
+    args = [FAKE] * 9 + [1, 1, 200000, 256, 64, 0.125, 0, FAKE, 0, 0, 2, 1]
+    need = lib.sdpa_bwd_workspace_size(1, 1, 200000, 64, 1)
+    assert lib.sdpa_bwd_blocksparse(*args, FAKE, need, None) == _abi.SDPA_ERR_UNSUPPORTED   # Lq above 131072
+
+
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_abi, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
