@@ -13,3 +13,4 @@ from .attention import (  # noqa: F401
     expand_block_mask,
 )
 from .bruteforce import bwd_bruteforce, fwd_bruteforce  # noqa: F401
+from .philox import dropout_keep, dropout_threshold, philox4x32_10  # noqa: F401

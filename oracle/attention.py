@@ -42,6 +42,11 @@ Self Attention", which passes ``None``): a float matrix M added to the scaled
 scores, ``softmax(scale * Q K^T + M)``; -inf entries exclude a score, and a
 row left with no finite score is empty as above.
 
+Dropout (the tutorial's ``dropout_p`` argument of the same call): the
+probabilities, not the normaliser, are dropped; O = (P * Z) V with Z = 0 for a
+dropped score and 1/(1-p) for a kept one, and LSE that of the full softmax.
+The keep pattern comes from Philox4x32-10 (``oracle/philox.py``).
+
 Layouts: dense tensors are ``[..., L, d]`` (any leading batch/head dims, the
 tutorial's ``[B, H, L, d]`` and its ``[2, 3, 8]`` example both fit); packed
 variable-length tensors (the tutorial's NestedTensor section) are
@@ -116,22 +121,26 @@ def attention_probs(q, k, scale: float, is_causal: bool = False, visible=None, b
     return p, lse
 
 
-def attn_fwd_unit(q, k, v, scale: float, is_causal: bool = False, visible=None, bias=None):
-    """O = P V and LSE for one unit. ``v``: [Lk, dv]. Returns (O [Lq, dv], LSE [Lq])."""
+def attn_fwd_unit(q, k, v, scale: float, is_causal: bool = False, visible=None, bias=None, drop=None):
+    """O = P V and LSE for one unit. ``v``: [Lk, dv]. Returns (O [Lq, dv], LSE [Lq]).
+    ``drop`` ([Lq, Lk], optional): dropout factors Z multiplying P in O only."""
     v = _f64(v)
     p, lse = attention_probs(q, k, scale, is_causal, visible, bias)
+    if drop is not None:
+        p = p * drop
     return p @ v, lse
 
 
-def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False, visible=None, bias=None):
+def attn_bwd_unit(q, k, v, do, scale: float, is_causal: bool = False, visible=None, bias=None, drop=None):
     """Gradients of sum(dO * O) w.r.t. Q, K, V for one unit (chain rule through
     the softmax; the pages only say the backward recomputes attention)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     if q.shape[0] == 0:
         return np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     p, _ = attention_probs(q, k, scale, is_causal, visible, bias)
-    dv = p.T @ do
-    dp = do @ v.T
+    z = np.ones_like(p) if drop is None else _f64(drop)
+    dv = (p * z).T @ do
+    dp = (do @ v.T) * z                      # gradient with respect to P
     dsum = np.sum(p * dp, axis=1, keepdims=True)
     ds = p * (dp - dsum)
     dq = float(scale) * (ds @ k)
@@ -188,8 +197,18 @@ def _unit_bias(attn_mask, lead, lq, lk):
     return m.reshape((-1, lq, lk))
 
 
+def _unit_drops(dropout_p, seed, nunits, lq, lk):
+    """Dropout factors Z per unit (None when p = 0)."""
+    if not dropout_p:
+        return None
+    from .philox import dropout_keep, dropout_threshold
+    t = dropout_threshold(dropout_p)
+    kept = 256.0 / (256.0 - t)
+    return [dropout_keep(seed, u, lq, lk, dropout_p) * kept for u in range(nunits)]
+
+
 def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None,
-                 block_mask=None, block_size: int = 128, attn_mask=None):
+                 block_mask=None, block_size: int = 128, attn_mask=None, dropout_p: float = 0.0, dropout_seed: int = 0):
     """Forward over a whole batch.
 
     Dense: ``q`` [..., Lq, d], ``k``/``v`` [..., Lk, d] -> ``O`` [..., Lq, d],
@@ -209,13 +228,14 @@ def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None
         qu, ku, vu = _units_dense(q), _units_dense(k), _units_dense(v)
         vis = _unit_masks(block_mask, lead, q.shape[-2], k.shape[-2], block_size)
         bias = _unit_bias(attn_mask, lead, q.shape[-2], k.shape[-2])
+        drops = _unit_drops(dropout_p, dropout_seed, qu.shape[0], q.shape[-2], k.shape[-2])
         o = np.empty(qu.shape[:2] + (vu.shape[-1],))
         lse = np.empty(qu.shape[:2])
         for u in range(qu.shape[0]):
             o[u], lse[u] = attn_fwd_unit(qu[u], ku[u], vu[u], scale, is_causal, None if vis is None else vis[u],
-                                         None if bias is None else bias[u])
+                                         None if bias is None else bias[u], None if drops is None else drops[u])
         return o.reshape(lead + o.shape[1:]), lse.reshape(lead + lse.shape[1:])
-    if block_mask is not None or attn_mask is not None:
+    if block_mask is not None or attn_mask is not None or dropout_p:
         raise ValueError("block masks and additive masks apply to dense batches only")
     total, nh, _ = q.shape
     o = np.zeros((total, nh, v.shape[-1]))
@@ -229,7 +249,7 @@ def attn_fwd_ref(q, k, v, scale: float, is_causal: bool = False, cu_seqlens=None
 
 
 def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=None, cu_seqlens_k=None,
-                 block_mask=None, block_size: int = 128, attn_mask=None):
+                 block_mask=None, block_size: int = 128, attn_mask=None, dropout_p: float = 0.0, dropout_seed: int = 0):
     """Backward over a whole batch; same layouts as :func:`attn_fwd_ref`.
     Returns ``(dQ, dK, dV)`` in float64."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -237,12 +257,14 @@ def attn_bwd_ref(q, k, v, do, scale: float, is_causal: bool = False, cu_seqlens=
         qu, ku, vu, du = (_units_dense(x) for x in (q, k, v, do))
         vis = _unit_masks(block_mask, q.shape[:-2], q.shape[-2], k.shape[-2], block_size)
         bias = _unit_bias(attn_mask, q.shape[:-2], q.shape[-2], k.shape[-2])
+        drops = _unit_drops(dropout_p, dropout_seed, qu.shape[0], q.shape[-2], k.shape[-2])
         dq, dk, dv = np.empty_like(qu), np.empty_like(ku), np.empty_like(vu)
         for u in range(qu.shape[0]):
             dq[u], dk[u], dv[u] = attn_bwd_unit(qu[u], ku[u], vu[u], du[u], scale, is_causal,
-                                                None if vis is None else vis[u], None if bias is None else bias[u])
+                                                None if vis is None else vis[u], None if bias is None else bias[u],
+                                                None if drops is None else drops[u])
         return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
-    if block_mask is not None or attn_mask is not None:
+    if block_mask is not None or attn_mask is not None or dropout_p:
         raise ValueError("block masks and additive masks apply to dense batches only")
     total, nh, _ = q.shape
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)

@@ -52,22 +52,25 @@ def _probs(q, k, scale, is_causal, allowed=None, bias=None):
     return p, lse
 
 
-def fwd_bruteforce(q, k, v, scale, is_causal=False, allowed=None, bias=None):
+def fwd_bruteforce(q, k, v, scale, is_causal=False, allowed=None, bias=None, drop=None):
     """q: list[Lq][d], k: list[Lk][d], v: list[Lk][dv] -> (O list[Lq][dv], LSE list[Lq]).
     ``allowed``: optional set of visible (query, key) index pairs; ``bias``:
     optional list[Lq][Lk] added to every score (-inf excludes it)."""
     p, lse = _probs(q, k, scale, is_causal, allowed, bias)
     dv = len(v[0])
-    o = [[sum(p[i][j] * v[j][c] for j in range(len(k))) for c in range(dv)] for i in range(len(q))]
+    z = (lambda i, j: 1.0) if drop is None else (lambda i, j: drop[i][j])
+    o = [[sum(p[i][j] * z(i, j) * v[j][c] for j in range(len(k))) for c in range(dv)] for i in range(len(q))]
     return o, lse
 
 
-def bwd_bruteforce(q, k, v, do, scale, is_causal=False, allowed=None, bias=None):
-    """Gradients of sum(dO * O) by the explicit softmax Jacobian."""
+def bwd_bruteforce(q, k, v, do, scale, is_causal=False, allowed=None, bias=None, drop=None):
+    """Gradients of sum(dO * O) by the explicit softmax Jacobian; ``drop``: the
+    dropout factors that multiply P in O."""
     lq, lk, d, dv_ = len(q), len(k), len(q[0]), len(v[0])
     p, _ = _probs(q, k, scale, is_causal, allowed, bias)
-    # dL/dP_ij = sum_c dO_ic V_jc
-    gp = [[sum(do[i][c] * v[j][c] for c in range(dv_)) for j in range(lk)] for i in range(lq)]
+    z = (lambda i, j: 1.0) if drop is None else (lambda i, j: drop[i][j])
+    # dL/dP_ij = z_ij * sum_c dO_ic V_jc
+    gp = [[z(i, j) * sum(do[i][c] * v[j][c] for c in range(dv_)) for j in range(lk)] for i in range(lq)]
     # dL/dS_ik = sum_j gp_ij * P_ij * (delta_jk - P_ik)
     gs = [[0.0] * lk for _ in range(lq)]
     for i in range(lq):
@@ -79,5 +82,5 @@ def bwd_bruteforce(q, k, v, do, scale, is_causal=False, allowed=None, bias=None)
             gs[i][kk] = acc
     dq = [[scale * sum(gs[i][j] * k[j][c] for j in range(lk)) for c in range(d)] for i in range(lq)]
     dk = [[scale * sum(gs[i][j] * q[i][c] for i in range(lq)) for c in range(d)] for j in range(lk)]
-    dv = [[sum(p[i][j] * do[i][c] for i in range(lq)) for c in range(dv_)] for j in range(lk)]
+    dv = [[sum(p[i][j] * z(i, j) * do[i][c] for i in range(lq)) for c in range(dv_)] for j in range(lk)]
     return dq, dk, dv

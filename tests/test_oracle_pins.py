@@ -18,7 +18,8 @@ import pytest
 import torch
 
 from oracle import (attention_probs, attn_bwd_ref, attn_bwd_unit, attn_fwd_ref,
-                    attn_fwd_rows, attn_fwd_unit, bwd_bruteforce, expand_block_mask, fwd_bruteforce)
+                    attn_fwd_rows, attn_fwd_unit, bwd_bruteforce, dropout_keep, dropout_threshold,
+                    expand_block_mask, fwd_bruteforce, philox4x32_10)
 from exact_attention_softmax_gb300 import workloads as wl
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -424,6 +425,72 @@ def test_additive_mask_backward_finite_differences():
         assert np.max(np.abs(num - g)) <= 1e-7 * max(1.0, np.max(np.abs(g)))
 
 
+# ------------------------------------------------------------------ dropout
+
+def test_philox_known_answers():
+    kat = json.load(open(os.path.join(HERE, "golden", "philox_kat.json")))
+    for vec in kat["vectors"]:
+        ctr = np.array([int(x, 16) for x in vec["counter"]], dtype=np.uint32)
+        key = np.array([int(x, 16) for x in vec["key"]], dtype=np.uint32)
+        out = philox4x32_10(ctr, key)
+        assert [f"{int(w):08x}" for w in out] == vec["output"]
+
+
+def test_dropout_keep_rate_and_independence():
+    for p in (0.1, 0.5, 0.9):
+        keep = dropout_keep(1234, 3, 256, 512, p)
+        rate = 1.0 - dropout_threshold(p) / 256.0
+        n = keep.size
+        assert abs(keep.mean() - rate) < 6.0 * np.sqrt(rate * (1 - rate) / n)
+    a = dropout_keep(7, 0, 64, 64, 0.5)
+    b = dropout_keep(7, 1, 64, 64, 0.5)
+    c = dropout_keep(8, 0, 64, 64, 0.5)
+    assert (a != b).mean() > 0.3 and (a != c).mean() > 0.3
+    assert np.array_equal(a, dropout_keep(7, 0, 64, 64, 0.5))     # deterministic
+    assert dropout_keep(7, 0, 8, 8, 0.0).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_matches_bruteforce(causal):
+    lq, lk, d, p, seed = 6, 21, 3, 0.3, 99
+    q, k, v, do = rnd(lq, d, seed=101), rnd(lk, d, seed=102), rnd(lk, d, seed=103), rnd(lq, d, seed=104)
+    o, lse = attn_fwd_ref(q[None], k[None], v[None], 0.7, causal, dropout_p=p, dropout_seed=seed)
+    grads = attn_bwd_ref(q[None], k[None], v[None], do[None], 0.7, causal, dropout_p=p, dropout_seed=seed)
+    z = dropout_keep(seed, 0, lq, lk, p) * (256.0 / (256.0 - dropout_threshold(p)))
+    ob, lb = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.7, causal, drop=z.tolist())
+    gb = bwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), do.tolist(), 0.7, causal, drop=z.tolist())
+    np.testing.assert_allclose(o[0], np.array(ob), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[0], np.array(lb), rtol=0, atol=1e-13)   # LSE ignores dropout
+    for g, r in zip(grads, gb):
+        np.testing.assert_allclose(g[0], np.array(r), rtol=0, atol=1e-13)
+    plain = attn_fwd_ref(q[None], k[None], v[None], 0.7, causal)
+    np.testing.assert_array_equal(plain[1], lse)
+    zero = attn_fwd_ref(q[None], k[None], v[None], 0.7, causal, dropout_p=0.0, dropout_seed=seed)
+    np.testing.assert_array_equal(plain[0], zero[0])
+
+
+def test_dropout_backward_finite_differences():
+    lq, lk, d = 4, 18, 3
+    q, k, v, do = rnd(lq, d, seed=111), rnd(lk, d, seed=112), rnd(lk, d, seed=113), rnd(lq, d, seed=114)
+    kw = dict(dropout_p=0.4, dropout_seed=5)
+    dq, dk, dv = attn_bwd_ref(q, k, v, do, 0.6, False, **kw)
+
+    def loss(qq, kk, vv):
+        o, _ = attn_fwd_ref(qq, kk, vv, 0.6, False, **kw)
+        return float(np.sum(do * o))
+    h = 1e-6
+    for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            ap, am = [q, k, v], [q, k, v]
+            ap[which], am[which] = xp, xm
+            num[idx] = (loss(*ap) - loss(*am)) / (2 * h)
+        assert np.max(np.abs(num - g)) <= 1e-7 * max(1.0, np.max(np.abs(g)))
+
+
 def test_rows_helper_matches_full_unit():
     q, k, v = rnd(10, 4, seed=1), rnd(10, 4, seed=2), rnd(10, 4, seed=3)
     rows = np.array([0, 3, 9])
@@ -561,6 +628,19 @@ def test_bruteforce_catches_mask_added_before_the_scale():
     m = rnd(4, 5, seed=94)
     wrong, _ = attn_fwd_unit(q, k, v, 0.3, False, bias=m * 0.3)
     ob, _ = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.3, False, bias=m.tolist())
+    assert np.max(np.abs(wrong - np.array(ob))) > 1e-3
+
+
+def test_bruteforce_catches_dropout_in_the_normaliser():
+    # an oracle that renormalised over the kept probabilities
+    lq, lk = 4, 16
+    q, k, v = rnd(lq, 3, seed=121), rnd(lk, 3, seed=122), rnd(lk, 3, seed=123)
+    keep = dropout_keep(3, 0, lq, lk, 0.5)
+    p, _ = attention_probs(q, k, 0.5)
+    pk = p * keep
+    wrong = (pk / pk.sum(1, keepdims=True)) @ v
+    z = keep * (256.0 / (256.0 - dropout_threshold(0.5)))
+    ob, _ = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.5, False, drop=z.tolist())
     assert np.max(np.abs(wrong - np.array(ob))) > 1e-3
 
 
