@@ -353,6 +353,18 @@ def extra_results(dev, flush, peaks):
           f"B={B} H={H} L={L} d={d} f16 non-causal, additive mask [1, {H}, {L}, {L}] f16 (N(0,1), 10 % -inf)")
     del q, k, v, do, o, lse, g, ws, x, am
 
+    # dropout on the probabilities, p = 0.1 (Philox keep pattern from a fixed seed)
+    x = wl.dense_inputs(B, H, L, L, d, "f16", "normal", seed=0)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = ops.sdpa_fwd_dropout(q, k, v, 0.1, 1234)
+    ws = torch.empty(ops.sdpa_bwd_workspace_size(B, H, L, d, 1), dtype=torch.uint8, device=dev)
+    g = [torch.empty_like(t) for t in (q, k, v)]
+    timed("dropout_f16_d64", lambda: ops.sdpa_fwd_dropout(q, k, v, 0.1, 1234, o, lse),
+          lambda: ops.sdpa_bwd_dropout(q, k, v, o, lse, do, 0.1, 1234, *g, workspace=ws),
+          4.0 * d * B * H * L * L, 2.5 * 4.0 * d * B * H * L * L,
+          f"B={B} H={H} L={L} d={d} f16 non-causal, dropout p = 0.1")
+    del q, k, v, do, o, lse, g, ws, x
+
     # packed cross-attention: 32 sequences, queries around 256 long, keys around 512
     lq = wl.varlen_lengths(32, 512, 0.5, 0)
     lk = wl.varlen_lengths(32, 1024, 0.5, 1)

@@ -20,7 +20,8 @@ from . import _abi
 from ._abi import SdpaError  # noqa: F401
 
 __all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_fwd_blocksparse",
-           "sdpa_bwd_blocksparse", "sdpa_fwd_masked", "sdpa_bwd_masked", "sdpa_bwd_workspace_size",
+           "sdpa_bwd_blocksparse", "sdpa_fwd_masked", "sdpa_bwd_masked", "sdpa_fwd_dropout",
+           "sdpa_bwd_dropout", "sdpa_bwd_workspace_size",
            "sdpa_device_status",
            "sdpa_debug_set", "sdpa_last_error", "sdpa_version", "SdpaError"]
 
@@ -331,6 +332,49 @@ def sdpa_bwd_masked(q, k, v, o, lse, dO, attn_mask, dq=None, dk=None, dv=None, *
     _abi.check(lib.sdpa_bwd_masked(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
                                    B, H, Lq, Lk, d, float(scale), int(bool(is_causal)), mp, sb, sh, sq, code,
                                    _vp(workspace), workspace.numel(), _stream(q.device, stream)))
+    return dq, dk, dv
+
+
+def sdpa_fwd_dropout(q, k, v, dropout_p, seed, o=None, lse=None, *, scale=None, is_causal=False, stream=None):
+    """Forward with dropout on the probabilities (dense [B,H,L,d]); the keep
+    pattern is a pure function of ``seed`` (Philox4x32-10, see the C header).
+    LSE is that of the full softmax."""
+    import torch
+    lib = _abi.load()
+    if q.dim() != 4:
+        raise ValueError("dropout q must be [B, H, L, d]")
+    B, H, Lq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensors({"k": k, "v": v, "o": o}, q.device, q.dtype)
+    _abi.check(lib.sdpa_fwd_dropout(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), B, H, Lq, k.shape[2], d, float(scale),
+                                    int(bool(is_causal)), float(dropout_p), int(seed) & ((1 << 64) - 1),
+                                    _dtype_code(q), _stream(q.device, stream)))
+    return o, lse
+
+
+def sdpa_bwd_dropout(q, k, v, o, lse, dO, dropout_p, seed, dq=None, dk=None, dv=None, *, scale=None,
+                     is_causal=False, workspace=None, stream=None):
+    """Backward of :func:`sdpa_fwd_dropout` (same ``dropout_p`` and ``seed``)."""
+    import torch
+    lib = _abi.load()
+    B, H, Lq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_tensors({"k": k, "v": v, "o": o, "dO": dO, "dq": dq, "dk": dk, "dv": dv}, q.device, q.dtype)
+    code = _dtype_code(q)
+    need = lib.sdpa_bwd_workspace_size(B, H, Lq, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _abi.check(lib.sdpa_bwd_dropout(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
+                                    B, H, Lq, k.shape[2], d, float(scale), int(bool(is_causal)), float(dropout_p),
+                                    int(seed) & ((1 << 64) - 1), code, _vp(workspace), workspace.numel(),
+                                    _stream(q.device, stream)))
     return dq, dk, dv
 
 

@@ -39,6 +39,9 @@ SIGNATURES = {
                              _vp, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong, _i, _vp]),
     "sdpa_bwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
                              _vp, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong, _i, _vp, _sz, _vp]),
+    "sdpa_fwd_dropout": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _f, ctypes.c_ulonglong, _i, _vp]),
+    "sdpa_bwd_dropout": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
+                              _f, ctypes.c_ulonglong, _i, _vp, _sz, _vp]),
     "sdpa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "sdpa_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),

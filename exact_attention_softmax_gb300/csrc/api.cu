@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/sdpa.h: argument checks, tensor-map
 // construction, the device status word, and dispatch to the kernels.
 // All checks run on the host before anything is launched; no call allocates.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -151,6 +152,12 @@ int check_addmask(const Shape& sh, const AddMask& am, int dtype) {
   return SDPA_OK;
 }
 
+// Dropout (dense layout only).
+struct Dropout {
+  float p;
+  unsigned long long seed;
+};
+
 // Longest query axis a block-sparse backward accepts: its CTAs list their
 // active query steps (up to 2048 of 64 or 128 rows) in shared memory.
 constexpr int kMaxSparseLq = 131072;
@@ -198,7 +205,14 @@ int check_tensors(const void* q, const void* k, const void* v, const void* o, co
 
 void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, const void* v, const void* o,
                   const float* lse, float scale, int is_causal, const BlockMask& bm,
-                  const AddMask& am = AddMask{nullptr, 0, 0, 0}) {
+                  const AddMask& am = AddMask{nullptr, 0, 0, 0}, const Dropout& dr = Dropout{0.f, 0ull}) {
+  // p is used as a multiple of 1/256: bytes below t = round(256 p) drop
+  const int t = std::min(static_cast<int>(std::lround(dr.p * 256.0f)), 255);
+  p.dropout = t > 0 ? 1 : 0;
+  p.drop_t = static_cast<unsigned>(t);
+  p.drop_scale = 256.0f / static_cast<float>(256 - t);
+  p.seed_lo = static_cast<unsigned>(dr.seed & 0xffffffffull);
+  p.seed_hi = static_cast<unsigned>(dr.seed >> 32);
   p.amask = am.m;
   p.am_sb = am.sb;
   p.am_sh = am.sh;
@@ -222,7 +236,8 @@ void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, con
 
 int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o, float* lse, float scale,
             int is_causal, int dtype, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0}, bool sparse = false,
-            const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false) {
+            const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false,
+            const Dropout& dr = Dropout{0.f, 0ull}) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
@@ -230,8 +245,9 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
   if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
   if (sparse && (rc = check_mask(sh, bm, false)) != SDPA_OK) return rc;
   if (masked && (rc = check_addmask(sh, am, dtype)) != SDPA_OK) return rc;
+  if (!(dr.p >= 0.f && dr.p < 1.f)) return fail(SDPA_ERR_ARG, "dropout probability must be in [0, 1) (got %g)", dr.p);
   Problem p{};
-  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am);
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am, dr);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -256,7 +272,8 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
 int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const void* o, const float* lse,
             const void* dO, void* dq, void* dk, void* dv, float scale, int is_causal, int dtype, void* workspace,
             size_t workspace_bytes, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0},
-            bool sparse = false, const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false) {
+            bool sparse = false, const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false,
+            const Dropout& dr = Dropout{0.f, 0ull}) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
@@ -264,6 +281,7 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
   if ((rc = check_tensors(q, k, v, o, lse, dtype)) != SDPA_OK) return rc;
   if (sparse && (rc = check_mask(sh, bm, true)) != SDPA_OK) return rc;
   if (masked && (rc = check_addmask(sh, am, dtype)) != SDPA_OK) return rc;
+  if (!(dr.p >= 0.f && dr.p < 1.f)) return fail(SDPA_ERR_ARG, "dropout probability must be in [0, 1) (got %g)", dr.p);
   if (!dO || !dq || !dk || !dv) return fail(SDPA_ERR_ARG, "null gradient pointer");
   if (dtype != SDPA_F32 && !(aligned16(dO) && aligned16(dq) && aligned16(dk) && aligned16(dv)))
     return fail(SDPA_ERR_ARG, "fp16/bf16 gradients must be 16-byte aligned");
@@ -278,7 +296,7 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
 
   BwdProblem bp{};
   Problem& p = bp.f;
-  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am);
+  fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am, dr);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
@@ -398,6 +416,22 @@ extern "C" int sdpa_bwd_masked(const void* q, const void* k, const void* v, cons
   const AddMask am{attn_mask, mask_stride_b, mask_stride_h, mask_stride_row};
   return run_bwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
                  workspace, workspace_bytes, stream, BlockMask{nullptr, 0, 0, 0}, false, am, true);
+}
+
+extern "C" int sdpa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int Lq, int Lk, int d, float scale, int is_causal, float dropout_p,
+                                unsigned long long seed, int dtype, void* stream) {
+  return run_fwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, scale, is_causal, dtype, stream,
+                 BlockMask{nullptr, 0, 0, 0}, false, AddMask{nullptr, 0, 0, 0}, false, Dropout{dropout_p, seed});
+}
+
+extern "C" int sdpa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                const void* dO, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+                                float scale, int is_causal, float dropout_p, unsigned long long seed, int dtype,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  return run_bwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
+                 workspace, workspace_bytes, stream, BlockMask{nullptr, 0, 0, 0}, false, AddMask{nullptr, 0, 0, 0},
+                 false, Dropout{dropout_p, seed});
 }
 
 extern "C" int sdpa_device_status(void* stream, unsigned* bits) {

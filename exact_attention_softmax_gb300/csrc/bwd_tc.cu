@@ -122,13 +122,14 @@ __device__ __forceinline__ void red_add_v4_f32(float* gdst, uint32_t a, uint32_t
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask (p.amask).
+// EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask
+// (p.amask), 3 dropout (p.dropout).
 template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO) {
   using C = BCfg<D>;
-  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2;
+  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3;
   constexpr int BQ = C::BQ;
   const Problem& p = bp.f;
   extern __shared__ uint8_t smem_raw[];
@@ -495,6 +496,18 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       const uint32_t sl = smem_u32(stat + stage * 2 * BQ + half * NH);   // lse2 of this half
       const uint32_t sd = sl + BQ * 4;                                     // delta of this half
       const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
+      // dropout: the 16 keys of a half-warp share one Philox call per query;
+      // lane o of the half makes the calls of columns o, o + 16, ... and the
+      // others read their byte from it with shuffles
+      uint4 rw[DROP ? NH / 16 : 1];
+      if (DROP) {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int t = 0; t < NH / 16; ++t)
+          rw[t] = philox4x32_10(make_uint4(static_cast<uint32_t>(key >> 4), static_cast<uint32_t>(q0 + (lane & 15) + 16 * t),
+                                           static_cast<uint32_t>(unit), 0u),
+                                p.seed_lo, p.seed_hi);
+      }
       uint32_t pk[NH / 2], dk[NH / 2];
 #pragma unroll
       for (int g = 0; g < NH / 4; ++g) {
@@ -514,8 +527,19 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
           }
           float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, bias2 - l4[h]));
           if (need_mask && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
-          pr[h] = pv;
-          ds[h] = pv * (__uint_as_float(dv[col]) - d4[h]);
+          float zf = 1.f;           // dropout factor of (query q0 + col, key)
+          if (DROP) {
+            const int src = (col & 15) | (threadIdx.x & 16);
+            const uint32_t wx = __shfl_sync(0xffffffffu, rw[col >> 4].x, src);
+            const uint32_t wy = __shfl_sync(0xffffffffu, rw[col >> 4].y, src);
+            const uint32_t wz = __shfl_sync(0xffffffffu, rw[col >> 4].z, src);
+            const uint32_t ww = __shfl_sync(0xffffffffu, rw[col >> 4].w, src);
+            const int b = key & 15;
+            const uint32_t word = b < 8 ? (b < 4 ? wx : wy) : (b < 12 ? wz : ww);
+            zf = ((word >> (8 * (b & 3))) & 0xffu) >= p.drop_t ? p.drop_scale : 0.f;
+          }
+          pr[h] = pv * zf;
+          ds[h] = pv * (__uint_as_float(dv[col]) * zf - d4[h]);
         }
         pk[2 * g] = Pack2<T>::pack(pr[0], pr[1]);
         pk[2 * g + 1] = Pack2<T>::pack(pr[2], pr[3]);
@@ -616,6 +640,8 @@ cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
     return bp.f.causal ? launch_one<D, T, true, false, 1>(bp, m, s) : launch_one<D, T, false, false, 1>(bp, m, s);
   if (bp.f.amask != nullptr)
     return bp.f.causal ? launch_one<D, T, true, false, 2>(bp, m, s) : launch_one<D, T, false, false, 2>(bp, m, s);
+  if (bp.f.dropout)
+    return bp.f.causal ? launch_one<D, T, true, false, 3>(bp, m, s) : launch_one<D, T, false, false, 3>(bp, m, s);
   if (bp.f.cu_seqlens != nullptr)
     return bp.f.causal ? launch_one<D, T, true, true, 0>(bp, m, s) : launch_one<D, T, false, true, 0>(bp, m, s);
   return bp.f.causal ? launch_one<D, T, true, false, 0>(bp, m, s) : launch_one<D, T, false, false, 0>(bp, m, s);

@@ -47,6 +47,13 @@ struct Problem {
   // amask[b * am_sb + h * am_sh + i * am_sq + j], in the input dtype, or NULL.
   const void* amask;
   long long am_sb, am_sh, am_sq;
+  // Dropout (dense layout only): score (i, j) of unit u is kept iff byte
+  // j % 16 of Philox4x32-10(counter (j / 16, i, u, 0), key (seed_lo, seed_hi))
+  // is at least drop_t; kept probabilities are scaled by drop_scale.
+  int dropout;                 // 0 / 1
+  unsigned drop_t;             // round(p * 256), 0..255
+  float drop_scale;            // 256 / (256 - drop_t)
+  unsigned seed_lo, seed_hi;
 };
 
 // Rows and keys per block of a block-sparse mask.

@@ -233,14 +233,15 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
   return it;
 }
 
-// EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask (p.amask).
+// EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask
+// (p.amask), 3 dropout (p.dropout).
 template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               unsigned* sched) {
   using C = Cfg<D>;
-  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2;
+  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
@@ -670,6 +671,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[BN / 4];
 #pragma unroll
+          uint4 rnd = make_uint4(0u, 0u, 0u, 0u);   // dropout bytes of the current 16 keys
+#pragma unroll
           for (int chunk = 0; chunk < BN / 16; ++chunk) {
             const float* xc = x + half * (BN / 2) + chunk * 8;
             float e[8];
@@ -683,6 +686,20 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             add2(s2, s3, e[2], e[3]);
             add2(s0, s1, e[4], e[5]);
             add2(s2, s3, e[6], e[7]);
+            if (DROP) {
+              // the row sum above keeps every probability; P . V sees the
+              // dropped and rescaled ones
+              if ((chunk & 1) == 0)
+                rnd = philox4x32_10(make_uint4(static_cast<uint32_t>(jk * (BN / 16) + half * (BN / 32) + chunk / 2),
+                                               static_cast<uint32_t>(row), static_cast<uint32_t>(it.unit), 0u),
+                                    p.seed_lo, p.seed_hi);
+              const uint32_t w0 = (chunk & 1) ? rnd.z : rnd.x, w1 = (chunk & 1) ? rnd.w : rnd.y;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const uint32_t byte = ((u < 4 ? w0 : w1) >> (8 * (u & 3))) & 0xffu;
+                e[u] = byte >= p.drop_t ? e[u] * p.drop_scale : 0.f;
+              }
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) pk[chunk * 4 + u] = Pack2<T>::pack(e[2 * u], e[2 * u + 1]);
           }
@@ -801,6 +818,8 @@ cudaError_t launch_d(const Problem& p, const FwdMaps& m, cudaStream_t s) {
     return p.causal ? launch_one<D, T, true, false, 1>(p, m, s) : launch_one<D, T, false, false, 1>(p, m, s);
   if (p.amask != nullptr)
     return p.causal ? launch_one<D, T, true, false, 2>(p, m, s) : launch_one<D, T, false, false, 2>(p, m, s);
+  if (p.dropout)
+    return p.causal ? launch_one<D, T, true, false, 3>(p, m, s) : launch_one<D, T, false, false, 3>(p, m, s);
   if (p.causal)
     return packed ? launch_one<D, T, true, true, 0>(p, m, s) : launch_one<D, T, true, false, 0>(p, m, s);
   return packed ? launch_one<D, T, false, true, 0>(p, m, s) : launch_one<D, T, false, false, 0>(p, m, s);

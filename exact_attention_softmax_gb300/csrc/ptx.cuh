@@ -269,6 +269,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Philox4x32 with ten rounds (Salmon, Moraes, Dror, Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3", SC 2011): counter (x, y, z, w), key (k0, k1).
+// Each round multiplies counter words x and z by the round multipliers,
+// keeping both halves of the products, and mixes in y, w and the round key;
+// the key advances by the Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = c.x * 0xD2511F53u, hi0 = __umulhi(c.x, 0xD2511F53u);
+    const uint32_t lo1 = c.z * 0xCD9E8D57u, hi1 = __umulhi(c.z, 0xCD9E8D57u);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
 template <typename T> struct Pack2;
 template <> struct Pack2<__half> {
   static __device__ __forceinline__ uint32_t pack(float a, float b) {

@@ -12,6 +12,7 @@
 // P_ij = exp(scale q_i.k_j - LSE_i) and dS_ij = P_ij (dO_i.v_j - D_i) with
 // D_i = rowsum(dO_i * O_i) from the prep kernel.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace sdpa {
 namespace {
@@ -49,6 +50,16 @@ __device__ __forceinline__ Unit unit_of(const Problem& p, int b, int h) {
     u.bad = u.len_q > p.max_q || u.len_k > p.Lk || (u.len_q > 0 && u.len_k <= 0);
   }
   return u;
+}
+
+// Dropout factor of score (i, j) of dense unit `unit` (see Problem::dropout).
+__device__ __forceinline__ float drop_factor(const Problem& p, int unit, int i, int j) {
+  const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j >> 4), static_cast<uint32_t>(i),
+                                           static_cast<uint32_t>(unit), 0u),
+                                p.seed_lo, p.seed_hi);
+  const int b = j & 15;
+  const uint32_t w = b < 8 ? (b < 4 ? r.x : r.y) : (b < 12 ? r.z : r.w);
+  return ((w >> (8 * (b & 3))) & 0xffu) >= p.drop_t ? p.drop_scale : 0.f;
 }
 
 template <int DMAX>
@@ -112,8 +123,9 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
       }
       const float e = expf(s - m);
       l += e;
+      const float ez = p.dropout ? e * drop_factor(p, b * p.H + h, row, key) : e;   // P . V sees dropout
 #pragma unroll
-      for (int c = 0; c < DMAX; ++c) acc[c] = fmaf(e, sv[jj][c], acc[c]);
+      for (int c = 0; c < DMAX; ++c) acc[c] = fmaf(ez, sv[jj][c], acc[c]);
     }
   }
   if (!live) return;
@@ -181,7 +193,8 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
         dp = fmaf(dor[c], sv[jj][c], dp);
       }
       const float pr = expf(s * p.scale + bias - lse);
-      const float ds = pr * (dp - D);
+      const float z = p.dropout ? drop_factor(p, b * p.H + h, row, key) : 1.f;
+      const float ds = pr * (dp * z - D);
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) dq[c] = fmaf(ds, sk[jj][c], dq[c]);
     }
@@ -252,10 +265,11 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
         dp = fmaf(sdo[ii][c], vr[c], dp);
       }
       const float pr = expf(s * p.scale + bias - slse[ii]);
-      const float ds = pr * (dp - sD[ii]);
+      const float z = p.dropout ? drop_factor(p, b * p.H + h, qi, key) : 1.f;
+      const float ds = pr * (dp * z - sD[ii]);
 #pragma unroll
       for (int c = 0; c < DMAX; ++c) {
-        dv[c] = fmaf(pr, sdo[ii][c], dv[c]);
+        dv[c] = fmaf(pr * z, sdo[ii][c], dv[c]);
         dk[c] = fmaf(ds, sq[ii][c], dk[c]);
       }
     }

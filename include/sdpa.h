@@ -221,6 +221,36 @@ int sdpa_bwd_masked(const void* q, const void* k, const void* v, const void* o, 
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Attention with dropout on the probabilities (the SDPA tutorial's
+ * dropout_p argument, section "Causal Self Attention"):
+ * O = (P * Z) V with P = softmax(scale * Q K^T [+ causal mask]) and Z = 0
+ * for a dropped score, 1/(1 - p') for a kept one; LSE is that of the full
+ * softmax. Dense layout only.
+ *   dropout_p : in [0, 1); used as p' = t / 256 with t = round(256 p)
+ *               (t = 0 is no dropout).
+ *   seed      : 64-bit key of the generator. Score (i, j) of head
+ *               u = b * H + h is kept iff byte (j mod 16) (little-endian
+ *               within the 32-bit words) of Philox4x32-10 (Salmon et al.,
+ *               SC 2011) at counter (j / 16, i, u, 0) and key
+ *               (seed mod 2^32, seed / 2^32) is at least t.
+ * Other arguments, support and errors as for sdpa_fwd with cu_seqlens = NULL.
+ */
+int sdpa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                     float dropout_p, unsigned long long seed, int dtype, void* stream);
+
+/*
+ * Backward of sdpa_fwd_dropout: the same dropout_p and seed reproduce the
+ * forward's keep pattern. Arguments, workspace and support as for sdpa_bwd
+ * with cu_seqlens = NULL.
+ */
+int sdpa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv,
+                     int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                     float dropout_p, unsigned long long seed, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward pass for callers that cannot allocate device memory: it takes the
  * same arguments as sdpa_bwd except the workspace and cu_seqlens (dense
  * layout only), and uses a scratch array of 16 MiB compiled into the library
