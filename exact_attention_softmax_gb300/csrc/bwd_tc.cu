@@ -65,7 +65,10 @@ struct BCfg {
   static constexpr int kQTile = BQ * D * 2;
   static constexpr int kPColBlk = BK * 128;                  // P^T / dS^T: [128 keys][64 queries] blocks
   static constexpr int kPBytes = BK * BQ * 2;
-  static constexpr int kStages = 2;
+  // Q/dO stages: a stage stays busy from its load until the dV/dK MMAs of
+  // its step, about one step after its S^T MMA; a third stage lets the next
+  // load start early enough at d = 64 (d = 128 has no room for it)
+  static constexpr int kStages = D == 64 ? 3 : 2;
   // shared memory map
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKTile;
@@ -90,8 +93,8 @@ struct BCfg {
 
 struct __align__(8) BBars {
   uint64_t kv;
-  uint64_t full[2];
-  uint64_t empty[2];
+  uint64_t full[3];
+  uint64_t empty[3];
   uint64_t s_full;     // S^T, dP^T of the current tile in TMEM
   uint64_t s_free;     // ... read into registers by both softmax groups
   uint64_t pds_full;   // P^T, dS^T in shared memory
@@ -185,9 +188,11 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars->full[i], 32);
       mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->dq_full[i], 1);
       mbar_init(&bars->dq_free[i], 128);
     }
@@ -268,7 +273,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     fetch(0);
     int s = 0;
     for (; s < nsteps; ++s) {
-      const int stage = s & 1, round = s >> 1;
+      const int stage = s % C::kStages, round = s / C::kStages;
       bool ok = !*abort_flag;
       if (ok && lane == 0 && round > 0) ok = mbar_wait(&bars->empty[stage], (round - 1) & 1, abort_flag, p.status);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
@@ -294,7 +299,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     }
     if (lane == 0 && *abort_flag) {
       mbar_wait_drain(&bars->kv, 0);
-      for (int f = max(0, s - 2); f < s; ++f) mbar_wait_drain(&bars->full[f & 1], (f >> 1) & 1);
+      for (int f = max(0, s - C::kStages); f < s; ++f) mbar_wait_drain(&bars->full[f % C::kStages], (f / C::kStages) & 1);
     }
    } else if (warp == kMmaSWarp || warp == kMmaGWarp) {
     // ------------------------------------------------------------ MMA issue
@@ -335,8 +340,8 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         const uint64_t dQ0 = smem_desc(sQ, 16, C::kSbo, C::kSw);
         const uint64_t dO0 = smem_desc(sDO, 16, C::kSbo, C::kSw);
         for (int s = 0; s < nsteps && ok; ++s) {
-          const int stage = s & 1;
-          if (!(ok = wait(&bars->full[stage], (s >> 1) & 1))) break;
+          const int stage = s % C::kStages;
+          if (!(ok = wait(&bars->full[stage], (s / C::kStages) & 1))) break;
           if (s > 0 && !(ok = wait(&bars->s_free, (s - 1) & 1))) break;
           tc_fence_after();
           const uint32_t qoff = (stage * C::kQTile) >> 4;
@@ -365,7 +370,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         const uint64_t dQm = smem_desc(sQ, C::kQColBlk, C::kSbo, C::kSw);
         const uint64_t dOm = smem_desc(sDO, C::kQColBlk, C::kSbo, C::kSw);
         for (int s = 0; s < nsteps && ok; ++s) {
-          const int stage = s & 1;
+          const int stage = s % C::kStages;
           if (!(ok = wait(&bars->pds_full, s & 1))) break;
           tc_fence_after();
           const uint32_t qoff = (stage * C::kQTile) >> 4;
@@ -462,7 +467,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     constexpr int NH = C::kHalf;
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
-      const int stage = s & 1;
+      const int stage = s % C::kStages;
       // additive mask: M[q][key] for this group's query columns, loaded before
       // the waits so the loads overlap them (a warp reads 32 adjacent keys)
       uint32_t amk[BIAS ? NH / 2 : 1];
@@ -480,7 +485,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         }
       }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, abort_flag, p.status) &&
-                                       mbar_wait(&bars->full[stage], (s >> 1) & 1, abort_flag, p.status));
+                                       mbar_wait(&bars->full[stage], (s / C::kStages) & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
       uint32_t sv[NH], dv[NH];
