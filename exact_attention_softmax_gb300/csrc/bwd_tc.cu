@@ -498,8 +498,6 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       tc_fence_before();
       mbar_arrive(&bars->s_free);               // the next S^T / dP^T may be written
       const int q0 = qstep(s) * BQ + half * NH;
-      const uint32_t sl = smem_u32(stat + stage * 2 * BQ + half * NH);   // lse2 of this half
-      const uint32_t sd = sl + BQ * 4;                                     // delta of this half
       const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
       // dropout: the 16 keys of a half-warp share one Philox call per query;
       // lane o of the half makes the calls of columns o, o + 16, ... and the
@@ -514,43 +512,53 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
                                 p.seed_lo, p.seed_hi);
       }
       uint32_t pk[NH / 2], dk[NH / 2];
+      // row statistics of this half's query columns (written by the producer
+      // before it arrived on full[stage])
+      const float* slf = stat + stage * 2 * BQ + half * NH;
+      // the per-element causal / length test only where the tile needs it
+      auto body = [&](auto masked) {
+        constexpr bool M = decltype(masked)::value;
 #pragma unroll
-      for (int g = 0; g < NH / 4; ++g) {
-        float l4[4], d4[4];
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(l4[0]), "=f"(l4[1]), "=f"(l4[2]), "=f"(l4[3]) : "r"(sl + g * 16));
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(d4[0]), "=f"(d4[1]), "=f"(d4[2]), "=f"(d4[3]) : "r"(sd + g * 16));
-        float pr[4], ds[4];
+        for (int g = 0; g < NH / 4; ++g) {
+          // loaded in program order: hoisting them costs registers and spills
+          float l4[4], d4[4];
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(l4[0]), "=f"(l4[1]), "=f"(l4[2]), "=f"(l4[3]) : "r"(smem_u32(slf + 4 * g)));
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(d4[0]), "=f"(d4[1]), "=f"(d4[2]), "=f"(d4[3]) : "r"(smem_u32(slf + BQ + 4 * g)));
+          float pr[4], ds[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int col = 4 * g + h;
-          float bias2 = 0.f;        // additive mask in base 2
-          if (BIAS) {
-            const float2 mf = Pack2<T>::unpack(amk[col / 2]);
-            bias2 = ((col & 1) ? mf.y : mf.x) * kLog2e;
+          for (int h = 0; h < 4; ++h) {
+            const int col = 4 * g + h;
+            float bias2 = 0.f;        // additive mask in base 2
+            if (BIAS) {
+              const float2 mf = Pack2<T>::unpack(amk[col / 2]);
+              bias2 = ((col & 1) ? mf.y : mf.x) * kLog2e;
+            }
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, bias2 - l4[h]));
+            if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
+            float zf = 1.f;           // dropout factor of (query q0 + col, key)
+            if (DROP) {
+              const int src = (col & 15) | (threadIdx.x & 16);
+              const uint32_t wx = __shfl_sync(0xffffffffu, rw[col >> 4].x, src);
+              const uint32_t wy = __shfl_sync(0xffffffffu, rw[col >> 4].y, src);
+              const uint32_t wz = __shfl_sync(0xffffffffu, rw[col >> 4].z, src);
+              const uint32_t ww = __shfl_sync(0xffffffffu, rw[col >> 4].w, src);
+              const int b = key & 15;
+              const uint32_t word = b < 8 ? (b < 4 ? wx : wy) : (b < 12 ? wz : ww);
+              zf = ((word >> (8 * (b & 3))) & 0xffu) >= p.drop_t ? p.drop_scale : 0.f;
+            }
+            pr[h] = pv * zf;
+            ds[h] = pv * (__uint_as_float(dv[col]) * zf - d4[h]);
           }
-          float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, bias2 - l4[h]));
-          if (need_mask && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
-          float zf = 1.f;           // dropout factor of (query q0 + col, key)
-          if (DROP) {
-            const int src = (col & 15) | (threadIdx.x & 16);
-            const uint32_t wx = __shfl_sync(0xffffffffu, rw[col >> 4].x, src);
-            const uint32_t wy = __shfl_sync(0xffffffffu, rw[col >> 4].y, src);
-            const uint32_t wz = __shfl_sync(0xffffffffu, rw[col >> 4].z, src);
-            const uint32_t ww = __shfl_sync(0xffffffffu, rw[col >> 4].w, src);
-            const int b = key & 15;
-            const uint32_t word = b < 8 ? (b < 4 ? wx : wy) : (b < 12 ? wz : ww);
-            zf = ((word >> (8 * (b & 3))) & 0xffu) >= p.drop_t ? p.drop_scale : 0.f;
-          }
-          pr[h] = pv * zf;
-          ds[h] = pv * (__uint_as_float(dv[col]) * zf - d4[h]);
+          pk[2 * g] = Pack2<T>::pack(pr[0], pr[1]);
+          pk[2 * g + 1] = Pack2<T>::pack(pr[2], pr[3]);
+          dk[2 * g] = Pack2<T>::pack(ds[0], ds[1]);
+          dk[2 * g + 1] = Pack2<T>::pack(ds[2], ds[3]);
         }
-        pk[2 * g] = Pack2<T>::pack(pr[0], pr[1]);
-        pk[2 * g + 1] = Pack2<T>::pack(pr[2], pr[3]);
-        dk[2 * g] = Pack2<T>::pack(ds[0], ds[1]);
-        dk[2 * g + 1] = Pack2<T>::pack(ds[2], ds[3]);
-      }
+      };
+      if (need_mask) body(std::true_type{});
+      else body(std::false_type{});
       // P^T / dS^T buffers are free once the previous tile's dV, dK, dQ MMAs finished
       if (s > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_free, (s - 1) & 1, abort_flag, p.status));
       if (!ok) break;
