@@ -51,35 +51,54 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdProblem bp, long long 
   const T* O = static_cast<const T*>(p.o) + elem;
   const T* dO = static_cast<const T*>(bp.dO) + elem;
   float acc = 0.f;
-  if (live) {
+  if (sizeof(T) == 2) {
+    // fp16 / bf16 (d a multiple of 8, rows 16-byte aligned): one 16-byte load
+    // of O and of dO per lane, and two 16-byte stores of zeros
+    if (live && sub * 8 < p.d) {
+      const uint4 ov = *reinterpret_cast<const uint4*>(O + sub * 8);
+      const uint4 gv = *reinterpret_cast<const uint4*>(dO + sub * 8);
+      const T* oe = reinterpret_cast<const T*>(&ov);
+      const T* ge = reinterpret_cast<const T*>(&gv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(to_f<T>(oe[e]), to_f<T>(ge[e]), acc);
+      if (zero_acc) {
+        float4* A = reinterpret_cast<float4*>(bp.dq_acc + elem + sub * 8);
+        A[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        A[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  } else if (live) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int c = sub * 8 + e;
       if (c < p.d) acc = fmaf(to_f<T>(O[c]), to_f<T>(dO[c]), acc);
     }
+    if (zero_acc) {
+      float* A = bp.dq_acc + elem;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = sub * 8 + e;
+        if (c < p.d) A[c] = 0.f;
+      }
+    }
   }
   for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (live && sub == 0) bp.delta[stat] = acc;
-  if (live && zero_acc) {
-    float* A = bp.dq_acc + elem;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int c = sub * 8 + e;
-      if (c < p.d) A[c] = 0.f;
-    }
-  }
 }
 
+// Eight elements per thread: two 16-byte loads, one 16-byte store (n is a
+// multiple of 8 on the fp16 / bf16 path, whose head dims are 64 or 128).
 template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq,
                                                          long long n, float scale) {
-  const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
-  if (i + 3 < n) {
+  const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  if (i + 7 < n) {
     const float4 a = *reinterpret_cast<const float4*>(acc + i);
-    dq[i] = from_f<T>(a.x * scale);
-    dq[i + 1] = from_f<T>(a.y * scale);
-    dq[i + 2] = from_f<T>(a.z * scale);
-    dq[i + 3] = from_f<T>(a.w * scale);
+    const float4 b = *reinterpret_cast<const float4*>(acc + i + 4);
+    __align__(16) T out[8] = {from_f<T>(a.x * scale), from_f<T>(a.y * scale), from_f<T>(a.z * scale),
+                              from_f<T>(a.w * scale), from_f<T>(b.x * scale), from_f<T>(b.y * scale),
+                              from_f<T>(b.z * scale), from_f<T>(b.w * scale)};
+    *reinterpret_cast<uint4*>(dq + i) = *reinterpret_cast<const uint4*>(out);
   } else {
     for (long long j = i; j < n; ++j) dq[j] = from_f<T>(acc[j] * scale);
   }
@@ -109,7 +128,7 @@ cudaError_t launch_dq_convert(const BwdProblem& bp, int dtype, cudaStream_t s) {
   const Problem& p = bp.f;
   const long long n = query_rows(p) * p.d;
   if (n == 0) return cudaSuccess;
-  const unsigned blocks = static_cast<unsigned>((n / 4 + 255) / 256 + 1);
+  const unsigned blocks = static_cast<unsigned>((n / 8 + 255) / 256 + 1);
   if (dtype == kF16)
     dq_convert_kernel<__half><<<blocks, 256, 0, s>>>(bp.dq_acc, static_cast<__half*>(bp.dq), n, p.scale);
   else
