@@ -647,30 +647,10 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
           for (int i = 0; i < BN; ++i) x[i] = i < lim ? x[i] : -INFINITY;
         }
-        // row maximum: four independent chains of three-input max
-        float mx0 = max3f(x[0], x[1], x[2]), mx1 = max3f(x[3], x[4], x[5]);
-        float mx2 = max3f(x[6], x[7], x[8]), mx3 = max3f(x[9], x[10], x[11]);
-#pragma unroll
-        for (int i = 12; i < BN - 4; i += 8) {
-          mx0 = max3f(mx0, x[i], x[i + 1]);
-          mx1 = max3f(mx1, x[i + 2], x[i + 3]);
-          mx2 = max3f(mx2, x[i + 4], x[i + 5]);
-          mx3 = max3f(mx3, x[i + 6], x[i + 7]);
-        }
-        mx0 = max3f(mx0, x[BN - 4], x[BN - 3]);
-        mx1 = max3f(mx1, x[BN - 2], x[BN - 1]);
-        const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * (BIAS ? 1.f : c);
-        const bool grow = mx > m_run + kRescaleThreshold;
-        const float m_new = grow ? mx : m_run;
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2_approx(m_run - m_use);
-        // exponentials into packed registers, stored to TMEM in two halves; the
-        // first half is computed before waiting for P_t's columns to be free
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[BN / 4];
-#pragma unroll
+        // exponentials of one half of the block (BN / 2 keys) against the
+        // exponent offset mu, packed for TMEM; the sums keep every probability
+        auto exps_half = [&](int half, float mu, uint32_t (&pk)[BN / 4], float& s0, float& s1, float& s2,
+                             float& s3) {
           uint4 rnd = make_uint4(0u, 0u, 0u, 0u);   // dropout bytes of the current 16 keys
 #pragma unroll
           for (int chunk = 0; chunk < BN / 16; ++chunk) {
@@ -678,7 +658,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             float e[8];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], BIAS ? 1.f : c, -m_use);
+              fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], BIAS ? 1.f : c, -mu);
               e[2 * u] = ex2_approx(e[2 * u]);
               e[2 * u + 1] = ex2_approx(e[2 * u + 1]);
             }
@@ -703,12 +683,81 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int u = 0; u < 4; ++u) pk[chunk * 4 + u] = Pack2<T>::pack(e[2 * u], e[2 * u + 1]);
           }
-          // P_t's columns are free once the previous P.V on this tile (possibly
-          // the last one of the previous item) has finished; at d = 128 they
-          // overlay S_t, already in registers, and that MMA finished before S_j
-          if (half == 0 && !C::kPAlias && (j > 0 || pend.on)) ok = wait_all(&bars->pv_done[t], (g - 1) & 1);
-          if (!ok) break;
-          tmem_st32(tP + half * 32, pk);
+        };
+        // P_t's columns are free once the previous P.V on this tile (possibly
+        // the last one of the previous item) has finished; at d = 128 they
+        // overlay S_t, already in registers, and that MMA finished before S_j
+        bool waited = C::kPAlias || !(j > 0 || pend.on);
+        auto wait_p_free = [&]() {
+          if (!waited) ok = wait_all(&bars->pv_done[t], (g - 1) & 1);
+          waited = true;
+        };
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        bool grow = false;
+        float m_new = m_run, alpha = 1.f;
+        bool done = false;
+        if (D == 128 && j > 0) {
+          // After the first block the running maximum is usually still good
+          // enough: exponentiate against it and keep the result if the block's
+          // probabilities sum to at most 2^kRescaleThreshold (so each is at most
+          // that, the bound the lazy rescale allows). Otherwise fall back to
+          // the block's own maximum below. Softmax is shift invariant, so both
+          // give the same result; the first avoids the max pass. (Measured: it
+          // pays at d = 128; at d <= 64 the extra warp votes cost more.)
+          const float mu = m_run == -INFINITY ? 0.f : m_run;
+          constexpr float kSumLimit = 256.f;   // 2^kRescaleThreshold
+          uint32_t pk[BN / 4];
+          exps_half(0, mu, pk, s0, s1, s2, s3);
+          if (!__any_sync(0xffffffffu, (s0 + s1) + (s2 + s3) > kSumLimit)) {
+            wait_p_free();
+            if (!ok) break;
+            tmem_st32(tP, pk);
+            float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+            exps_half(1, mu, pk, t0, t1, t2, t3);
+            const float tot = ((s0 + s1) + (s2 + s3)) + ((t0 + t1) + (t2 + t3));
+            if (!__any_sync(0xffffffffu, tot > kSumLimit)) {
+              tmem_st32(tP + 32, pk);
+              s0 += t0;
+              s1 += t1;
+              s2 += t2;
+              s3 += t3;
+              // the offset used becomes the running maximum (it differs only
+              // for a row whose earlier keys were all masked: then l = 0, O = 0)
+              m_new = mu;
+              alpha = ex2_approx(m_run - mu);
+              done = true;
+            }
+          }
+        }
+        if (!done) {
+          // row maximum: four independent chains of three-input max
+          float mx0 = max3f(x[0], x[1], x[2]), mx1 = max3f(x[3], x[4], x[5]);
+          float mx2 = max3f(x[6], x[7], x[8]), mx3 = max3f(x[9], x[10], x[11]);
+#pragma unroll
+          for (int i = 12; i < BN - 4; i += 8) {
+            mx0 = max3f(mx0, x[i], x[i + 1]);
+            mx1 = max3f(mx1, x[i + 2], x[i + 3]);
+            mx2 = max3f(mx2, x[i + 4], x[i + 5]);
+            mx3 = max3f(mx3, x[i + 6], x[i + 7]);
+          }
+          mx0 = max3f(mx0, x[BN - 4], x[BN - 3]);
+          mx1 = max3f(mx1, x[BN - 2], x[BN - 1]);
+          const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * (BIAS ? 1.f : c);
+          grow = mx > m_run + kRescaleThreshold;
+          m_new = grow ? mx : m_run;
+          const float m_use = m_new == -INFINITY ? 0.f : m_new;
+          alpha = ex2_approx(m_run - m_use);
+          // exponentials into packed registers, stored to TMEM in two halves; the
+          // first half is computed before waiting for P_t's columns to be free
+          s0 = s1 = s2 = s3 = 0.f;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[BN / 4];
+            exps_half(half, m_use, pk, s0, s1, s2, s3);
+            if (half == 0) wait_p_free();
+            if (!ok) break;
+            tmem_st32(tP + half * 32, pk);
+          }
         }
         if (!ok) break;
         l = l * alpha + ((s0 + s1) + (s2 + s3));
