@@ -96,6 +96,7 @@ struct Cfg {
   // warps (the rest of it idles), so that registers can move between them.
   static constexpr int kThreads = 384;
   static_assert(kPAlias || kColP + 2 * (BN / 2) <= 512, "TMEM budget");
+  static_assert(kSlots <= 16 && kQBufs <= 2, "the barrier arrays hold 16 ring slots and 2 Q buffers per tile");
 };
 
 struct __align__(8) Bars {
