@@ -89,6 +89,7 @@ struct BCfg {
   static constexpr int kDqCols = kDqT ? BQ : D;
   static constexpr uint32_t kTS = 0, kTdP = BQ, kTdV = 2 * BQ, kTdK = 2 * BQ + D, kTdQ = 2 * BQ + 2 * D;
   static_assert(kTdQ + 2 * kDqCols <= 512, "TMEM budget");
+  static_assert(kStages <= 3, "the barrier arrays hold 3 Q/dO stages");
 };
 
 struct __align__(8) BBars {
