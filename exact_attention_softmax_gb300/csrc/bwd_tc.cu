@@ -18,7 +18,8 @@
 //
 // Warps: 0-3 and 4-7 build P^T / dS^T for the first and second half of the
 // tile's queries (then write dV and dK); 8-11 drain dQ; 12 loads with TMA;
-// 13 issues S^T and dP^T; 14 issues dV, dK and dQ; 15 idles. The softmax
+// 13 issues S^T and dP^T; 14 issues dV, dK and dQ; 15 loads the additive
+// mask (masked kernels; it idles otherwise). The softmax
 // groups release S^T / dP^T as soon as they hold them in registers, so the
 // next tile's S^T, dP^T run under their arithmetic, and dQ has two TMEM
 // buffers so its drain overlaps the next tile.
@@ -37,6 +38,7 @@ constexpr int kDqWarp0 = 8;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaSWarp = 13;
 constexpr int kMmaGWarp = 14;
+constexpr int kMaskWarp = 15;    // additive mask loads (the warp idles otherwise)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 // Register split (launch: 512 threads x 128): softmax groups 160, dQ drain and
@@ -45,7 +47,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kRegsSoftmax = 160;
 constexpr uint32_t kRegsOther = 96;
 
-template <int D>
+template <int D, int EXT>
 struct BCfg {
   static constexpr int BQ = D == 128 ? 64 : 128;            // query rows per step
   static constexpr int kHalf = BQ / 2;                       // query columns per softmax group
@@ -67,8 +69,10 @@ struct BCfg {
   static constexpr int kPBytes = BK * BQ * 2;
   // Q/dO stages: a stage stays busy from its load until the dV/dK MMAs of
   // its step, about one step after its S^T MMA; a third stage lets the next
-  // load start early enough at d = 64 (d = 128 has no room for it)
-  static constexpr int kStages = D == 64 ? 3 : 2;
+  // load start early enough at d = 64 (d = 128, and the additive-mask kernel
+  // with its mask ring, have no room for it)
+  static constexpr bool kMask = EXT == 2;
+  static constexpr int kStages = D == 64 && !kMask ? 3 : 2;
   // shared memory map
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKTile;
@@ -79,10 +83,14 @@ struct BCfg {
   static constexpr int kDqBytes = kDqT ? BQ * D * 4 : 0;     // fp32 dQ staging tile (d = 128 only)
   static constexpr int kOffDQ = kOffDST + kPBytes;
   static constexpr int kOffStat = kOffDQ + kDqBytes;                    // kStages x (lse2[BQ], delta[BQ])
-  // block-sparse: the CTA's active query steps (uint16 indices)
+  // block-sparse: the CTA's active query steps (uint16 indices); additive
+  // mask: a ring of two slots, each 32 query rows x 128 keys for both
+  // softmax groups (the same region)
   static constexpr int kMaxSteps = 2048;
+  static constexpr int kMaskTile = 32 * BK * 2;
+  static constexpr int kMaskSlot = 2 * kMaskTile;
   static constexpr int kOffList = kOffStat + kStages * BQ * 8;
-  static constexpr int kOffBar = kOffList + kMaxSteps * 2;
+  static constexpr int kOffBar = kOffList + (kMask ? 2 * kMaskSlot : kMaxSteps * 2);
   static constexpr int kSmem = kOffBar + 256 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   // TMEM columns: S^T, dP^T, dV, dK, two dQ buffers
@@ -104,10 +112,13 @@ struct __align__(8) BBars {
   uint64_t dq_free[2];
   uint64_t kv_done;
   uint64_t done;
+  uint64_t mfull[2];   // additive mask slot loaded
+  uint64_t mempty[2];  // ... read by the 8 softmax warps
   uint32_t tmem_base;
   uint32_t abort_flag;
   int nsteps;          // block-sparse: number of active query steps
 };
+static_assert(sizeof(BBars) <= 256, "the barrier block has 256 bytes of shared memory");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -126,15 +137,64 @@ __device__ __forceinline__ void red_add_v4_f32(float* gdst, uint32_t a, uint32_t
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 16 x 16 byte transpose across the half-warp that holds lanes hl = 0..15:
+// on entry byte k of lane hl's 16 bytes belongs to lane k, on return byte c
+// of lane k's 16 bytes came from lane c. Four butterfly stages; stage j
+// swaps bit j of the lane index with bit j of the byte index, exchanging 8
+// of the 16 bytes with lane hl ^ 2^j (two shuffles a stage).
+__device__ __forceinline__ void transpose16_bytes(uint32_t (&w)[4], int hl) {
+  {
+    const bool b = hl & 8;
+    const uint32_t ra = __shfl_xor_sync(0xffffffffu, b ? w[0] : w[2], 8);
+    const uint32_t rb = __shfl_xor_sync(0xffffffffu, b ? w[1] : w[3], 8);
+    if (b) { w[0] = ra; w[1] = rb; } else { w[2] = ra; w[3] = rb; }
+  }
+  {
+    const bool b = hl & 4;
+    const uint32_t ra = __shfl_xor_sync(0xffffffffu, b ? w[0] : w[1], 4);
+    const uint32_t rb = __shfl_xor_sync(0xffffffffu, b ? w[2] : w[3], 4);
+    if (b) { w[0] = ra; w[2] = rb; } else { w[1] = ra; w[3] = rb; }
+  }
+  // bytes within a word: send the half (then byte) the partner owns, keep the
+  // rest, and put the partner's bytes where the sent ones were
+  {
+    const bool b = hl & 2;
+    const uint32_t sel = b ? 0x5410u : 0x7632u, p0 = b ? 0x3254u : 0x5410u, p1 = b ? 0x3276u : 0x7610u;
+    const uint32_t ra = __shfl_xor_sync(0xffffffffu, __byte_perm(w[0], w[1], sel), 2);
+    const uint32_t rb = __shfl_xor_sync(0xffffffffu, __byte_perm(w[2], w[3], sel), 2);
+    w[0] = __byte_perm(w[0], ra, p0); w[1] = __byte_perm(w[1], ra, p1);
+    w[2] = __byte_perm(w[2], rb, p0); w[3] = __byte_perm(w[3], rb, p1);
+  }
+  {
+    const bool b = hl & 1;
+    const uint32_t sel = b ? 0x6420u : 0x7531u, p0 = b ? 0x3514u : 0x5240u, p1 = b ? 0x3716u : 0x7260u;
+    const uint32_t ra = __shfl_xor_sync(0xffffffffu, __byte_perm(w[0], w[1], sel), 1);
+    const uint32_t rb = __shfl_xor_sync(0xffffffffu, __byte_perm(w[2], w[3], sel), 1);
+    w[0] = __byte_perm(w[0], ra, p0); w[1] = __byte_perm(w[1], ra, p1);
+    w[2] = __byte_perm(w[2], rb, p0); w[3] = __byte_perm(w[3], rb, p1);
+  }
+}
+
 // EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask
 // (p.amask), 3 dropout (p.dropout).
 template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO) {
-  using C = BCfg<D>;
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmM) {
+  using C = BCfg<D, EXT>;
   constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3;
   constexpr int BQ = C::BQ;
+  constexpr int NH = C::kHalf;     // query columns per softmax group
+  // The additive mask and dropout need registers of their own, so their
+  // steps go through in chunks of 32 query columns (S^T / dP^T read from
+  // TMEM a chunk at a time); the other kernels take the half in one piece.
+  constexpr int CH = (BIAS || DROP) && NH > 32 ? 32 : NH;
+  constexpr int NCH = NH / CH;
+  static_assert(!BIAS || CH * BK * 2 == C::kMaskTile, "a mask slot holds one chunk of each softmax group");
   const Problem& p = bp.f;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,6 +263,10 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     mbar_init(&bars->pds_free, 2);     // dV/dK warp and dQ warp
     mbar_init(&bars->kv_done, 1);
     mbar_init(&bars->done, 2);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->mfull[i], 1);
+      mbar_init(&bars->mempty[i], 8);
+    }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -392,6 +456,28 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       mma_commit(&bars->done);
       mbar_wait_drain(&bars->done, 0);
     }
+   } else if (BIAS && warp == kMaskWarp) {
+    // ------------------------------------------------ additive mask loads
+    // Chunk n (query step n / NCH, columns (n % NCH) * CH of each group) goes
+    // to slot n % 2 as one 32 x 128 box per softmax group, so the mask of the
+    // next chunk is in flight while a chunk computes.
+    if (lane == 0 && !*abort_flag) {
+      tma_prefetch_desc(&tmM);
+      const int zc = p.am_sh ? unit % p.H : 0, wc = p.am_sb ? unit / p.H : 0;
+      const int total = nsteps * NCH;
+      int n = 0;
+      for (; n < total; ++n) {
+        const int slot = n & 1;
+        if (n >= 2 && !mbar_wait(&bars->mempty[slot], ((n - 2) >> 1) & 1, abort_flag, p.status)) break;
+        const int q0 = qstep(n / NCH) * BQ + (n % NCH) * CH;
+        mbar_expect_tx(&bars->mfull[slot], C::kMaskSlot);
+        for (int h = 0; h < 2; ++h)
+          tma_load_4d(smem + C::kOffList + slot * C::kMaskSlot + h * C::kMaskTile, &tmM, &bars->mfull[slot], key0,
+                      q0 + h * NH, zc, wc);
+      }
+      if (*abort_flag)
+        for (int f = max(0, n - 2); f < n; ++f) mbar_wait_drain(&bars->mfull[f & 1], (f >> 1) & 1);
+    }
    } else if (warp < kDqWarp0 + 4) {
     // ------------------------------------------------ dQ drain
     // d = 128 (lane = head dim, columns = queries): staged as [query][D] in
@@ -465,112 +551,123 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     const int key = key0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale * kLog2e;
-    constexpr int NH = C::kHalf;
     bool ok = true;
+    // this thread's key column of the additive mask slots ([32 queries][128 keys] per group)
+    const T* mkey = reinterpret_cast<const T*>(smem + C::kOffList + half * C::kMaskTile) + r;
     for (int s = 0; s < nsteps; ++s) {
       const int stage = s % C::kStages;
-      // additive mask: M[q][key] for this group's query columns, loaded before
-      // the waits so the loads overlap them (a warp reads 32 adjacent keys)
-      uint32_t amk[BIAS ? NH / 2 : 1];
-      if (BIAS) {
-        const int qa = qstep(s) * BQ + half * NH;
-        const T* mcol = static_cast<const T*>(p.amask) + (unit / p.H) * p.am_sb + (unit % p.H) * p.am_sh + key;
-#pragma unroll
-        for (int cpair = 0; cpair < NH / 2; ++cpair) {
-          unsigned short lo = 0, hi = 0;
-          const int qa0 = qa + 2 * cpair;
-          if (key < Lk && qa0 < Lq) lo = *reinterpret_cast<const unsigned short*>(mcol + static_cast<long long>(qa0) * p.am_sq);
-          if (key < Lk && qa0 + 1 < Lq)
-            hi = *reinterpret_cast<const unsigned short*>(mcol + static_cast<long long>(qa0 + 1) * p.am_sq);
-          amk[cpair] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-        }
-      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, abort_flag, p.status) &&
                                        mbar_wait(&bars->full[stage], (s / C::kStages) & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv[NH], dv[NH];
+      uint32_t sv[NCH][CH], dv[NCH][CH];
 #pragma unroll
-      for (int cc = 0; cc < NH / 32; ++cc) {
-        tmem_ld32(tmem + lane_off + C::kTS + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[cc * 32]));
-        tmem_ld32(tmem + lane_off + C::kTdP + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[cc * 32]));
+      for (int cc = 0; cc < CH / 32; ++cc) {
+        tmem_ld32(tmem + lane_off + C::kTS + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[0][cc * 32]));
+        tmem_ld32(tmem + lane_off + C::kTdP + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[0][cc * 32]));
       }
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->s_free);               // the next S^T / dP^T may be written
-      const int q0 = qstep(s) * BQ + half * NH;
-      const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
-      // dropout: the 16 keys of a half-warp share one Philox call per query;
-      // lane o of the half makes the calls of columns o, o + 16, ... and the
-      // others read their byte from it with shuffles
-      uint4 rw[DROP ? NH / 16 : 1];
-      if (DROP) {
-        const int lane = threadIdx.x & 31;
-#pragma unroll
-        for (int t = 0; t < NH / 16; ++t)
-          rw[t] = philox4x32_10(make_uint4(static_cast<uint32_t>(key >> 4), static_cast<uint32_t>(q0 + (lane & 15) + 16 * t),
-                                           static_cast<uint32_t>(unit), 0u),
-                                p.seed_lo, p.seed_hi);
+      if (NCH == 1) {
+        tc_fence_before();
+        mbar_arrive(&bars->s_free);             // the next S^T / dP^T may be written
       }
-      uint32_t pk[NH / 2], dk[NH / 2];
-      // row statistics of this half's query columns (written by the producer
-      // before it arrived on full[stage])
-      const float* slf = stat + stage * 2 * BQ + half * NH;
-      // the per-element causal / length test only where the tile needs it
-      auto body = [&](auto masked) {
-        constexpr bool M = decltype(masked)::value;
+      const int qh = qstep(s) * BQ + half * NH;  // this group's first query column
 #pragma unroll
-        for (int g = 0; g < NH / 4; ++g) {
-          // loaded in program order: hoisting them costs registers and spills
-          float l4[4], d4[4];
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(l4[0]), "=f"(l4[1]), "=f"(l4[2]), "=f"(l4[3]) : "r"(smem_u32(slf + 4 * g)));
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(d4[0]), "=f"(d4[1]), "=f"(d4[2]), "=f"(d4[3]) : "r"(smem_u32(slf + BQ + 4 * g)));
-          float pr[4], ds[4];
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int q0 = qh + ch * CH;
+        const bool need_mask = (CAUSAL && q0 < key0 + BK - 1) || (key0 + BK > Lk);
+        // dropout: the 16 keys of a half-warp share one Philox block per
+        // query; lane o of the half computes the blocks of columns o and
+        // o + 16, and a byte transpose hands every lane its own bytes
+        uint32_t dw[DROP ? CH / 16 : 1][4];
+        if (DROP) {
+          const int hl = threadIdx.x & 15;
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int col = 4 * g + h;
-            float bias2 = 0.f;        // additive mask in base 2
-            if (BIAS) {
-              const float2 mf = Pack2<T>::unpack(amk[col / 2]);
-              bias2 = ((col & 1) ? mf.y : mf.x) * kLog2e;
-            }
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, bias2 - l4[h]));
-            if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
-            float zf = 1.f;           // dropout factor of (query q0 + col, key)
-            if (DROP) {
-              const int src = (col & 15) | (threadIdx.x & 16);
-              const uint32_t wx = __shfl_sync(0xffffffffu, rw[col >> 4].x, src);
-              const uint32_t wy = __shfl_sync(0xffffffffu, rw[col >> 4].y, src);
-              const uint32_t wz = __shfl_sync(0xffffffffu, rw[col >> 4].z, src);
-              const uint32_t ww = __shfl_sync(0xffffffffu, rw[col >> 4].w, src);
-              const int b = key & 15;
-              const uint32_t word = b < 8 ? (b < 4 ? wx : wy) : (b < 12 ? wz : ww);
-              zf = ((word >> (8 * (b & 3))) & 0xffu) >= p.drop_t ? p.drop_scale : 0.f;
-            }
-            pr[h] = pv * zf;
-            ds[h] = pv * (__uint_as_float(dv[col]) * zf - d4[h]);
+          for (int t = 0; t < CH / 16; ++t) {
+            const uint4 rv = philox4x32_10(make_uint4(static_cast<uint32_t>(key >> 4), static_cast<uint32_t>(q0 + hl + 16 * t),
+                                                      static_cast<uint32_t>(unit), 0u),
+                                           p.seed_lo, p.seed_hi);
+            dw[t][0] = rv.x; dw[t][1] = rv.y; dw[t][2] = rv.z; dw[t][3] = rv.w;
+            transpose16_bytes(dw[t], hl);
           }
-          pk[2 * g] = Pack2<T>::pack(pr[0], pr[1]);
-          pk[2 * g + 1] = Pack2<T>::pack(pr[2], pr[3]);
-          dk[2 * g] = Pack2<T>::pack(ds[0], ds[1]);
-          dk[2 * g + 1] = Pack2<T>::pack(ds[2], ds[3]);
         }
-      };
-      if (need_mask) body(std::true_type{});
-      else body(std::false_type{});
-      // P^T / dS^T buffers are free once the previous tile's dV, dK, dQ MMAs finished
-      if (s > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_free, (s - 1) & 1, abort_flag, p.status));
-      if (!ok) break;
-      // [key row][query] in 128-byte swizzled rows, 64 queries per column block
+        // additive mask of this chunk, staged in slot n % 2 by the mask warp
+        const int n = s * NCH + ch;
+        const T* mt = mkey + (n & 1) * (C::kMaskSlot / 2);
+        if (BIAS) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->mfull[n & 1], (n >> 1) & 1, abort_flag, p.status));
+          if (!ok) break;
+        }
+        uint32_t pk[CH / 2], dk[CH / 2];
+        // row statistics of these query columns (written by the producer
+        // before it arrived on full[stage])
+        const float* slf = stat + stage * 2 * BQ + half * NH + ch * CH;
+        // the per-element causal / length test only where the tile needs it
+        auto body = [&](auto masked) {
+          constexpr bool M = decltype(masked)::value;
 #pragma unroll
-      for (int ch = 0; ch < NH / 8; ++ch) {
-        const int chunk = half * (NH / 8) + ch;    // 8-query chunk index within the tile
-        const uint32_t off = (chunk / 8) * C::kPColBlk + r * 128 + (((chunk % 8) ^ (r & 7)) << 4);
-        st_shared_v4(sPT + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        st_shared_v4(sDST + off, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+          for (int g = 0; g < CH / 4; ++g) {
+            // loaded in program order: hoisting them costs registers and spills
+            float l4[4], d4[4];
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(l4[0]), "=f"(l4[1]), "=f"(l4[2]), "=f"(l4[3]) : "r"(smem_u32(slf + 4 * g)));
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(d4[0]), "=f"(d4[1]), "=f"(d4[2]), "=f"(d4[3]) : "r"(smem_u32(slf + BQ + 4 * g)));
+            float pr[4], ds[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int col = 4 * g + h;
+              float bias2 = 0.f;        // additive mask in base 2
+              if (BIAS) bias2 = to_f32(mt[col * BK]) * kLog2e;
+              float pv = ex2_approx(fmaf(__uint_as_float(sv[ch][col]), c, bias2 - l4[h]));
+              if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
+              float zf = 1.f;           // dropout factor of (query q0 + col, key)
+              if (DROP) {
+                const uint32_t byte = __byte_perm(dw[col >> 4][(col & 15) >> 2], 0u, 0x4440u | (col & 3));
+                zf = byte >= p.drop_t ? p.drop_scale : 0.f;
+              }
+              pr[h] = pv * zf;
+              ds[h] = pv * (__uint_as_float(dv[ch][col]) * zf - d4[h]);
+            }
+            pk[2 * g] = Pack2<T>::pack(pr[0], pr[1]);
+            pk[2 * g + 1] = Pack2<T>::pack(pr[2], pr[3]);
+            dk[2 * g] = Pack2<T>::pack(ds[0], ds[1]);
+            dk[2 * g + 1] = Pack2<T>::pack(ds[2], ds[3]);
+          }
+        };
+        if (need_mask) body(std::true_type{});
+        else body(std::false_type{});
+        if (BIAS) {
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) mbar_arrive(&bars->mempty[n & 1]);   // slot read
+        }
+        if (ch + 1 < NCH) {
+          // the next chunk's S^T / dP^T; after the last one TMEM is free
+#pragma unroll
+          for (int cc = 0; cc < CH / 32; ++cc) {
+            const int col = half * NH + (ch + 1) * CH + cc * 32;
+            tmem_ld32(tmem + lane_off + C::kTS + col, *reinterpret_cast<uint32_t(*)[32]>(&sv[ch + 1][cc * 32]));
+            tmem_ld32(tmem + lane_off + C::kTdP + col, *reinterpret_cast<uint32_t(*)[32]>(&dv[ch + 1][cc * 32]));
+          }
+          tmem_ld_wait();
+          if (ch + 1 == NCH - 1) {
+            tc_fence_before();
+            mbar_arrive(&bars->s_free);
+          }
+        }
+        // P^T / dS^T buffers are free once the previous tile's dV, dK, dQ MMAs finished
+        if (ch == 0 && s > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_free, (s - 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+        // [key row][query] in 128-byte swizzled rows, 64 queries per column block
+#pragma unroll
+        for (int c8 = 0; c8 < CH / 8; ++c8) {
+          const int chunk = half * (NH / 8) + ch * (CH / 8) + c8;   // 8-query chunk index within the tile
+          const uint32_t off = (chunk / 8) * C::kPColBlk + r * 128 + (((chunk % 8) ^ (r & 7)) << 4);
+          st_shared_v4(sPT + off, pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+          st_shared_v4(sDST + off, dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2], dk[4 * c8 + 3]);
+        }
       }
+      if (!ok) break;
       fence_proxy_async_smem();
       mbar_arrive(&bars->pds_full);
     }
@@ -617,12 +714,13 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
   auto kern = bwd_tc_kernel<D, T, CAUSAL, PACKED, EXT>;
+  using C = BCfg<D, EXT>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     // setmaxnreg redistributes the registers the block is launched with; a
     // split larger than that would wait forever, so refuse to launch instead
@@ -644,7 +742,7 @@ cudaError_t launch_one(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
   constexpr long long kL2Budget = 48ll << 20;
   const long long unit_bytes = static_cast<long long>(p.cu_seqlens ? p.max_q : p.Lq) * D * 8;
   g.group = p.causal ? static_cast<int>(std::max(1ll, std::min(units, kL2Budget / std::max(1ll, unit_bytes)))) : 1;
-  kern<<<static_cast<unsigned>(blocks), kThreads, BCfg<D>::kSmem, s>>>(g, m.q, m.k, m.v, m.dO);
+  kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmem, s>>>(g, m.q, m.k, m.v, m.dO, m.mask);
   return cudaGetLastError();
 }
 

@@ -76,6 +76,7 @@ struct FwdMaps {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO;
+  CUtensorMap mask;   // additive mask [B|1][H|1][Lq][Lk], 32 x 128 boxes (masked backward only)
 };
 
 // Records the message sdpa_last_error() returns on this thread; returns `code`.

@@ -89,6 +89,22 @@ def test_masked_broadcast_and_d32_forward(causal):
     _check_fwd(got, _oracle(x, mask, Lk, causal, 0.2, bwd=False), "f16")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mshape", ["hqk", "qk", "b1qk"])
+def test_masked_broadcast_bwd(d, mshape):
+    """Masks shared across the batch ([H, Lq, Lk]), across everything
+    ([Lq, Lk]) or across heads ([B, 1, Lq, Lk]) through the backward."""
+    from _gpu import assert_grads_close
+    B, H, Lq, Lk = 2, 3, 200, 260
+    x = wl.dense_inputs(B, H, Lq, Lk, d, "bf16", "normal", seed=58)
+    shape = {"hqk": (H, Lq, Lk), "qk": (Lq, Lk), "b1qk": (B, 1, Lq, Lk)}[mshape]
+    mask = wl.attn_mask(shape, "bf16", seed=59, empty_rows=(5,))
+    got = _run(x, mask, Lk, False, 0.125)
+    ref = _oracle(x, mask, Lk, False, 0.125)
+    _check_fwd(got[:2], ref[:2], "bf16")
+    assert_grads_close(got[2:], ref[2:], "bf16")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_masked_f32(causal):
     from _gpu import assert_grads_close
