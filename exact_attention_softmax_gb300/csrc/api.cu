@@ -97,10 +97,11 @@ int make_operand_map(CUtensorMap* m, const void* base, int dtype, bool packed, i
 
 // Map over an additive mask with element strides (sb, sh, sq): dims {Lk, Lq,
 // H, B}, a batch or head stride of 0 (broadcast) becomes a dimension of size
-// 1; boxes of 32 query rows x 128 keys, unswizzled. Reads past Lk or Lq fill
+// 1; boxes of `box_rows` query rows x `box_keys` keys, 128-byte swizzled when
+// a box row is 128 bytes (64 keys), else unswizzled. Reads past Lk or Lq fill
 // zeros, so no padding of the rows is read.
 int make_mask_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int Lq, int Lk, long long sb, long long sh,
-                  long long sq) {
+                  long long sq, uint32_t box_keys, uint32_t box_rows) {
   const uint64_t es = 2;
   const uint64_t nh = sh ? static_cast<uint64_t>(H) : 1, nb = sb ? static_cast<uint64_t>(B) : 1;
   const uint64_t rs = static_cast<uint64_t>(sq) * es;
@@ -108,12 +109,13 @@ int make_mask_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int
   const uint64_t bs = sb ? static_cast<uint64_t>(sb) * es : hs * nh;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(Lk), static_cast<cuuint64_t>(Lq), nh, nb};
   const cuuint64_t strides[3] = {rs, hs, bs};
-  const cuuint32_t box[4] = {128, 32, 1, 1};
+  const cuuint32_t box[4] = {box_keys, box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt =
       dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw = box_keys * es == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the attention mask (CUresult %d)", static_cast<int>(r));
   return SDPA_OK;
@@ -284,10 +286,15 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
   rc = get_encoder();
   if (rc != SDPA_OK) return rc;
   const bool packed = sh.packed();
-  FwdMaps maps;
+  FwdMaps maps{};
   if ((rc = make_operand_map(&maps.q, q, dtype, packed, sh.B, sh.H, sh.total_q, sh.d)) != SDPA_OK) return rc;
   if ((rc = make_operand_map(&maps.k, k, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
   if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
+  // additive mask: each softmax warp loads its 32 rows of a 128-key block as two 64-key boxes
+  if (masked &&
+      (rc = make_mask_map(&maps.mask, am.m, dtype, sh.B, sh.H, sh.total_q, sh.total_k, am.sb, am.sh, am.sq, 64, 32)) !=
+          SDPA_OK)
+    return rc;
   e = launch_fwd_tc(p, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "forward (tensor-core) launch");
   return SDPA_OK;
@@ -345,7 +352,8 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
   if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
   if ((rc = make_operand_map(&maps.dO, dO, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, bq)) != SDPA_OK) return rc;
   if (masked &&
-      (rc = make_mask_map(&maps.mask, am.m, dtype, sh.B, sh.H, sh.total_q, sh.total_k, am.sb, am.sh, am.sq)) != SDPA_OK)
+      (rc = make_mask_map(&maps.mask, am.m, dtype, sh.B, sh.H, sh.total_q, sh.total_k, am.sb, am.sh, am.sq, 128, 32)) !=
+          SDPA_OK)
     return rc;
   e = launch_bwd_tc(bp, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward (tensor-core) launch");

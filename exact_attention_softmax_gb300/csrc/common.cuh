@@ -73,6 +73,7 @@ struct BwdProblem {
 // Tensor maps for the tensor-core kernels (built on the host by the C-ABI layer).
 struct FwdMaps {
   CUtensorMap q, k, v;
+  CUtensorMap mask;   // additive mask [B|1][H|1][Lq][Lk], 32 x 64 swizzled boxes (masked forward only)
 };
 struct BwdMaps {
   CUtensorMap q, k, v, dO;

@@ -61,7 +61,7 @@ constexpr int kSchedSlots = 1024;
 __device__ unsigned g_fwd_sched[2 * kSchedSlots];
 constexpr int kItemQueue = 4;
 
-template <int D>
+template <int D, int EXT = 0>
 struct Cfg {
   static constexpr int kBlk = D >= 64 ? 64 : D;             // elements per swizzled row
   static constexpr int kNBlk = D / kBlk;                      // column blocks per tile
@@ -73,11 +73,16 @@ struct Cfg {
   // Q tiles are double-buffered where each CTA runs many work items (d <= 64),
   // so the next item's Q and K/V stream in while the current item finishes.
   static constexpr int kQBufs = D == 128 ? 1 : 2;
-  static constexpr int kSlots = D == 128 ? 5 : (D == 64 ? 10 : 16);
+  // The additive-mask kernel gives up K/V ring slots at d >= 64 for its mask
+  // slots: one 32-row x 128-key slot per softmax warp (two 64-key boxes).
+  static constexpr bool kMask = EXT == 2;
+  static constexpr int kSlots = D == 128 ? (kMask ? 3 : 5) : (D == 64 ? (kMask ? 6 : 10) : 16);
   static constexpr int kOffQ = 0;
   static constexpr int kOffSlots = 2 * kQBufs * kTileBytes;
-  static constexpr int kOffBar = kOffSlots + kSlots * kTileBytes;
-  static constexpr int kSmem = kOffBar + 512 + 1024;          // barriers + alignment slack
+  static constexpr int kMaskWarpBytes = 32 * BN * 2;
+  static constexpr int kOffMask = kOffSlots + kSlots * kTileBytes;
+  static constexpr int kOffBar = kOffMask + (kMask ? 8 * kMaskWarpBytes : 0);
+  static constexpr int kSmem = kOffBar + 640 + 1024;          // barriers + alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   // TMEM columns. P (BN fp16/bf16 per row, two per 32-bit column) has its own
   // columns when they fit; at d = 128 it overlays the upper half of S_t, which
@@ -109,6 +114,7 @@ struct __align__(8) Bars {
   uint64_t p_full[2];     // P_t in TMEM (and O_t rescaled)
   uint64_t pv_done[2];    // O_t += P_t V_j finished
   uint64_t o_free[2];     // O_t read out by the epilogue: the next item may overwrite it
+  uint64_t mfull[8];      // additive mask: softmax warp w's slot loaded
   uint64_t item_full[4];  // work-item queue from the producer to the other roles
   uint64_t item_empty[4];
   int item[4];
@@ -116,6 +122,7 @@ struct __align__(8) Bars {
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+static_assert(sizeof(Bars) <= 640, "the barrier block has 640 bytes of shared memory");
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float m;
@@ -203,6 +210,9 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
   } else {
     it.len_q = p.Lq;
     it.len_k = p.Lk;
+    // an additive mask shared across the batch: the units of one head run
+    // side by side, so the rows of its mask they all read come from L2
+    if (p.amask != nullptr && p.am_sb == 0 && p.am_sh != 0 && p.B > 1) it.unit = (it.unit % p.B) * p.H + it.unit / p.B;
   }
   it.r0 = pair * 2 * BM;
   it.n0 = tile_blocks<CAUSAL>(it.r0, it.len_q, it.len_k);
@@ -240,8 +250,8 @@ template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-              unsigned* sched) {
-  using C = Cfg<D>;
+              const __grid_constant__ CUtensorMap tmM, unsigned* sched) {
+  using C = Cfg<D, EXT>;
   constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -276,6 +286,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       mbar_init(&bars->item_empty[i], 8 + C::kMmaWarps);   // one arrival per consuming warp
     }
     mbar_init(&bars->done, C::kMmaWarps);
+    for (int w = 0; w < 8; ++w) mbar_init(&bars->mfull[w], 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -571,6 +582,23 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         p.lse[e.li] = e.l > 0.f ? (e.m + __log2f(e.l)) * kLn2 : -INFINITY;
       }
     };
+    // Additive mask: each warp loads its own 32 rows x BN keys of a block
+    // with TMA into its slot (mcons loads consumed, missued issued so far).
+    int mcons = 0, missued = 0;
+    auto issue_mask = [&](const Item& x, int kb) {
+      // the slot's previous contents have been read by every lane
+      __syncwarp();
+      fence_proxy_async_smem();
+      if (lane == 0) {
+        uint8_t* dst = smem + C::kOffMask + warp * C::kMaskWarpBytes;
+        const int zc = p.am_sh ? x.unit % p.H : 0, wc = p.am_sb ? x.unit / p.H : 0;
+        const int r0w = x.r0 + t * BM + (warp & 3) * 32;     // this warp's first row within the unit
+        mbar_expect_tx(&bars->mfull[warp], C::kMaskWarpBytes);
+        for (int h = 0; h < 2; ++h)
+          tma_load_4d(dst + h * (C::kMaskWarpBytes / 2), &tmM, &bars->mfull[warp], kb + h * (BN / 2), r0w, zc, wc);
+      }
+      ++missued;
+    };
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int q = k % kItemQueue;
@@ -596,23 +624,26 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       }
       constexpr bool sparse = SPARSE;
       const unsigned char* mine = t == 0 ? it.m0 : it.m1;
+      if (BIAS) issue_mask(it, 0);           // the item's first mask block
       int jk = -1;                           // key block of the current loaded block
       float m_run = -INFINITY, l = 0.f;      // maximum used in the exponent (base 2), running sum
       for (int j = 0; j < nt; ++j) {
         const int g = blocks + j;
         jk = sparse ? next_loaded(it, jk + 1) : j;
         const int kbase = jk * BN;
-        // additive mask: this row's BN entries, loaded before the S wait so the
-        // load overlaps it (rows of 8 entries; the row stride is padded to 8, so
-        // a chunk that starts before len_k stays inside the row)
+        // additive mask: this row's BN entries from the warp's slot (two
+        // 64-key boxes, 128-byte swizzled: 16-byte chunk c of row r sits at
+        // chunk c ^ (r % 8)); once read, the slot takes the next block's mask,
+        // which lands while this block computes
         uint4 am[BIAS ? BN / 8 : 1];
         if (BIAS) {
-          const T* mrow = static_cast<const T*>(p.amask) + (it.unit / p.H) * p.am_sb + (it.unit % p.H) * p.am_sh +
-                          static_cast<long long>(row) * p.am_sq + kbase;
+          if (!(ok = wait_all(&bars->mfull[warp], mcons & 1))) break;
+          ++mcons;
+          const uint8_t* ms = smem + C::kOffMask + warp * C::kMaskWarpBytes + lane * 128;
 #pragma unroll
           for (int u = 0; u < BN / 8; ++u)
-            am[u] = (row < it.len_q && kbase + 8 * u < it.len_k) ? *reinterpret_cast<const uint4*>(mrow + 8 * u)
-                                                                 : make_uint4(0u, 0u, 0u, 0u);
+            am[u] = *reinterpret_cast<const uint4*>(ms + (u / 8) * (C::kMaskWarpBytes / 2) + (((u % 8) ^ (lane & 7)) << 4));
+          if (j + 1 < nt) issue_mask(it, kbase + BN);
         }
         if (!(ok = wait_all(&bars->s_full[t], g & 1))) break;
         tc_fence_after();
@@ -802,6 +833,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       }
     }
     if (ok && pend.on && wait_all(&bars->pv_done[t], (blocks - 1) & 1)) epilogue(pend);
+    // after a failed wait, let a mask load still in flight land before the
+    // CTA's shared memory is released
+    if (BIAS && missued > mcons && lane == 0) mbar_wait_drain(&bars->mfull[warp], mcons & 1);
   }
 
   tc_fence_before();
@@ -820,7 +854,7 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, EXT>::kSmem);
     if (e != cudaSuccess) return e;
     // setmaxnreg redistributes the registers the block is launched with; a
     // split larger than that would wait forever, so refuse to launch instead
@@ -857,7 +891,7 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
   }
   static std::atomic<unsigned> launches{0};
   unsigned* sched = sched_base[dev] + 2 * (launches.fetch_add(1) % kSchedSlots);
-  kern<<<grid, Cfg<D>::kThreads, Cfg<D>::kSmem, s>>>(p, m.q, m.k, m.v, sched);
+  kern<<<grid, Cfg<D>::kThreads, Cfg<D, EXT>::kSmem, s>>>(p, m.q, m.k, m.v, m.mask, sched);
   return cudaGetLastError();
 }
 
