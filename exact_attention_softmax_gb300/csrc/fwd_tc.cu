@@ -659,15 +659,17 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         }
         float* x = reinterpret_cast<float*>(sr);
         if (BIAS) {
-          // x = S * scale * log2(e) + M * log2(e): the exponent in base 2
+          // x = S * scale + M, the exponent in natural-log units; the max and
+          // the exponentials below scale it by log2(e) like they scale S by
+          // scale * log2(e) without a mask
 #pragma unroll
           for (int u = 0; u < BN / 8; ++u) {
             const uint32_t w[4] = {am[u].x, am[u].y, am[u].z, am[u].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 mf = Pack2<T>::unpack(w[e]);
-              x[8 * u + 2 * e] = fmaf(x[8 * u + 2 * e], c, mf.x * kLog2e);
-              x[8 * u + 2 * e + 1] = fmaf(x[8 * u + 2 * e + 1], c, mf.y * kLog2e);
+              x[8 * u + 2 * e] = fmaf(x[8 * u + 2 * e], p.scale, mf.x);
+              x[8 * u + 2 * e + 1] = fmaf(x[8 * u + 2 * e + 1], p.scale, mf.y);
             }
           }
         }
@@ -690,7 +692,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             float e[8];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], BIAS ? 1.f : c, -mu);
+              fma2(e[2 * u], e[2 * u + 1], xc[2 * u], xc[2 * u + 1], BIAS ? kLog2e : c, -mu);
               e[2 * u] = ex2_approx(e[2 * u]);
               e[2 * u + 1] = ex2_approx(e[2 * u + 1]);
             }
@@ -774,7 +776,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           }
           mx0 = max3f(mx0, x[BN - 4], x[BN - 3]);
           mx1 = max3f(mx1, x[BN - 2], x[BN - 1]);
-          const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * (BIAS ? 1.f : c);
+          const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3)) * (BIAS ? kLog2e : c);
           grow = mx > m_run + kRescaleThreshold;
           m_new = grow ? mx : m_run;
           const float m_use = m_new == -INFINITY ? 0.f : m_new;
