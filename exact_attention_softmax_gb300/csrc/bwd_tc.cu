@@ -617,9 +617,15 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               const int col = 4 * g + h;
-              float bias2 = 0.f;        // additive mask in base 2
-              if (BIAS) bias2 = to_f32(mt[col * BK]) * kLog2e;
-              float pv = ex2_approx(fmaf(__uint_as_float(sv[ch][col]), c, bias2 - l4[h]));
+              // P = 2^(S * scale * log2(e) - LSE2); with a mask S * scale + M
+              // is formed first, in natural-log units. (The plain d = 64
+              // kernels keep the addend as a subtraction: with the negated
+              // operand ptxas spills there and they measured slower.)
+              const float s_ = __uint_as_float(sv[ch][col]);
+              float pv;
+              if (BIAS) pv = ex2_approx(fmaf(fmaf(s_, p.scale, to_f32(mt[col * BK])), kLog2e, -l4[h]));
+              else if (D == 128 || DROP) pv = ex2_approx(fmaf(s_, c, -l4[h]));
+              else pv = ex2_approx(fmaf(s_, c, 0.f - l4[h]));
               if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
               float zf = 1.f;           // dropout factor of (query q0 + col, key)
               if (DROP) {
