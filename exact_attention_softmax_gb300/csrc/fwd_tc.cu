@@ -187,12 +187,15 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
   Item it;
   // Causal items get shorter with their query position, so they are handed
   // out longest first across all units (ord-major), which keeps the last
-  // CTAs to finish from starting long items late; without masking every item
-  // costs the same and the units are taken one after another.
+  // CTAs to finish from starting long items late. Packed batches go the same
+  // way: only long sequences have items at high query positions, and those
+  // items are the longest. Dense items without masking all cost the same and
+  // the units are taken one after another.
   const int units = p.B * p.H;
-  it.unit = CAUSAL ? idx % units : idx / npairs;
-  const int ord = CAUSAL ? idx / units : idx % npairs;
-  const int pair = CAUSAL ? (npairs - 1 - ord) : ord;
+  constexpr bool kOrdMajor = CAUSAL || PACKED;
+  it.unit = kOrdMajor ? idx % units : idx / npairs;
+  const int ord = kOrdMajor ? idx / units : idx % npairs;
+  const int pair = kOrdMajor ? (npairs - 1 - ord) : ord;
   it.h = 0;
   it.tok0 = it.tok0k = 0;
   if (PACKED) {
