@@ -292,8 +292,9 @@ def _attn_mask_args(attn_mask, q, Lq, Lk):
 def sdpa_fwd_masked(q, k, v, attn_mask, o=None, lse=None, *, scale=None, is_causal=False, stream=None):
     """Forward with an additive mask: ``softmax(scale * Q K^T + attn_mask) V``
     (dense [B,H,L,d]; -inf entries exclude a score). For fp16/bf16 the mask's
-    row stride must be a multiple of 8 elements and at least Lk rounded up to
-    8 (pad the key axis). Rows with no visible key get O = 0, LSE = -inf."""
+    base must be 16-byte aligned and its strides multiples of 8 elements
+    (pad the key axis to a multiple of 8; the padding is never read). Rows
+    with no visible key get O = 0, LSE = -inf."""
     import torch
     lib = _abi.load()
     if q.dim() != 4:

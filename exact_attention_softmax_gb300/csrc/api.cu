@@ -169,7 +169,7 @@ int check_addmask(const Shape& sh, const AddMask& am, int dtype) {
   if (am.sb < 0 || am.sh < 0 || am.sq < sh.total_k)
     return fail(SDPA_ERR_ARG, "attention mask strides must be non-negative and the row stride at least Lk = %d", sh.total_k);
   if (dtype != SDPA_F32) {
-    // rows are read 8 entries (16 bytes) at a time
+    // the tensor-core kernels read the mask with TMA: 16-byte aligned base and strides
     const long long lk8 = (sh.total_k + 7) / 8 * 8;
     if (!aligned16(am.m) || am.sq % 8 != 0 || am.sb % 8 != 0 || am.sh % 8 != 0 || am.sq < lk8)
       return fail(SDPA_ERR_ARG, "fp16/bf16 attention masks need a 16-byte aligned base, strides that are multiples of 8 "

@@ -195,10 +195,11 @@ int sdpa_bwd_blocksparse(const void* q, const void* k, const void* v, const void
  *               + i * mask_stride_row + j] for i < Lq, j < Lk (keys
  *               contiguous). Strides are in elements; 0 broadcasts over the
  *               batch or the heads. Entries are finite or -inf (-inf excludes
- *               the score). fp16/bf16: the base must be 16-byte aligned, the
- *               strides multiples of 8 and mask_stride_row at least Lk rounded
- *               up to 8 (rows are read 8 entries at a time); fp32: row stride
- *               at least Lk.
+ *               the score). fp16/bf16: the base must be 16-byte aligned and
+ *               the strides multiples of 8 elements (the tensor-core kernels
+ *               read the mask with TMA), so mask_stride_row is at least Lk
+ *               rounded up to 8; entries past Lk are never read. fp32: row
+ *               stride at least Lk.
  *   A query row with no visible key gets O = 0 and LSE = -inf, and no gradient.
  * LSE is the log-sum-exp of the masked scores. Other arguments, support and
  * errors as for sdpa_fwd with cu_seqlens = NULL.
