@@ -634,6 +634,32 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         const int g = blocks + j;
         jk = sparse ? next_loaded(it, jk + 1) : j;
         const int kbase = jk * BN;
+        if (sparse && !mine[jk]) {
+          // A loaded block this tile's mask row drops: its probabilities are
+          // all 0, so P_t = 0 goes to the tensor cores with the same handshakes
+          // as any block, and the max, exponentials and rescale are skipped.
+          if (!(ok = wait_all(&bars->s_full[t], g & 1))) break;
+          if (!C::kPAlias) {
+            tc_fence_before();
+            mbar_arrive(&bars->s_free[t]);
+          }
+          // P_t's columns are free once the previous P.V on this tile has finished
+          if (!C::kPAlias && (j > 0 || pend.on) && !(ok = wait_all(&bars->pv_done[t], (g - 1) & 1))) break;
+          tc_fence_after();
+          uint32_t zero[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) zero[i] = 0u;
+          tmem_st32(tP, zero);
+          tmem_st32(tP + 32, zero);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full[t]);
+          if (kDefer && j == 0 && pend.on) {
+            epilogue(pend);
+            pend.on = false;
+          }
+          continue;
+        }
         // additive mask: this row's BN entries from the warp's slot (two
         // 64-key boxes, 128-byte swizzled: 16-byte chunk c of row r sits at
         // chunk c ^ (r % 8)); once read, the slot takes the next block's mask,
@@ -676,11 +702,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             }
           }
         }
-        // block-sparse: a loaded block this tile's mask row drops is masked whole
-        const bool drop = sparse && !mine[jk];
-        if (drop || (kbase + BN > it.len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
+        if ((kbase + BN > it.len_k) || (CAUSAL && kbase + BN - 1 > rt)) {
           // keys kbase + i with i >= lim are past the end or (causal) after the row
-          const int lim = drop ? 0 : (CAUSAL ? min(it.len_k, row + 1) : it.len_k) - kbase;
+          const int lim = (CAUSAL ? min(it.len_k, row + 1) : it.len_k) - kbase;
 #pragma unroll
           for (int i = 0; i < BN; ++i) x[i] = i < lim ? x[i] : -INFINITY;
         }

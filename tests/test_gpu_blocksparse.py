@@ -108,6 +108,24 @@ def test_blocksparse_f32(causal):
     assert_grads_close(got[2:], ref[2:], "f32")
 
 
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocksparse_many_items_per_cta(d, causal):
+    """More work items than SMs, so each persistent CTA runs several items in
+    a row while its tiles drop some of their pair's loaded blocks: the path
+    that carries barrier phases and the deferred epilogue from one item into
+    the next. Sampled (batch, head) units against the oracle."""
+    B, H, L = 8, 24, 1024          # 192 units x 2 items of 256 rows
+    scale = d ** -0.5
+    x = wl.dense_inputs(B, H, L, L, d, "f16", "normal", seed=48, with_do=False)
+    mask = wl.block_mask((B, H, _nb(L), _nb(L)), 0.5, seed=49)
+    got = _run(x, mask, causal, scale, bwd=False)
+    for b, h in [(0, 0), (3, 7), (7, 23)]:
+        sub = {n: x[n][b:b + 1, h:h + 1] for n in ("q", "k", "v")}
+        ref = _oracle(sub, mask[b:b + 1, h:h + 1], causal, scale, bwd=False)
+        _check_fwd((got[0][b:b + 1, h:h + 1], got[1][b:b + 1, h:h + 1]), ref, "f16")
+
+
 def test_all_ones_mask_matches_dense_call():
     """With every tile kept the block-sparse forward gives the dense call's
     results bit for bit (same blocks, same order)."""
