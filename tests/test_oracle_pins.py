@@ -403,6 +403,30 @@ def test_additive_mask_special_cases():
     np.testing.assert_allclose(lse, lse2, atol=1e-14)
 
 
+def test_additive_mask_broadcast_axes():
+    """A mask shared across the batch ([H, Lq, Lk]) or across heads
+    ([B, 1, Lq, Lk]) reaches unit (b, h) as its own slice: each unit of the
+    batched result equals a single-unit call with that slice, so a mask
+    aligned against the wrong axis fails."""
+    B, H, lq, lk, d = 2, 3, 5, 6, 4
+    q, k, v, do = rnd(B, H, lq, d, seed=81), rnd(B, H, lk, d, seed=82), rnd(B, H, lk, d, seed=83), rnd(B, H, lq, d, seed=84)
+    per_head = rnd(H, lq, lk, seed=85)
+    per_batch = rnd(B, 1, lq, lk, seed=86)
+    for mask, pick in ((per_head, lambda b, h: per_head[h]), (per_batch, lambda b, h: per_batch[b, 0])):
+        full = attn_fwd_ref(q, k, v, 0.7, False, attn_mask=mask) + attn_bwd_ref(q, k, v, do, 0.7, False, attn_mask=mask)
+        for b in range(B):
+            for h in range(H):
+                one = (attn_fwd_ref(q[b, h][None], k[b, h][None], v[b, h][None], 0.7, False, attn_mask=pick(b, h))
+                       + attn_bwd_ref(q[b, h][None], k[b, h][None], v[b, h][None], do[b, h][None], 0.7, False,
+                                      attn_mask=pick(b, h)))
+                for a, r in zip(full, one):
+                    np.testing.assert_allclose(a[b, h], r[0], rtol=0, atol=1e-13)
+    # and the two layouts differ, so the check above can tell them apart
+    a = attn_fwd_ref(q, k, v, 0.7, False, attn_mask=per_head)[0]
+    c = attn_fwd_ref(q, k, v, 0.7, False, attn_mask=per_batch)[0]
+    assert np.max(np.abs(a - c)) > 1e-3
+
+
 def test_additive_mask_backward_finite_differences():
     lq, lk, d = 4, 5, 3
     q, k, v, do = rnd(lq, d, seed=81), rnd(lk, d, seed=82), rnd(lk, d, seed=83), rnd(lq, d, seed=84)
