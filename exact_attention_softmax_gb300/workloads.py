@@ -183,8 +183,9 @@ def attn_mask(shape, dtype="f16", seed: int = 0, neg_inf: float = 0.1, empty_row
     """Seeded additive mask [..., Lq, Lk]: N(0,1) entries, a fraction
     ``neg_inf`` of them -inf, the rows in ``empty_rows`` entirely -inf. Returned
     with the key axis padded to a multiple of ``pad_to`` ([..., Lq, Lk_padded];
-    take ``[..., :Lk]`` after moving it to the device to keep the padded row
-    stride the fp16/bf16 kernels read 8 entries at a time from)."""
+    take ``[..., :Lk]`` after moving it to the device, so the row stride stays
+    a multiple of 8 entries, as the fp16/bf16 kernels' TMA reads of the mask
+    need)."""
     g = torch.Generator("cpu").manual_seed(seed)
     *lead, lq, lk = shape
     lkp = (lk + pad_to - 1) // pad_to * pad_to
