@@ -63,6 +63,8 @@ def _geometry(q, k, cu_seqlens, max_seqlen):
 
 
 def _check_tensors(ts, dev, dt):
+    if dev.type != "cuda":
+        raise ValueError(f"q is on {dev}: the attention ops take CUDA tensors only (there is no CPU implementation)")
     for name, t in ts.items():
         if t is None:
             continue

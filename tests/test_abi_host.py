@@ -145,3 +145,18 @@ def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_abi, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         _abi.load(str(tmp_path / "nope.so"))
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    """Every op takes CUDA tensors only: CPU tensors are refused with a clear
+    error before any call reaches the library (there is no CPU implementation)."""
+    import torch
+    import exact_attention_softmax_gb300 as ops
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        ops.sdpa_fwd(q, q, q)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        ops.sdpa_fwd_dropout(q, q, q, 0.1, 7)
+    lse = torch.zeros(1, 1, 8)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        ops.sdpa_bwd(q, q, q, q, lse, q)
