@@ -44,7 +44,9 @@ row left with no finite score is empty as above.
 
 Dropout (the tutorial's ``dropout_p`` argument of the same call): the
 probabilities, not the normaliser, are dropped; O = (P * Z) V with Z = 0 for a
-dropped score and 1/(1-p) for a kept one, and LSE that of the full softmax.
+dropped score and 1/(1 - t/256) for a kept one, where t = round(256 p) is the
+byte threshold of the keep test (so the realised drop rate is t/256, which
+equals p when p is a multiple of 1/256), and LSE that of the full softmax.
 The keep pattern comes from Philox4x32-10 (``oracle/philox.py``).
 
 Layouts: dense tensors are ``[..., L, d]`` (any leading batch/head dims, the

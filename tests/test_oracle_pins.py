@@ -460,6 +460,64 @@ def test_philox_known_answers():
         assert [f"{int(w):08x}" for w in out] == vec["output"]
 
 
+def _philox_scalar(ctr, key):
+    """Philox4x32-10 for one counter, in plain Python integers: a second
+    statement of the SC 2011 generator (ten rounds; each multiplies counter
+    words 0 and 2 by 0xD2511F53 and 0xCD9E8D57, splits the 64-bit products
+    into high and low words, and xors the high words with the other two
+    counter words and the round key; the key advances by 0x9E3779B9 and
+    0xBB67AE85 after every round but the last)."""
+    x0, x1, x2, x3 = ctr
+    k0, k1 = key
+    for rnd_ in range(10):
+        p0, p1 = 0xD2511F53 * x0, 0xCD9E8D57 * x2
+        x0, x1, x2, x3 = ((p1 >> 32) ^ x1 ^ k0, p1 & 0xFFFFFFFF, (p0 >> 32) ^ x3 ^ k1, p0 & 0xFFFFFFFF)
+        if rnd_ < 9:
+            k0, k1 = (k0 + 0x9E3779B9) & 0xFFFFFFFF, (k1 + 0xBB67AE85) & 0xFFFFFFFF
+    return x0, x1, x2, x3
+
+
+def test_scalar_philox_known_answers():
+    kat = json.load(open(os.path.join(HERE, "golden", "philox_kat.json")))
+    for vec in kat["vectors"]:
+        out = _philox_scalar([int(x, 16) for x in vec["counter"]], [int(x, 16) for x in vec["key"]])
+        assert [f"{w:08x}" for w in out] == vec["output"]
+
+
+def test_dropout_keep_bytes_from_published_vector():
+    """Keep bits read by hand off Random123's first vector (counter 0, key 0):
+    byte order within a word, the >= comparison and t = round(256 p)."""
+    g = json.load(open(os.path.join(HERE, "golden", "dropout_keep_kat.json")))
+    for case in g["cases"]:
+        p = case["t"] / 256.0
+        assert dropout_threshold(p) == case["t"]
+        keep = dropout_keep(g["seed"], g["unit"], 1, 16, p)[0]
+        assert keep.astype(int).tolist() == case["keep"], case["why"]
+
+
+@pytest.mark.parametrize("seed", [0, 0x9E3779B97F4A7C15, (5 << 32) | 7])
+def test_dropout_keep_one_counter_at_a_time(seed):
+    """The vectorised keep mask against an explicit loop: for each score
+    (i, j) of unit u, one Philox call at counter (j // 16, i, u, 0) with key
+    (seed mod 2^32, seed div 2^32), then byte j mod 16 taken by shifting the
+    word j mod 16 div 4 right by 8 (j mod 4) bits. Keys cross the 16- and
+    32-key counter steps; rows and units differ so a swapped counter word or
+    key word shows."""
+    lq, lk, t = 5, 41, 77
+    key = (seed & 0xFFFFFFFF, seed >> 32)
+    for u in (0, 3):
+        got = dropout_keep(seed, u, lq, lk, t / 256.0)
+        want = np.zeros((lq, lk), dtype=bool)
+        for i in range(lq):
+            for j in range(lk):
+                words = _philox_scalar((j // 16, i, u, 0), key)
+                byte = (words[(j % 16) // 4] >> (8 * (j % 4))) & 0xFF
+                want[i, j] = byte >= t
+        assert np.array_equal(got, want)
+    # the unit and the row are different counter words
+    assert not np.array_equal(dropout_keep(seed, 1, 2, 32, 0.5)[0], dropout_keep(seed, 0, 2, 32, 0.5)[1])
+
+
 def test_dropout_keep_rate_and_independence():
     for p in (0.1, 0.5, 0.9):
         keep = dropout_keep(1234, 3, 256, 512, p)
@@ -677,3 +735,28 @@ def test_bruteforce_catches_planted_mask_mistake():
     p /= p.sum(1, keepdims=True)
     ob, _ = fwd_bruteforce(q.tolist(), k.tolist(), v.tolist(), 0.5, True)
     assert np.max(np.abs(p @ v - np.array(ob))) > 1e-3
+
+
+def _keep_variant(seed, unit, lq, lk, t, order="<u4", counter=lambda g, i, u: (g, i, u, 0), cmp=np.greater_equal):
+    """A copy of the keep-mask construction with one planted change."""
+    groups = -(-lk // 16)
+    ctr = np.array([[counter(g, i, unit) for g in range(groups)] for i in range(lq)], dtype=np.uint32)
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], dtype=np.uint32)
+    words = philox4x32_10(ctr, key).astype(np.uint32)
+    by = words.astype(order).view(np.uint8).reshape(lq, groups * 16)[:, :lk]
+    return cmp(by, t)
+
+
+def test_dropout_pins_catch_planted_mistakes():
+    g = json.load(open(os.path.join(HERE, "golden", "dropout_keep_kat.json")))
+    # the unchanged copy passes both pins
+    for case in g["cases"]:
+        assert _keep_variant(0, 0, 1, 16, case["t"])[0].astype(int).tolist() == case["keep"]
+    # big-endian bytes, and > instead of >=: the published-vector bytes catch them
+    caught = [any(_keep_variant(0, 0, 1, 16, c["t"], **kw)[0].astype(int).tolist() != c["keep"] for c in g["cases"])
+              for kw in (dict(order=">u4"), dict(cmp=np.greater))]
+    assert all(caught)
+    # row and unit swapped in the counter: the one-counter-at-a-time loop catches it
+    seed = (5 << 32) | 7
+    wrong = _keep_variant(seed, 3, 5, 41, 77, counter=lambda g_, i, u: (g_, u, i, 0))
+    assert not np.array_equal(wrong, dropout_keep(seed, 3, 5, 41, 77 / 256.0))
