@@ -115,7 +115,7 @@ def test_blocksparse_many_items_per_cta(d, causal):
     a row while its tiles drop some of their pair's loaded blocks: the path
     that carries barrier phases and the deferred epilogue from one item into
     the next. Sampled (batch, head) units against the oracle."""
-    B, H, L = 8, 24, 1024          # 192 units x 2 items of 256 rows
+    B, H, L = 8, 24, 1024          # 192 units x 4 items of 256 rows: 768 items on at most 152 CTAs
     scale = d ** -0.5
     x = wl.dense_inputs(B, H, L, L, d, "f16", "normal", seed=48, with_do=False)
     mask = wl.block_mask((B, H, _nb(L), _nb(L)), 0.5, seed=49)
