@@ -10,16 +10,19 @@
 // it from a fixed array compiled into the library instead of asking the
 // caller for one.
 //
-// The scratch is a file-scope device array of kNoAllocScratchBytes. Every GPU
-// that loads the library keeps it until the process exits. Host code only
+// The scratch is a file-scope device array of kNoAllocScratchBytes, held on
+// every GPU where it has been loaded until the process exits. Host code only
 // sees a host-side stand-in under the array's name, so the device address is
 // looked up with cudaGetSymbolAddress once per device, on the first call made
-// while that device is current; that first call should therefore come before
-// any stream capture. All calls share the one array and it keeps whatever the
-// last call left in it: the backward's prep kernel rewrites D and zeroes the
-// dQ accumulator at the start of every call, so nothing carries over between
-// calls, but two calls whose kernels overlap on the GPU (different streams,
-// no ordering between them) race on the array and give wrong gradients.
+// while that device is current. Under CUDA's lazy module loading that lookup
+// is also what loads this file's device module, and with it the 16 MiB, onto
+// the device: callers on a fixed memory budget make that first call at
+// start-up, and before any stream capture. All calls share the one array and
+// it keeps whatever the last call left in it: the backward's prep kernel
+// rewrites D and zeroes the dQ accumulator at the start of every call, so
+// nothing carries over between calls, but two calls whose kernels overlap on
+// the GPU (different streams, no ordering between them) race on the array and
+// give wrong gradients.
 #include "common.cuh"
 #include "sdpa.h"
 
@@ -57,8 +60,10 @@ extern "C" int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, con
     // set-up, once per device, with that device current
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || ptr == nullptr)
+    if (e != cudaSuccess)
       return set_last_error(SDPA_ERR_CUDA, "sdpa_bwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    if (ptr == nullptr)
+      return set_last_error(SDPA_ERR_CUDA, "sdpa_bwd_noalloc: cudaGetSymbolAddress returned no address for the scratch array");
     g_scratch_dev_ptr[dev] = ptr;
   }
   return sdpa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Lq, Lk, d, scale, is_causal, nullptr, dtype,

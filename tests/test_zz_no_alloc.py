@@ -5,7 +5,9 @@ backward (a fixed-size memory pool, a plugin handed only its buffers, a host
 that forbids cudaMalloc after start-up): the scratch comes from an array built
 into the library. Its gradients must match those of sdpa_bwd with a
 caller-provided workspace, on two calls in a row (the second call reuses the
-array the first one left behind). This file is collected last on purpose.
+array the first one left behind), and the fp64 oracle's; the second call must
+leave the device's free memory unchanged. This file is collected last on
+purpose.
 """
 import ctypes
 
@@ -51,14 +53,23 @@ def test_noalloc_matches_workspace_backward_twice(lib, dtype, d, causal):
     ref = [torch.empty_like(t) for t in (q, k, v)]
     _abi.check(lib.sdpa_bwd(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(do), *(_p(t) for t in ref),
                             B, H, L, L, d, scale, int(causal), None, code, _p(ws), ws.numel(), _stream()))
-    for call in range(2):
-        got = [torch.full_like(t, float("nan")) for t in (q, k, v)]
+    from oracle import attn_bwd_ref
+    exact = attn_bwd_ref(*(f64(x[n]) for n in ("q", "k", "v", "do")), scale, causal)
+    outs = [[torch.full_like(t, float("nan")) for t in (q, k, v)] for _ in range(2)]
+    torch.cuda.synchronize()
+    for call, got in enumerate(outs):
+        free_before = torch.cuda.mem_get_info(dev)[0]
         _abi.check(lib.sdpa_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(do), *(_p(t) for t in got),
                                         B, H, L, L, d, scale, int(causal), code, _stream()))
         torch.cuda.synchronize()
-        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        if call == 1:
+            # the first call may load the scratch array; the second allocates nothing
+            assert torch.cuda.mem_get_info(dev)[0] == free_before
+        for name, g, r, ex in zip(("dQ", "dK", "dV"), got, ref, exact):
             e = rel_fro(f64(g), f64(r))
             assert e <= GRAD_RTOL[dtype], f"call {call}: {name} differs from sdpa_bwd by {e:.3e}"
+            e = rel_fro(f64(g), ex)
+            assert e <= GRAD_RTOL[dtype], f"call {call}: {name} differs from the oracle by {e:.3e}"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
