@@ -1,20 +1,24 @@
 """Benchmark of the GB300 exact-attention library.
 
 ``python bench.py --gpus N --steps K --warmup W`` (N > 1 under torchrun) prints
-one JSON line. A step is one pass of the measured workload -- by default the
-dense fp16 forward the SDPA tutorial's dispatcher benchmark uses (B=32, H=32,
-L=1024, d=32, torch.rand inputs, non-causal) -- through the library's C ABI.
-Device time is taken with CUDA events on the launching stream, with L2
-flushed (a 256 MiB write) before every timed step; ``e2e`` repeats the same
-steps with the inputs copied in from pinned host memory and the outputs
-copied back inside the timed region. Every rank runs its own replica (the
-work per GPU is fixed: weak scaling); rank 0 prints the aggregate.
+one JSON line. A step is one pass of the measured workload through the
+library's C ABI -- by default the largest single-GPU configuration, the long
+causal bf16 batch (B=2, H=16, L=16384, d=128, N(0,1) inputs): its forward and
+its backward, the whole hot path. Device time is taken with CUDA events on the
+launching stream, with L2 flushed (a 256 MiB write) before every timed step;
+the library's timing hook records a second pair of events around each main
+attention kernel, which gives the roofline of the dominant kernel. ``e2e``
+repeats the same steps with the inputs copied in from pinned host memory and
+the outputs copied back inside the timed region. Every rank runs its own
+replica (the work per GPU is fixed: weak scaling); rank 0 prints the
+aggregate.
 
 The same line carries the roofline of the dominant kernel, the fp64 CPU
-oracle timed on a bounded sample on the host cores, SM clocks sampled during
-the timed region, and (N = 1, rank 0) per-workload results for all five
-workloads (forward and backward TFLOP/s, microseconds per call, fraction of
-the measured tensor peak).
+oracle timed on the host cores (for the largest configuration: one whole
+(batch, head) slice), SM clocks sampled during the timed region, the
+exponential unit's throughput measured by a probe kernel, and (N = 1,
+rank 0) per-workload results for all five workloads (forward and backward
+TFLOP/s, microseconds per call, fraction of the measured tensor peak).
 
 ``--impl reference`` times the oracle itself on the host cores (each step a
 bounded sample of the same workload) and prints the same kind of line.
@@ -36,15 +40,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SDPA fwd/bwd TFLOP/s and µs/call at 1 GB300; fraction of dense fp16/bf16 peak"
-HEADLINE = "dense_f16_d32"
-# The tutorial's own number for this exact workload (flash backend, 2262.901 us,
-# hardware not stated) expressed in the same unit: 4*B*H*L*L*d / t.
+HEADLINE = "long_causal_bf16_d128"
+# The tutorial's own number for the dense fp16 d = 32 batch (flash backend,
+# 2262.901 us, hardware not stated) in the same unit: 4*B*H*L*L*d / t. The
+# pages time no other configuration.
+PAGES_WORKLOAD = "dense_f16_d32"
 PAGES_TFLOPS = 4.0 * 32 * 32 * 1024 * 1024 * 32 / 2262.901e-6 / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-# ex2 results per clock per SM on GB300, inferred from ncu: the XU pipe is 40 %
-# busy while the d = 32 forward issues 11.7 ex2 per clock per SM.
-EX2_PER_CLK_SM = 32
+# Used only when the probe library is missing: the exponential unit's rate
+# the probe measured on GB300 (32 ex2 results per clock per SM).
+EX2_PER_CLK_SM_DEFAULT = 32.0
 
 
 def load_peaks():
@@ -161,36 +167,98 @@ def profiled_traffic(kernel_file, workload):
     return None
 
 
-def oracle_sample(w, x, budget_s, max_units=None):
-    """Time the fp64 oracle (as it stands) on whole units of the workload until
-    ``budget_s`` seconds of CPU work; returns (flops, seconds, description)."""
-    import numpy as np
-    from oracle import attn_fwd_unit
-    done_flops, t_total, n = 0.0, 0.0, 0
+def _unit_arrays(w, x, unit):
+    """fp64 arrays (q, k, v, dO or None) of one (batch|sequence, head) unit."""
     if w.varlen:
         cu = x["cu_seqlens"].numpy()
-        units = [("s", s, h) for s in range(w.nseq) for h in range(w.H)]
+        s_, h = divmod(unit, w.H)
+        lo, hi = int(cu[s_]), int(cu[s_ + 1])
+        pick = lambda t: t[lo:hi, h]          # noqa: E731
     else:
-        units = [("d", b, h) for b in range(w.B) for h in range(w.H)]
-    order = np.random.default_rng(0).permutation(len(units))
-    for idx in order:
-        kind, a, h = units[idx]
-        if kind == "s":
-            lo, hi = int(cu[a]), int(cu[a + 1])
-            q, k, v = (x[t][lo:hi, h].double().numpy() for t in ("q", "k", "v"))
-            f = 4.0 * w.d * (hi - lo) ** 2 * (0.5 if w.causal else 1.0)
+        b, h = divmod(unit, w.H)
+        pick = lambda t: t[b, h]              # noqa: E731
+    arrs = [pick(x[n]).double().numpy() for n in ("q", "k", "v")]
+    arrs.append(pick(x["do"]).double().numpy() if "do" in x else None)
+    return arrs
+
+
+def oracle_work(w, x, unit, with_bwd, rows=None):
+    """Time the fp64 oracle, as it stands, on one unit of the workload --
+    forward, and backward when ``with_bwd`` -- or on the query rows
+    ``rows = (r0, r1)`` of that unit (every key they see). Returns
+    (algorithmic flops, seconds)."""
+    import numpy as np
+    from oracle import attn_bwd_unit, attn_fwd_unit
+    q, k, v, do = _unit_arrays(w, x, unit)
+    vis = None
+    if rows is None:
+        n = q.shape[0]
+        pairs = n * k.shape[0] * (0.5 if w.causal else 1.0)
+        causal = w.causal
+    else:
+        r0, r1 = rows
+        kv = r1 if w.causal else k.shape[0]
+        q, k, v = q[r0:r1], k[:kv], v[:kv]
+        do = None if do is None else do[r0:r1]
+        if w.causal:
+            # query r0 + i sees keys j <= r0 + i
+            vis = np.arange(kv)[None, :] <= (r0 + np.arange(r1 - r0))[:, None]
+            pairs = float(vis.sum())
         else:
-            q, k, v = (x[t][a, h].double().numpy() for t in ("q", "k", "v"))
-            f = 4.0 * w.d * w.Lq * w.Lk * (0.5 if w.causal else 1.0)
-        t0 = time.perf_counter()
-        attn_fwd_unit(q, k, v, w.scale, w.causal)
-        t_total += time.perf_counter() - t0
+            pairs = float((r1 - r0) * kv)
+        causal = False
+    flops = 4.0 * w.d * pairs * (3.5 if with_bwd else 1.0)
+    t0 = time.perf_counter()
+    attn_fwd_unit(q, k, v, w.scale, causal, visible=vis)
+    if with_bwd:
+        attn_bwd_unit(q, k, v, do, w.scale, causal, visible=vis)
+    return flops, time.perf_counter() - t0
+
+
+def units_of(w, x):
+    return (w.nseq if w.varlen else w.B) * w.H
+
+
+def oracle_sample(w, x, budget_s, with_bwd, max_units=None):
+    """Whole units of the workload through the oracle until ``budget_s``
+    seconds of CPU work (or ``max_units``); returns (flops, seconds, text)."""
+    import numpy as np
+    order = np.random.default_rng(0).permutation(units_of(w, x))
+    done_flops, t_total, n = 0.0, 0.0, 0
+    for u in order:
+        f, t = oracle_work(w, x, int(u), with_bwd)
         done_flops += f
+        t_total += t
         n += 1
         if t_total >= budget_s or (max_units and n >= max_units):
             break
-    desc = f"{n} of {len(units)} (unit, head) slices of {w.name}, forward, fp64 NumPy"
-    return done_flops, t_total, desc
+    what = "forward + backward" if with_bwd else "forward"
+    return done_flops, t_total, f"{n} of {len(order)} whole (unit, head) slices of {w.name}, {what}, fp64 NumPy"
+
+
+def measure_ex2(dev_index=0):
+    """Exponentials per SM per clock of the exponential unit, measured by the
+    probe kernel (fp32 ex2, and the packed fp16 / bf16 forms); None if the
+    probe library is missing."""
+    from exact_attention_softmax_gb300.build import PROBE_PATH
+    if not os.path.exists(PROBE_PATH):
+        return None
+    lib = ctypes.CDLL(PROBE_PATH)
+    lib.sdpa_probe_ex2.restype = ctypes.c_int
+    lib.sdpa_probe_ex2.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]
+    out = {}
+    for kind, name in ((0, "f32"), (1, "f16x2"), (2, "bf16x2")):
+        per = (ctypes.c_double * 1024)()
+        ms = ctypes.c_float()
+        runs = []
+        for _ in range(3):
+            n = lib.sdpa_probe_ex2(kind, 2000, per, ctypes.byref(ms), None)
+            if n <= 0:
+                return None
+            runs.append((statistics.median(per[:n]), ms.value))
+        out[name] = {"per_clk_sm": round(max(r[0] for r in runs), 3), "launch_ms": round(min(r[1] for r in runs), 4)}
+    return out
 
 
 def reduce_max_ms(ms, world, device=None):
@@ -264,7 +332,14 @@ def time_calls(fn, iters, flush, stream):
     return [a.elapsed_time(b) for a, b in ts]
 
 
-def per_workload_results(dev, flush, peaks, peak_kind):
+def exp_ceiling_tflops(d, ex2_rate, sms, clk_mhz):
+    """Forward ceiling set by the exponential unit: one ex2 per score element,
+    4*d algorithmic flops per score element, ``ex2_rate`` results per clock
+    per SM."""
+    return 4.0 * d * ex2_rate * sms * clk_mhz * 1e6 / 1e12
+
+
+def per_workload_results(dev, flush, peaks, peak_kind, ex2_rate=EX2_PER_CLK_SM_DEFAULT, clk_mhz=2070):
     """Forward (and backward) timings of all five workloads (N = 1 only)."""
     import torch
     from exact_attention_softmax_gb300 import workloads as wl
@@ -289,6 +364,8 @@ def per_workload_results(dev, flush, peaks, peak_kind):
             min_bytes = 2 * 4 * w.B * w.H * w.Lq * w.d + 4 * w.B * w.H * w.Lq
             res["fwd_hbm_gbs"] = min_bytes / (res["fwd_us"] * 1e-6) / 1e9
             res["fwd_frac_of_hbm"] = res["fwd_hbm_gbs"] / peaks["hbm_gbs"]
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            res["fwd_frac_of_exp_ceiling"] = res["fwd_tflops"] / exp_ceiling_tflops(w.d, ex2_rate, sms, clk_mhz)
         if w.bwd:
             tb = time_calls(r.bwd, iters, flush, stream)
             bf = wl.bwd_flops(w, lengths)
@@ -403,15 +480,22 @@ def run_ours(args):
     w = wl.WORKLOADS[args.workload]
     x = wl.workload_inputs(w, seed=rank)
     lengths = x.get("lengths")
-    do_fwd = args.passes in ("fwd", "both")
-    do_bwd = args.passes in ("bwd", "both")
+    passes = args.passes if args.passes != "auto" else ("both" if w.bwd else "fwd")
+    do_fwd = passes in ("fwd", "both")
+    do_bwd = passes in ("bwd", "both")
     if do_bwd and not w.bwd:
         raise SystemExit(f"workload {w.name} has no backward")
-    flops = (wl.fwd_flops(w, lengths) if do_fwd else 0.0) + (wl.bwd_flops(w, lengths) if do_bwd else 0.0)
+    fwd_f = wl.fwd_flops(w, lengths)
+    bwd_f = wl.bwd_flops(w, lengths) if w.bwd else 0.0
+    flops = (fwd_f if do_fwd else 0.0) + (bwd_f if do_bwd else 0.0)
     r = Runner(w, x, dev, with_bwd=do_bwd)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # kernels of one step: the forward's, and the backward's row-statistic
+    # pass, main kernel and dQ conversion
     launches_per_step = (1 if do_fwd else 0) + (3 if do_bwd else 0)
+    ex2 = measure_ex2(local)
+    ex2_rate = ex2["f32"]["per_clk_sm"] if ex2 else EX2_PER_CLK_SM_DEFAULT
 
     def step():
         if do_fwd:
@@ -430,12 +514,26 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # one event pair per step around each main kernel (the library records
+    # them on the launching stream); created before the timed region
+    def pairs(n):
+        ps = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a_, b_ in ps:
+            a_.record(stream)
+            b_.record(stream)
+        return ps
+    kev = {"fwd": pairs(args.steps) if do_fwd else [], "bwd": pairs(args.steps) if do_bwd else []}
+
     # ---- device-resident timed region
     clocks = ClockSampler(local).start()
     barrier()
     evs = []
-    for _ in range(args.steps):
+    for i in range(args.steps):
         flush.zero_()
+        if do_fwd:
+            ops.sdpa_trace_events("fwd", *kev["fwd"][i])
+        if do_bwd:
+            ops.sdpa_trace_events("bwd", *kev["bwd"][i])
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -444,8 +542,11 @@ def run_ours(args):
         evs.append((a, b))
     barrier()
     clk = clocks.stop()
+    ops.sdpa_trace_events("fwd")
+    ops.sdpa_trace_events("bwd")
     kernel_ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = reduce_max_ms(sum(kernel_ms), world, dev)
+    main_ms = {k: [a.elapsed_time(b) for a, b in v] for k, v in kev.items() if v}
     ops.sdpa_device_status()
 
     # ---- end to end: pinned host inputs in, outputs out, inside the timed region
@@ -519,31 +620,37 @@ def run_ours(args):
 
     value = whole_job_tflops(world, flops, args.steps, total_ms)
     # the end-to-end step always runs the forward (the backward needs its O and LSE)
-    e2e_flops = flops + (wl.fwd_flops(w, lengths) if not do_fwd else 0.0)
+    e2e_flops = flops + (fwd_f if not do_fwd else 0.0)
     e2e_value = whole_job_tflops(world, e2e_flops, e2e_steps, e2e_ms)
-    avg_kernel_s = statistics.mean(kernel_ms) * 1e-3
-    kern_file = "fwd_tc.cu" if do_fwd and not do_bwd else "bwd_tc.cu"
-    kern_name = "fwd_tc_kernel" if kern_file == "fwd_tc.cu" else "bwd_tc_kernel"
-    achieved = flops / avg_kernel_s / 1e12
-    traffic = profiled_traffic(kern_file, args.workload)
-    # Two ceilings for the dominant kernel: the tensor cores (measured dense
-    # bf16 peak; fp16 has the same rate) and, for the forward, the exponential
-    # unit: one ex2 per score element, 4*d algorithmic flops per score element,
-    # EX2_PER_CLK_SM results per clock per SM.
+
+    # Rooflines of the main kernels, from their own events. The tensor-core
+    # ceiling is the measured dense bf16 peak (fp16 has the same rate); the
+    # small-head-dim forward has a lower one, the exponential unit's: one ex2
+    # per score element at the rate the probe measured.
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clk_mhz = clk.get("sm_max_mhz") or 2070
-    exp_ceiling = 4.0 * w.d * EX2_PER_CLK_SM * sms * clk_mhz * 1e6 / 1e12
-    if do_fwd and not do_bwd and exp_ceiling < peaks["bf16_tflops"]:
-        roof = {"kernel": kern_name, "bound": "alu", "achieved": round(achieved, 2), "peak": round(exp_ceiling, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / exp_ceiling, 4),
-                "peak_source": f"exponential unit: {EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {clk_mhz} MHz, "
-                               f"{4 * w.d} flop per score element",
-                "tensor_peak": peaks["bf16_tflops"], "tensor_frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": traffic}
-    else:
-        roof = {"kernel": kern_name, "bound": "tensor", "achieved": round(achieved, 2),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "peak_source": f"{peak_kind} dense bf16 burst (fp16 has the same tensor rate)", "traffic": traffic}
+    kinfo = {"fwd": ("fwd_tc_kernel", "fwd_tc.cu", fwd_f), "bwd": ("bwd_tc_kernel", "bwd_tc.cu", bwd_f)}
+    kernels = {}
+    for key, ms in main_ms.items():
+        name, src, f = kinfo[key]
+        avg_s = statistics.mean(ms) * 1e-3
+        achieved = f / avg_s / 1e12
+        exp_ceiling = exp_ceiling_tflops(w.d, ex2_rate, sms, clk_mhz)
+        if key == "fwd" and exp_ceiling < peaks["bf16_tflops"]:
+            roof = {"kernel": name, "bound": "alu", "achieved": round(achieved, 2), "peak": round(exp_ceiling, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / exp_ceiling, 4),
+                    "peak_source": f"exponential unit: {ex2_rate:g} ex2/clk/SM (probe, measured in this run) x "
+                                   f"{sms} SMs x {clk_mhz} MHz, {4 * w.d} flop per score element",
+                    "tensor_peak": peaks["bf16_tflops"], "tensor_frac": round(achieved / peaks["bf16_tflops"], 4)}
+        else:
+            roof = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "peak_source": f"{peak_kind} dense bf16 burst (fp16 has the same tensor rate), of {peak_kind}"}
+        roof["us_per_launch"] = round(1e3 * statistics.mean(ms), 2)
+        roof["share_of_step"] = round(sum(ms) / sum(kernel_ms), 4)
+        roof["traffic"] = profiled_traffic(src, w.name)
+        kernels[name] = roof
+    dominant = max(kernels.values(), key=lambda k: k["share_of_step"])
     shape = (f"B={w.B} H={w.H} Lq={w.Lq} Lk={w.Lk} d={w.d}" if not w.varlen else
              f"{w.nseq} packed sequences (max {w.max_len}, total {x['q'].shape[0]}) H={w.H} d={w.d}")
     line = {
@@ -558,27 +665,37 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": (round(value / world / PAGES_TFLOPS, 3)
-                        if args.workload == HEADLINE and args.passes == "fwd" else None),
+                        if args.workload == PAGES_WORKLOAD and passes == "fwd" else None),
         "dtype": w.dtype,
         "data": "synthetic (seeded torch.rand / torch.randn of the workload's shape)",
         "config": {"workload": f"{w.name}: {shape} {w.dtype} {w.dist} "
-                               f"{'causal' if w.causal else 'non-causal'} {args.passes}",
-                   "flops_per_step": flops, "l2": "flushed before every timed step (256 MiB write)",
+                               f"{'causal' if w.causal else 'non-causal'} {passes}",
+                   "flops_per_step": flops, "fwd_flops": fwd_f if do_fwd else 0.0,
+                   "bwd_flops": bwd_f if do_bwd else 0.0,
+                   "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas x{world} (one independent problem per GPU)"},
-        "roofline": roof,
+        "roofline": dominant,
+        "kernels": kernels,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "pipelining": "inputs of step k+1 and outputs of step k-1 copied while step k computes "
                               "(two device buffer sets, three streams)"},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
+        "ex2_probe": ex2,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f, s, desc = oracle_sample(w, x, budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
-                                "kind": "oracle", "sample": desc + f", {s:.1f} s"}
+        if w.name == HEADLINE:
+            # the largest configuration: one whole (batch, head) slice
+            f, sec = oracle_work(w, x, 0, do_bwd)
+            desc = (f"one whole (batch, head) slice, (0, 0), of {w.name} (1 of {units_of(w, x)}), "
+                    f"{'forward + backward' if do_bwd else 'forward'}, fp64 NumPy")
+        else:
+            f, sec, desc = oracle_sample(w, x, args.cpu_budget, do_bwd)
+        line["cpu_baseline"] = {"value": round(f / sec / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
+                                "kind": "oracle", "sample": desc + f", {sec:.1f} s"}
     if rank == 0 and world == 1 and not args.no_extras:
-        line["per_workload"] = per_workload_results(dev, flush, peaks, peak_kind)
+        line["per_workload"] = per_workload_results(dev, flush, peaks, peak_kind, ex2_rate, clk_mhz)
         line["extras"] = extra_results(dev, flush, peaks)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -589,29 +706,47 @@ def run_ours(args):
 # ---------------------------------------------------------- reference arm
 def run_reference(args):
     """The fp64 oracle, as it stands, on the host cores; each step is a bounded
-    sample of the workload (whole (batch, head) slices)."""
+    sample of the workload: one whole (batch, head) unit, or for the long
+    sequences a block of 1024 query rows of one unit (with every key those
+    rows see), the blocks walking over units and positions from step to step."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from exact_attention_softmax_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
     x = wl.workload_inputs(w, seed=0)
-    per_step_units = 2
-    for _ in range(args.warmup):
-        oracle_sample(w, x, budget_s=0.0, max_units=1)
+    passes = args.passes if args.passes != "auto" else ("both" if w.bwd else "fwd")
+    with_bwd = passes in ("bwd", "both")
+    nunits = units_of(w, x)
+    blocked = not w.varlen and w.Lq > 4096
+    rows = 1024
+
+    def sample(i):
+        unit = (7 * i) % nunits
+        if blocked:
+            nb = w.Lq // rows
+            r0 = ((5 * i + 3) % nb) * rows
+            return oracle_work(w, x, unit, with_bwd, rows=(r0, r0 + rows))
+        return oracle_work(w, x, unit, with_bwd)
+
+    for i in range(args.warmup):
+        sample(1000 + i)
     flops = secs = 0.0
-    desc = ""
-    for _ in range(args.steps):
-        f, s, desc = oracle_sample(w, x, budget_s=1e9, max_units=per_step_units)
+    for i in range(args.steps):
+        f, t = sample(i)
         flops += f
-        secs += s
+        secs += t
     value = flops / secs / 1e12
+    what = "forward + backward" if with_bwd else "forward"
+    desc = (f"per step one block of {rows} query rows of one (batch, head) unit of {w.name} with every key "
+            f"they see, {what}, fp64 NumPy" if blocked else
+            f"per step one whole (unit, head) slice of {w.name}, {what}, fp64 NumPy")
     line = {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "sample_per_step": desc},
+        "data": "synthetic", "config": {"workload": w.name, "passes": passes, "sample_per_step": desc},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": host_cores(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -627,8 +762,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
-    ap.add_argument("--pass", dest="passes", choices=["fwd", "bwd", "both"], default="fwd",
-                    help="what one step runs (the headline workload is a forward-only workload)")
+    ap.add_argument("--pass", dest="passes", choices=["auto", "fwd", "bwd", "both"], default="auto",
+                    help="what one step runs (auto: forward and backward where the workload has a backward)")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")

@@ -22,7 +22,7 @@ from ._abi import SdpaError  # noqa: F401
 __all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_fwd_blocksparse",
            "sdpa_bwd_blocksparse", "sdpa_fwd_masked", "sdpa_bwd_masked", "sdpa_fwd_dropout",
            "sdpa_bwd_dropout", "sdpa_bwd_workspace_size",
-           "sdpa_device_status",
+           "sdpa_device_status", "sdpa_trace_events",
            "sdpa_debug_set", "sdpa_last_error", "sdpa_version", "SdpaError"]
 
 
@@ -390,6 +390,24 @@ def sdpa_device_status(stream=None):
     s = ctypes.c_void_p(stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream)
     _abi.check(lib.sdpa_device_status(s, ctypes.byref(bits)))
     return bits.value
+
+
+def sdpa_trace_events(which, begin=None, end=None):
+    """Kernel timing aid: later calls record ``begin`` and ``end``
+    (``torch.cuda.Event(enable_timing=True)``) on their stream around their
+    main attention kernel -- the forward's for ``which`` = 0 (or "fwd"), the
+    backward's for 1 (or "bwd"); ``None`` for both removes them. Read the time
+    with ``begin.elapsed_time(end)`` after synchronising."""
+    import torch
+    w = {"fwd": 0, "bwd": 1}.get(which, which)
+
+    def handle(ev):
+        if ev is None:
+            return ctypes.c_void_p(0)
+        if ev.cuda_event == 0:      # PyTorch creates the CUDA event on its first record
+            ev.record(torch.cuda.current_stream())
+        return ctypes.c_void_p(ev.cuda_event)
+    _abi.check(_abi.load().sdpa_trace_events(int(w), handle(begin), handle(end)))
 
 
 def sdpa_debug_set(flags: int) -> int:

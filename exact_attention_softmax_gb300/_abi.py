@@ -45,6 +45,7 @@ SIGNATURES = {
     "sdpa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "sdpa_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
+    "sdpa_trace_events": (_i, [_i, _vp, _vp]),
     "sdpa_debug_set": (_i, [_i]),
     "sdpa_last_error": (ctypes.c_char_p, []),
     "sdpa_version": (_i, []),

@@ -23,6 +23,10 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libsdpa_gb300.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
+# The exponential-unit throughput probe the benchmark measures its ceiling
+# with; a library of its own, outside the attention ABI.
+PROBE_DIR = os.path.join(PKG, "probe")
+PROBE_PATH = os.path.join(LIB_DIR, "libsdpa_probe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
@@ -76,8 +80,22 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
             raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
         return r.stdout + r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+    probe_srcs = sorted(os.path.join(PROBE_DIR, f) for f in os.listdir(PROBE_DIR) if f.endswith(".cu"))
+
+    def build_probe():
+        if not force and os.path.exists(PROBE_PATH) and all(
+                os.path.getmtime(PROBE_PATH) >= os.path.getmtime(x) for x in probe_srcs):
+            return ""
+        cmd = [nvcc, *ARCH, *FLAGS, "-shared", "-o", PROBE_PATH, *probe_srcs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for the probe:\n{r.stdout}\n{r.stderr}")
+        return ""
+
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs) + 1)) as ex:
+        probe = ex.submit(build_probe)
         logs = list(ex.map(compile_one, zip(srcs, objs)))
+        probe.result()
     if verbose or ptxas_info:
         for s, log in zip(srcs, logs):
             if log.strip():

@@ -19,6 +19,15 @@ namespace {
 thread_local std::string g_last_error;
 int g_debug_flags = 0;
 
+// Kernel timing aid: caller-owned CUDA events recorded on the call's stream
+// around the main attention kernel of the forward ([0]) and backward ([1]).
+cudaEvent_t g_trace_begin[2] = {nullptr, nullptr};
+cudaEvent_t g_trace_end[2] = {nullptr, nullptr};
+
+cudaError_t trace_mark(const cudaEvent_t* evs, int which, cudaStream_t s) {
+  return evs[which] ? cudaEventRecord(evs[which], s) : cudaSuccess;
+}
+
 int fail(int code, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -279,8 +288,10 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (dtype == SDPA_F32) {
+    if ((e = trace_mark(g_trace_begin, 0, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
     e = launch_fwd_simt(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward (fp32) launch");
+    if ((e = trace_mark(g_trace_end, 0, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
     return SDPA_OK;
   }
   rc = get_encoder();
@@ -295,8 +306,10 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
       (rc = make_mask_map(&maps.mask, am.m, dtype, sh.B, sh.H, sh.total_q, sh.total_k, am.sb, am.sh, am.sq, 64, 32)) !=
           SDPA_OK)
     return rc;
+  if ((e = trace_mark(g_trace_begin, 0, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
   e = launch_fwd_tc(p, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "forward (tensor-core) launch");
+  if ((e = trace_mark(g_trace_end, 0, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
   return SDPA_OK;
 }
 
@@ -339,8 +352,10 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
   cudaError_t e = launch_bwd_prep(bp, dtype, dtype == SDPA_F32 ? 0 : 1, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward prep launch");
   if (dtype == SDPA_F32) {
+    if ((e = trace_mark(g_trace_begin, 1, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
     e = launch_bwd_simt(bp, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward (fp32) launch");
+    if ((e = trace_mark(g_trace_end, 1, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
     return SDPA_OK;
   }
   rc = get_encoder();
@@ -355,8 +370,10 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
       (rc = make_mask_map(&maps.mask, am.m, dtype, sh.B, sh.H, sh.total_q, sh.total_k, am.sb, am.sh, am.sq, 128, 32)) !=
           SDPA_OK)
     return rc;
+  if ((e = trace_mark(g_trace_begin, 1, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
   e = launch_bwd_tc(bp, dtype, maps, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward (tensor-core) launch");
+  if ((e = trace_mark(g_trace_end, 1, s)) != cudaSuccess) return cuda_fail(e, "recording the trace event");
   e = launch_dq_convert(bp, dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "dQ convert launch");
   return SDPA_OK;
@@ -488,6 +505,16 @@ extern "C" int sdpa_device_status(void* stream, unsigned* bits) {
   if (bits) *bits = word;
   if (word & SDPA_STATUS_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", word);
   if (word & SDPA_STATUS_SEQLEN) return fail(SDPA_ERR_ARG, "a packed sequence is longer than its bound or has queries but no keys (status 0x%x)", word);
+  return SDPA_OK;
+}
+
+extern "C" int sdpa_trace_events(int which, void* begin_event, void* end_event) {
+  g_last_error.clear();
+  if (which != 0 && which != 1) return fail(SDPA_ERR_ARG, "trace target must be 0 (forward) or 1 (backward), got %d", which);
+  if ((begin_event == nullptr) != (end_event == nullptr))
+    return fail(SDPA_ERR_ARG, "trace events must both be set or both be NULL");
+  g_trace_begin[which] = static_cast<cudaEvent_t>(begin_event);
+  g_trace_end[which] = static_cast<cudaEvent_t>(end_event);
   return SDPA_OK;
 }
 

@@ -114,15 +114,19 @@ int sdpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
 /*
  * Bytes of device workspace sdpa_bwd needs for these sizes (a float32 row
  * statistic D = rowsum(dO * O) and a float32 dQ accumulator, both over the
- * query rows). Packed mode: pass B = 1 and Lq = total. Never fails; returns
- * 0 when nothing is needed.
+ * query rows). The FlashAttention news article (QbitAI repost, section
+ * "FlashAttention") has the backward rebuild the attention matrix from the
+ * inputs instead of storing it; these two arrays, linear in the query rows,
+ * are what that rebuild keeps between its kernels. Packed mode: pass B = 1
+ * and Lq = total. Never fails; returns 0 when nothing is needed.
  */
 size_t sdpa_bwd_workspace_size(int B, int H, int Lq, int d, int dtype);
 
 /*
- * Backward: gradients of sum(dO * O) w.r.t. q, k, v, recomputing the
- * probabilities from q, k and the forward's lse (the pages' "recompute in
- * the backward pass").
+ * Backward: gradients of sum(dO * O) w.r.t. q, k, v. As the FlashAttention
+ * news article (QbitAI repost, section "FlashAttention") describes, the
+ * probabilities are not stored by the forward but rebuilt here from q, k and
+ * the forward's lse.
  *   q, k, v, o, lse : the forward's inputs and outputs (o and lse exactly as
  *                     sdpa_fwd wrote them).
  *   dO      : upstream gradient, layout of o.
@@ -263,11 +267,15 @@ int sdpa_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
  *   16 MiB (B*H*Lq*(d+1)*4 bytes, rounded, for fp16/bf16); larger problems
  *   return SDPA_ERR_WORKSPACE before anything is launched.
  *   The first call on each device looks up the array's device address while
- *   that device is current; make that first call before any stream capture.
+ *   that device is current. With CUDA's lazy module loading (the default)
+ *   that lookup is also what loads the array onto the device and reserves
+ *   its 16 MiB, so a caller with a fixed memory budget should make the first
+ *   call at start-up, and before any stream capture. Later calls on that
+ *   device allocate nothing.
  *   Every call on a device shares the one array (it is held until the process
  *   exits and keeps the last call's contents; each call re-initialises what it
  *   needs), so calls whose kernels may overlap on the GPU race and must be
- *   ordered by the caller (same stream, or events). No call allocates.
+ *   ordered by the caller (same stream, or events).
  */
 int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dO, void* dq, void* dk, void* dv,
@@ -283,6 +291,21 @@ int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
 int sdpa_device_status(void* stream, unsigned* bits);
 
 /*
+ * Kernel timing aid (no counterpart on the pages: it serves measurement).
+ * Installs two CUDA events (cudaEvent_t handles the caller created, with
+ * timing enabled) that every later call records on its own stream directly
+ * before and directly after its main attention kernel: the tensor-core (or
+ * fp32) forward kernel for which = 0, the backward's for which = 1 (the
+ * backward's row-statistic pass and dQ conversion fall outside the pair).
+ * cudaEventElapsedTime on the pair then gives the last such kernel's device
+ * time. NULL for both removes them. The setting is process-wide and not
+ * synchronised: install events from one thread, with no calls in flight on
+ * other threads. Returns SDPA_OK, or SDPA_ERR_ARG for another `which` or a
+ * single NULL.
+ */
+int sdpa_trace_events(int which, void* begin_event, void* end_event);
+
+/*
  * Testing aid: sets debug flags for later calls on any thread and returns the
  * previous value. Flag 1 makes the forward tensor-core kernel skip its Q load,
  * so every wait in it runs out and sdpa_device_status() reports
@@ -290,7 +313,12 @@ int sdpa_device_status(void* stream, unsigned* bits);
  */
 int sdpa_debug_set(int flags);
 
-/* Message for the last nonzero return on the calling thread ("" if none). */
+/*
+ * Message for the last nonzero return on the calling thread ("" if none).
+ * The SDPA tutorial's calls raise RuntimeError with a message when an input
+ * is not supported (section "Explicit Dispatcher Control"); the Python
+ * binding raises with this text.
+ */
 const char* sdpa_last_error(void);
 
 /* Library version as major*10000 + minor*100 + patch. */

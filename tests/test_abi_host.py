@@ -160,3 +160,12 @@ def test_python_binding_rejects_cpu_tensors(lib):
     lse = torch.zeros(1, 1, 8)
     with pytest.raises(ValueError, match="CUDA tensors only"):
         ops.sdpa_bwd(q, q, q, q, lse, q)
+
+
+def test_trace_events_argument_checks(lib):
+    # setting and clearing the timing hook touches no CUDA state
+    assert lib.sdpa_trace_events(2, None, None) == _abi.SDPA_ERR_ARG
+    assert b"trace" in lib.sdpa_last_error()
+    assert lib.sdpa_trace_events(0, FAKE, None) == _abi.SDPA_ERR_ARG
+    assert lib.sdpa_trace_events(0, None, None) == _abi.SDPA_OK
+    assert lib.sdpa_trace_events(1, None, None) == _abi.SDPA_OK
