@@ -442,6 +442,27 @@ def extra_results(dev, flush, peaks):
           f"B={B} H={H} L={L} d={d} f16 non-causal, dropout p = 0.1")
     del q, k, v, do, o, lse, g, ws, x
 
+    # strided: the SDPA tutorial module's [B, L, 3E] projection viewed as
+    # [B, H, L, d] (the causal d = 64 workload's shape), outputs written into
+    # [B, L, E] / [B, L, 3E] views, no copy
+    B, L, H, d = 32, 1024, 8, 64
+    E = H * d
+    g = torch.Generator("cpu").manual_seed(0)
+    qkv = torch.randn(B, L, 3 * E, generator=g).half().to(dev)
+    q, k, v = (t.view(B, L, H, d).transpose(1, 2) for t in qkv.split(E, dim=2))
+    do = torch.randn(B, L, E, generator=g).half().to(dev).view(B, L, H, d).transpose(1, 2)
+    o = torch.empty(B, L, E, dtype=torch.half, device=dev).view(B, L, H, d).transpose(1, 2)
+    dqkv = torch.empty(B, L, 3 * E, dtype=torch.half, device=dev)
+    g3 = [t.view(B, L, H, d).transpose(1, 2) for t in dqkv.split(E, dim=2)]
+    _, lse = ops.sdpa_fwd(q, k, v, o, is_causal=True)
+    ws = torch.empty(ops.sdpa_bwd_workspace_size(B, H, L, d, 1), dtype=torch.uint8, device=dev)
+    timed("strided_module_f16_d64", lambda: ops.sdpa_fwd(q, k, v, o, lse, is_causal=True),
+          lambda: ops.sdpa_bwd(q, k, v, o, lse, do, *g3, is_causal=True, workspace=ws),
+          2.0 * d * B * H * L * L, 2.5 * 2.0 * d * B * H * L * L,
+          f"B={B} H={H} L={L} d={d} f16 causal, q/k/v views of a [B, L, 3E] projection, O and dQ/dK/dV "
+          "written into [B, L, E] / [B, L, 3E] views (strided calls, no copy)")
+    del qkv, q, k, v, do, o, dqkv, g3, lse, ws
+
     # packed cross-attention: 32 sequences, queries around 256 long, keys around 512
     lq = wl.varlen_lengths(32, 512, 0.5, 0)
     lk = wl.varlen_lengths(32, 1024, 0.5, 1)

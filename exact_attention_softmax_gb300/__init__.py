@@ -62,7 +62,10 @@ def _geometry(q, k, cu_seqlens, max_seqlen):
     return B, H, Lq, k.shape[2], d, False
 
 
-def _check_tensors(ts, dev, dt):
+def _check_tensors(ts, dev, dt, strided_ok=False):
+    """Device, dtype and layout checks. With ``strided_ok`` (dense calls) a
+    tensor may have any strides whose innermost one is 1; otherwise it must
+    be contiguous."""
     if dev.type != "cuda":
         raise ValueError(f"q is on {dev}: the attention ops take CUDA tensors only (there is no CPU implementation)")
     for name, t in ts.items():
@@ -72,8 +75,24 @@ def _check_tensors(ts, dev, dt):
             raise ValueError(f"{name} is on {t.device}, expected {dev}")
         if t.dtype != dt:
             raise TypeError(f"{name} has dtype {t.dtype}, expected {dt}")
+        if strided_ok and t.dim() >= 3 and t.stride(-1) == 1:
+            continue
         if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
+            raise ValueError(f"{name} must be contiguous" + (" or have a unit innermost stride" if strided_ok else ""))
+
+
+def _strides(ts):
+    """ctypes array of the (batch, head, row) element strides of dense
+    [B, H, L, d] (or one-head [B, L, d]) tensors, in the C ABI's order."""
+    vals = []
+    for t in ts:
+        st = t.stride()
+        vals += list(st[:3]) if t.dim() == 4 else [st[0], st[0], st[1]]
+    return (ctypes.c_longlong * len(vals))(*vals)
+
+
+def _is_strided(ts):
+    return any(t is not None and not t.is_contiguous() for t in ts)
 
 
 def sdpa_fwd(q, k, v, o=None, lse=None, *, scale=None, is_causal=False, cu_seqlens=None,
@@ -95,11 +114,18 @@ def sdpa_fwd(q, k, v, o=None, lse=None, *, scale=None, is_causal=False, cu_seqle
     if lse is None:
         shape = (H, Lq) if packed else tuple(q.shape[:-1])
         lse = torch.empty(shape, dtype=torch.float32, device=q.device)
-    _check_tensors({"k": k, "v": v, "o": o}, q.device, q.dtype)
+    _check_tensors({"q": q, "k": k, "v": v, "o": o}, q.device, q.dtype, strided_ok=not packed)
     if lse.dtype != torch.float32 or not lse.is_contiguous():
         raise TypeError("lse must be contiguous float32")
     if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != q.device):
         raise TypeError("cu_seqlens must be int32 on the device of q")
+    if not packed and _is_strided((q, k, v, o)):
+        # dense tensors at any strides (e.g. the [B, L, H, d] projections
+        # viewed as [B, H, L, d]): no copy
+        _abi.check(lib.sdpa_fwd_strided(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), B, H, Lq, Lk, d, float(scale),
+                                        int(bool(is_causal)), _strides((q, k, v, o)), _dtype_code(q),
+                                        _stream(q.device, stream)))
+        return o, lse
     _abi.check(lib.sdpa_fwd(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), B, H, Lq, Lk, d, float(scale),
                             int(bool(is_causal)), _vp(cu_seqlens), _dtype_code(q), _stream(q.device, stream)))
     return o, lse
@@ -122,11 +148,20 @@ def sdpa_bwd(q, k, v, o, lse, dO, dq=None, dk=None, dv=None, *, scale=None, is_c
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check_tensors({"k": k, "v": v, "o": o, "dO": dO, "dq": dq, "dk": dk, "dv": dv}, q.device, q.dtype)
+    _check_tensors({"q": q, "k": k, "v": v, "o": o, "dO": dO, "dq": dq, "dk": dk, "dv": dv}, q.device, q.dtype,
+                   strided_ok=not packed)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise TypeError("lse must be contiguous float32")
     code = _dtype_code(q)
     need = lib.sdpa_bwd_workspace_size(1 if packed else B, H, Lq, d, code)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if not packed and _is_strided((q, k, v, o, dO, dq, dk, dv)):
+        _abi.check(lib.sdpa_bwd_strided(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk),
+                                        _vp(dv), B, H, Lq, Lk, d, float(scale), int(bool(is_causal)),
+                                        _strides((q, k, v, o, dO, dq, dk, dv)), code, _vp(workspace),
+                                        workspace.numel(), _stream(q.device, stream)))
+        return dq, dk, dv
     _abi.check(lib.sdpa_bwd(_vp(q), _vp(k), _vp(v), _vp(o), _vp(lse), _vp(dO), _vp(dq), _vp(dk), _vp(dv),
                             B, H, Lq, Lk, d, float(scale), int(bool(is_causal)), _vp(cu_seqlens), code,
                             _vp(workspace), workspace.numel(), _stream(q.device, stream)))

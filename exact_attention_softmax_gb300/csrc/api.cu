@@ -75,12 +75,34 @@ int get_encoder() {
   return SDPA_OK;
 }
 
+// 4-D tiled map over 16-bit elements: dims {d, n1, n2, n3} with the byte
+// strides of dims 1..3, box {box0, box1, 1, 1} or {box0, 1, box2, 1}. A
+// dimension of size 1 takes a harmless stride (its coordinate is always 0).
+int make_map4(CUtensorMap* m, const void* base, int dtype, uint64_t d, uint64_t n1, uint64_t n2, uint64_t n3,
+              uint64_t s1, uint64_t s2, uint64_t s3, uint32_t box0, uint32_t box1, uint32_t box2) {
+  const uint64_t fill = std::max<uint64_t>({16, n1 * s1, n2 * s2});
+  if (n1 == 1) s1 = (s1 % 16 == 0 && s1 > 0) ? s1 : (d * 2 + 15) / 16 * 16;
+  if (n2 == 1) s2 = (s2 % 16 == 0 && s2 > 0) ? s2 : (fill + 15) / 16 * 16;
+  if (n3 == 1) s3 = (s3 % 16 == 0 && s3 > 0) ? s3 : (fill + 15) / 16 * 16;
+  const cuuint64_t dims[4] = {d, n1, n2, n3};
+  const cuuint64_t strides[3] = {s1, s2, s3};
+  const cuuint32_t box[4] = {box0, box1, box2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw = box0 * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+  return SDPA_OK;
+}
+
 // 3-D tiled map over 16-bit elements: dims {d, n1, n2}, byte strides of
 // dims 1 and 2, box {box0, box1, box2}.
-int make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d, uint64_t n1, uint64_t n2,
-             uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2) {
+int make_map3(CUtensorMap* m, const void* base, int dtype, uint64_t d, uint64_t n1, uint64_t n2, uint64_t s1,
+              uint64_t s2, uint32_t box0, uint32_t box1, uint32_t box2) {
   const cuuint64_t dims[3] = {d, n1, n2};
-  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint64_t strides[2] = {s1, s2};
   const cuuint32_t box[3] = {box0, box1, box2};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt =
@@ -92,16 +114,20 @@ int make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d, uint64_t n
   return SDPA_OK;
 }
 
-// Map for a q/k/v-like tensor with `rows` rows per unit (dense) or `total`
-// packed tokens, tiled in 128-row boxes of 64 (d >= 64) or 32 (d = 32) columns.
+// Map for a q/k/v-like tensor, tiled in `box_rows`-row boxes of 64 (d >= 64)
+// or 32 (d = 32) columns. Contiguous dense: dims {d, rows, B*H}, boxes at
+// (column, row, unit). Strided dense: dims {d, rows, H, B} at the tensor's
+// element strides `st` = (batch, head, row), boxes at (column, row, head,
+// batch). Packed [total, H, d]: dims {d, H, total}, boxes at (column, head,
+// token).
 int make_operand_map(CUtensorMap* m, const void* base, int dtype, bool packed, int B, int H, int rows, int d,
-                     uint32_t box_rows = 128) {
+                     const long long* st, int strided, uint32_t box_rows = 128) {
   const uint32_t blk = d >= 64 ? 64 : static_cast<uint32_t>(d);
   const uint64_t es = 2;
-  if (!packed)
-    return make_map(m, base, dtype, d, rows, static_cast<uint64_t>(B) * H, d * es, static_cast<uint64_t>(rows) * d * es,
-                    blk, box_rows, 1);
-  return make_map(m, base, dtype, d, H, rows, d * es, static_cast<uint64_t>(H) * d * es, blk, 1, box_rows);
+  if (packed) return make_map3(m, base, dtype, d, H, rows, d * es, static_cast<uint64_t>(H) * d * es, blk, 1, box_rows);
+  if (strided) return make_map4(m, base, dtype, d, rows, H, B, st[2] * es, st[1] * es, st[0] * es, blk, box_rows, 1);
+  return make_map3(m, base, dtype, d, rows, static_cast<uint64_t>(B) * H, d * es, static_cast<uint64_t>(rows) * d * es,
+                   blk, box_rows, 1);
 }
 
 // Map over an additive mask with element strides (sb, sh, sq): dims {Lk, Lq,
@@ -267,12 +293,49 @@ void fill_problem(Problem& p, const Shape& sh, const void* q, const void* k, con
   p.total_k = sh.total_k;
   p.max_q = sh.packed() ? sh.max_q : sh.total_q;
   p.debug = g_debug_flags;
+  // dense tensors contiguous unless the call gives strides
+  for (int t = 0; t < kTensors; ++t) {
+    const bool key = t == kTk || t == kTv || t == kTdk || t == kTdv;
+    const long long rows = key ? sh.total_k : sh.total_q;
+    p.st[t][2] = sh.d;
+    p.st[t][1] = rows * sh.d;
+    p.st[t][0] = static_cast<long long>(sh.H) * rows * sh.d;
+  }
+}
+
+// Strides of a strided call: `n` tensors in Tensor order, (batch, head, row)
+// each, in elements. Every stride of a dimension longer than 1 must be
+// positive; fp16 / bf16 strides must be multiples of 8 elements (16 bytes:
+// the tensor-core kernels read with TMA and store 16-byte vectors).
+int check_strides(const Shape& sh, const long long* strides, int n, int dtype) {
+  if (strides == nullptr) return fail(SDPA_ERR_ARG, "stride array is NULL");
+  static const char* names[kTensors] = {"q", "k", "v", "o", "dO", "dq", "dk", "dv"};
+  for (int t = 0; t < n; ++t) {
+    const bool key = t == kTk || t == kTv || t == kTdk || t == kTdv;
+    const long long ext[3] = {sh.B, sh.H, key ? sh.total_k : sh.total_q};
+    for (int i = 0; i < 3; ++i) {
+      const long long v = strides[3 * t + i];
+      if (v < 0 || (v == 0 && ext[i] > 1))
+        return fail(SDPA_ERR_ARG, "stride %d of %s is %lld: strides must be positive", i, names[t], v);
+      if (dtype != SDPA_F32 && v % 8 != 0)
+        return fail(SDPA_ERR_ARG, "stride %d of %s is %lld: fp16/bf16 strides must be multiples of 8 elements", i,
+                    names[t], v);
+    }
+  }
+  return SDPA_OK;
+}
+
+void set_strides(Problem& p, const long long* strides, int n) {
+  if (strides == nullptr) return;
+  p.strided = 1;
+  for (int t = 0; t < n; ++t)
+    for (int i = 0; i < 3; ++i) p.st[t][i] = strides[3 * t + i];
 }
 
 int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o, float* lse, float scale,
             int is_causal, int dtype, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0}, bool sparse = false,
             const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false,
-            const Dropout& dr = Dropout{0.f, 0ull}) {
+            const Dropout& dr = Dropout{0.f, 0ull}, const long long* strides = nullptr) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
@@ -281,8 +344,10 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
   if (sparse && (rc = check_mask(sh, bm, false)) != SDPA_OK) return rc;
   if (masked && (rc = check_addmask(sh, am, dtype)) != SDPA_OK) return rc;
   if (!(dr.p >= 0.f && dr.p < 1.f)) return fail(SDPA_ERR_ARG, "dropout probability must be in [0, 1) (got %g)", dr.p);
+  if (strides != nullptr && (rc = check_strides(sh, strides, 4, dtype)) != SDPA_OK) return rc;
   Problem p{};
   fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am, dr);
+  set_strides(p, strides, 4);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -298,9 +363,12 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
   if (rc != SDPA_OK) return rc;
   const bool packed = sh.packed();
   FwdMaps maps{};
-  if ((rc = make_operand_map(&maps.q, q, dtype, packed, sh.B, sh.H, sh.total_q, sh.d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.k, k, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.q, q, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, p.st[kTq], p.strided)) != SDPA_OK)
+    return rc;
+  if ((rc = make_operand_map(&maps.k, k, dtype, packed, sh.B, sh.H, sh.total_k, sh.d, p.st[kTk], p.strided)) != SDPA_OK)
+    return rc;
+  if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d, p.st[kTv], p.strided)) != SDPA_OK)
+    return rc;
   // additive mask: each softmax warp loads its 32 rows of a 128-key block as two 64-key boxes
   if (masked &&
       (rc = make_mask_map(&maps.mask, am.m, dtype, sh.B, sh.H, sh.total_q, sh.total_k, am.sb, am.sh, am.sq, 64, 32)) !=
@@ -317,7 +385,7 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
             const void* dO, void* dq, void* dk, void* dv, float scale, int is_causal, int dtype, void* workspace,
             size_t workspace_bytes, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0},
             bool sparse = false, const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false,
-            const Dropout& dr = Dropout{0.f, 0ull}) {
+            const Dropout& dr = Dropout{0.f, 0ull}, const long long* strides = nullptr) {
   g_last_error.clear();
   bool noop = false;
   int rc = check_shape(sh, scale, is_causal, dtype, &noop);
@@ -338,9 +406,11 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace == nullptr ? 0 : workspace_bytes);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(SDPA_ERR_ARG, "workspace must be 256-byte aligned");
 
+  if (strides != nullptr && (rc = check_strides(sh, strides, kTensors, dtype)) != SDPA_OK) return rc;
   BwdProblem bp{};
   Problem& p = bp.f;
   fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am, dr);
+  set_strides(p, strides, kTensors);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
@@ -362,10 +432,16 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
   if (rc != SDPA_OK) return rc;
   BwdMaps maps{};
   const uint32_t bq = sh.d == 128 ? 64 : 128;  // query rows per backward step
-  if ((rc = make_operand_map(&maps.q, q, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, bq)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.k, k, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d)) != SDPA_OK) return rc;
-  if ((rc = make_operand_map(&maps.dO, dO, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, bq)) != SDPA_OK) return rc;
+  if ((rc = make_operand_map(&maps.q, q, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, p.st[kTq], p.strided, bq)) !=
+      SDPA_OK)
+    return rc;
+  if ((rc = make_operand_map(&maps.k, k, dtype, packed, sh.B, sh.H, sh.total_k, sh.d, p.st[kTk], p.strided)) != SDPA_OK)
+    return rc;
+  if ((rc = make_operand_map(&maps.v, v, dtype, packed, sh.B, sh.H, sh.total_k, sh.d, p.st[kTv], p.strided)) != SDPA_OK)
+    return rc;
+  if ((rc = make_operand_map(&maps.dO, dO, dtype, packed, sh.B, sh.H, sh.total_q, sh.d, p.st[kTdo], p.strided, bq)) !=
+      SDPA_OK)
+    return rc;
   if (masked &&
       (rc = make_mask_map(&maps.mask, am.m, dtype, sh.B, sh.H, sh.total_q, sh.total_k, am.sb, am.sh, am.sq, 128, 32)) !=
           SDPA_OK)
@@ -393,6 +469,15 @@ extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* o, fl
   return run_fwd(self_shape(B, H, Lq, Lk, d, cu_seqlens), q, k, v, o, lse, scale, is_causal, dtype, stream);
 }
 
+extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int Lq, int Lk, int d, float scale, int is_causal, const long long* strides,
+                                int dtype, void* stream) {
+  g_last_error.clear();
+  if (strides == nullptr) return fail(SDPA_ERR_ARG, "stride array is NULL");
+  return run_fwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, scale, is_causal, dtype, stream,
+                 BlockMask{nullptr, 0, 0, 0}, false, AddMask{nullptr, 0, 0, 0}, false, Dropout{0.f, 0ull}, strides);
+}
+
 extern "C" int sdpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int nseq, int H,
                                int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, float scale,
                                int is_causal, const int* cu_seqlens_q, const int* cu_seqlens_k, int dtype,
@@ -418,6 +503,17 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
                         const int* cu_seqlens, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
   return run_bwd(self_shape(B, H, Lq, Lk, d, cu_seqlens), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
                  workspace, workspace_bytes, stream);
+}
+
+extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                const void* dO, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+                                float scale, int is_causal, const long long* strides, int dtype, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  if (strides == nullptr) return fail(SDPA_ERR_ARG, "stride array is NULL");
+  return run_bwd(self_shape(B, H, Lq, Lk, d, nullptr), q, k, v, o, lse, dO, dq, dk, dv, scale, is_causal, dtype,
+                 workspace, workspace_bytes, stream, BlockMask{nullptr, 0, 0, 0}, false, AddMask{nullptr, 0, 0, 0},
+                 false, Dropout{0.f, 0ull}, strides);
 }
 
 extern "C" int sdpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,

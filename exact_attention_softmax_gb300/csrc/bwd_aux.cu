@@ -21,117 +21,144 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// Row r (0 <= r < rows) of the flattened query side -> (element offset, stat offset).
-// Dense: r = (b*H + h)*Lq + i, element offset r*d, stat offset r.
-// Packed: r = tok*H + h (memory order), stat offset h*total + tok.
-__device__ __forceinline__ void row_offsets(const Problem& p, long long r, long long& elem, long long& stat) {
-  elem = r * p.d;
-  if (p.cu_seqlens == nullptr) {
-    stat = r;
-  } else {
-    const long long tok = r / p.H, h = r % p.H;
-    stat = h * p.Lq + tok;
-  }
+// Row offsets. Dense: unit u = b*H + h holds rows r = u*Lq + i of the
+// contiguous fp32 dQ accumulator (offset r*d) and of the statistics (offset
+// r); its tensors are addressed at their strides. Packed: r = tok*H + h
+// (memory order, every tensor [total, H, d]), statistic at h*total + tok.
+__device__ __forceinline__ long long packed_stat(const Problem& p, long long r) {
+  const long long tok = r / p.H, h = r % p.H;
+  return h * p.Lq + tok;
 }
 
 // One group of `lanes` threads per row, each lane covering 8 consecutive
-// elements; the group reduces with shuffles.
+// elements; the group reduces with shuffles. Dense: blockIdx.y walks the
+// (batch, head) units and x the rows of a unit, so no thread divides by a
+// run-time size; packed: x walks all rows.
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdProblem bp, long long rows, int lanes, int zero_acc) {
+__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdProblem bp, long long rows_per_unit, int lanes, int zero_acc) {
   const Problem& p = bp.f;
+  const bool dense = p.cu_seqlens == nullptr;
+  const int units = dense ? p.B * p.H : 1;
   const int rows_per_warp = 32 / lanes;
   const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x & 31;
-  const long long r = warp * rows_per_warp + lane / lanes;
+  const long long i = warp * rows_per_warp + lane / lanes;    // row within the unit
   const int sub = lane % lanes;
-  const bool live = r < rows;
-  long long elem = 0, stat = 0;
-  if (live) row_offsets(p, r, elem, stat);
-  const T* O = static_cast<const T*>(p.o) + elem;
-  const T* dO = static_cast<const T*>(bp.dO) + elem;
-  float acc = 0.f;
-  if (sizeof(T) == 2) {
-    // fp16 / bf16 (d a multiple of 8, rows 16-byte aligned): one 16-byte load
-    // of O and of dO per lane, and two 16-byte stores of zeros
-    if (live && sub * 8 < p.d) {
-      const uint4 ov = *reinterpret_cast<const uint4*>(O + sub * 8);
-      const uint4 gv = *reinterpret_cast<const uint4*>(dO + sub * 8);
-      const T* oe = reinterpret_cast<const T*>(&ov);
-      const T* ge = reinterpret_cast<const T*>(&gv);
+  for (int u = blockIdx.y; u < units; u += gridDim.y) {
+    const bool live = i < rows_per_unit;
+    const long long r = static_cast<long long>(u) * rows_per_unit + i;
+    long long eo = 0, edo = 0;
+    if (live) {
+      eo = p.strided ? dense_off(p, kTo, u / p.H, u % p.H, i) : r * p.d;
+      edo = p.strided ? dense_off(p, kTdo, u / p.H, u % p.H, i) : r * p.d;
+    }
+    const long long elem = r * p.d;
+    const T* O = static_cast<const T*>(p.o) + eo;
+    const T* dO = static_cast<const T*>(bp.dO) + edo;
+    float acc = 0.f;
+    if (sizeof(T) == 2) {
+      // fp16 / bf16 (d a multiple of 8, rows 16-byte aligned): one 16-byte load
+      // of O and of dO per lane, and two 16-byte stores of zeros
+      if (live && sub * 8 < p.d) {
+        const uint4 ov = *reinterpret_cast<const uint4*>(O + sub * 8);
+        const uint4 gv = *reinterpret_cast<const uint4*>(dO + sub * 8);
+        const T* oe = reinterpret_cast<const T*>(&ov);
+        const T* ge = reinterpret_cast<const T*>(&gv);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc = fmaf(to_f<T>(oe[e]), to_f<T>(ge[e]), acc);
-      if (zero_acc) {
-        float4* A = reinterpret_cast<float4*>(bp.dq_acc + elem + sub * 8);
-        A[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        A[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < 8; ++e) acc = fmaf(to_f<T>(oe[e]), to_f<T>(ge[e]), acc);
+        if (zero_acc) {
+          float4* A = reinterpret_cast<float4*>(bp.dq_acc + elem + sub * 8);
+          A[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          A[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-    }
-  } else if (live) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int c = sub * 8 + e;
-      if (c < p.d) acc = fmaf(to_f<T>(O[c]), to_f<T>(dO[c]), acc);
-    }
-    if (zero_acc) {
-      float* A = bp.dq_acc + elem;
+    } else if (live) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int c = sub * 8 + e;
-        if (c < p.d) A[c] = 0.f;
+        if (c < p.d) acc = fmaf(to_f<T>(O[c]), to_f<T>(dO[c]), acc);
+      }
+      if (zero_acc) {
+        float* A = bp.dq_acc + elem;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = sub * 8 + e;
+          if (c < p.d) A[c] = 0.f;
+        }
       }
     }
+    for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && sub == 0) bp.delta[dense ? r : packed_stat(p, r)] = acc;
   }
-  for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (live && sub == 0) bp.delta[stat] = acc;
 }
 
-// Eight elements per thread: two 16-byte loads, one 16-byte store (n is a
-// multiple of 8 on the fp16 / bf16 path, whose head dims are 64 or 128).
-template <typename T>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq,
-                                                         long long n, float scale) {
-  const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-  if (i + 7 < n) {
-    const float4 a = *reinterpret_cast<const float4*>(acc + i);
-    const float4 b = *reinterpret_cast<const float4*>(acc + i + 4);
+// Eight elements of one row per thread (the fp16 / bf16 head dims, 64 or
+// 128, are multiples of 8): two 16-byte loads of the contiguous accumulator,
+// one 16-byte store into dQ at its strides. Dense: blockIdx.y walks the units
+// and x the chunks of a unit; packed ([total, H, d], contiguous): x walks all.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const BwdProblem bp, long long chunks_per_unit) {
+  const Problem& p = bp.f;
+  const bool dense = p.cu_seqlens == nullptr;
+  const int units = dense ? p.B * p.H : 1;
+  constexpr int kChunks = D / 8;                           // chunks per row
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= chunks_per_unit) return;
+  const long long i = t / kChunks;                         // row within the unit
+  const int c = static_cast<int>(t % kChunks) * 8;
+  const float scale = p.scale;
+  for (int u = blockIdx.y; u < units; u += gridDim.y) {
+    const long long a_off = (static_cast<long long>(u) * chunks_per_unit + t) * 8;
+    const long long q_off = p.strided ? dense_off(p, kTdq, u / p.H, u % p.H, i) + c : a_off;
+    const float4 a = *reinterpret_cast<const float4*>(bp.dq_acc + a_off);
+    const float4 b = *reinterpret_cast<const float4*>(bp.dq_acc + a_off + 4);
     __align__(16) T out[8] = {from_f<T>(a.x * scale), from_f<T>(a.y * scale), from_f<T>(a.z * scale),
                               from_f<T>(a.w * scale), from_f<T>(b.x * scale), from_f<T>(b.y * scale),
                               from_f<T>(b.z * scale), from_f<T>(b.w * scale)};
-    *reinterpret_cast<uint4*>(dq + i) = *reinterpret_cast<const uint4*>(out);
-  } else {
-    for (long long j = i; j < n; ++j) dq[j] = from_f<T>(acc[j] * scale);
+    *reinterpret_cast<uint4*>(static_cast<T*>(bp.dq) + q_off) = *reinterpret_cast<const uint4*>(out);
   }
 }
 
-long long query_rows(const Problem& p) {
-  return static_cast<long long>(p.cu_seqlens == nullptr ? p.B : 1) * p.H * p.Lq;
+// Rows of one unit (dense) or of the whole packed batch.
+long long rows_per_unit(const Problem& p) {
+  return p.cu_seqlens == nullptr ? static_cast<long long>(p.Lq) : static_cast<long long>(p.H) * p.Lq;
+}
+
+unsigned unit_blocks(const Problem& p) {
+  const long long u = p.cu_seqlens == nullptr ? static_cast<long long>(p.B) * p.H : 1;
+  return static_cast<unsigned>(u < 65535 ? u : 65535);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_prep(const BwdProblem& bp, int dtype, int zero_dq_acc, cudaStream_t s) {
   const Problem& p = bp.f;
-  const long long rows = query_rows(p);
-  if (rows == 0) return cudaSuccess;
+  const long long rows = rows_per_unit(p);
+  if (rows == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
   int lanes = 1;
   while (lanes * 8 < p.d) lanes *= 2;
   const long long threads = (rows + (32 / lanes) - 1) / (32 / lanes) * 32;
-  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-  if (dtype == kF32) bwd_prep_kernel<float><<<blocks, 256, 0, s>>>(bp, rows, lanes, zero_dq_acc);
-  else if (dtype == kF16) bwd_prep_kernel<__half><<<blocks, 256, 0, s>>>(bp, rows, lanes, zero_dq_acc);
-  else bwd_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(bp, rows, lanes, zero_dq_acc);
+  const dim3 grid(static_cast<unsigned>((threads + 255) / 256), unit_blocks(p));
+  if (dtype == kF32) bwd_prep_kernel<float><<<grid, 256, 0, s>>>(bp, rows, lanes, zero_dq_acc);
+  else if (dtype == kF16) bwd_prep_kernel<__half><<<grid, 256, 0, s>>>(bp, rows, lanes, zero_dq_acc);
+  else bwd_prep_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(bp, rows, lanes, zero_dq_acc);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dq_convert(const BwdProblem& bp, int dtype, cudaStream_t s) {
   const Problem& p = bp.f;
-  const long long n = query_rows(p) * p.d;
-  if (n == 0) return cudaSuccess;
-  const unsigned blocks = static_cast<unsigned>((n / 8 + 255) / 256 + 1);
-  if (dtype == kF16)
-    dq_convert_kernel<__half><<<blocks, 256, 0, s>>>(bp.dq_acc, static_cast<__half*>(bp.dq), n, p.scale);
-  else
-    dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(bp.dq_acc, static_cast<__nv_bfloat16*>(bp.dq), n, p.scale);
+  const long long chunks = rows_per_unit(p) * p.d / 8;
+  if (chunks == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((chunks + 255) / 256), unit_blocks(p));
+  if (p.d == 64) {
+    if (dtype == kF16) dq_convert_kernel<__half, 64><<<grid, 256, 0, s>>>(bp, chunks);
+    else dq_convert_kernel<__nv_bfloat16, 64><<<grid, 256, 0, s>>>(bp, chunks);
+  } else if (p.d == 128) {
+    if (dtype == kF16) dq_convert_kernel<__half, 128><<<grid, 256, 0, s>>>(bp, chunks);
+    else dq_convert_kernel<__nv_bfloat16, 128><<<grid, 256, 0, s>>>(bp, chunks);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

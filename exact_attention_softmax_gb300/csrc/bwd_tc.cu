@@ -179,14 +179,14 @@ __device__ __forceinline__ void transpose16_bytes(uint32_t (&w)[4], int hl) {
 }
 
 // EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask
-// (p.amask), 3 dropout (p.dropout).
+// (p.amask), 3 dropout (p.dropout), 4 plain on strided tensors (p.strided).
 template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmM) {
   using C = BCfg<D, EXT>;
-  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3;
+  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3, STRIDED = EXT == 4;
   constexpr int BQ = C::BQ;
   constexpr int NH = C::kHalf;     // query columns per softmax group
   // The additive mask and dropout need registers of their own, so their
@@ -305,16 +305,22 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
    regs_dec<kRegsOther>();
    if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // boxes: packed (column, head, token); dense (column, row, unit), or
+    // (column, row, head, batch) through 4-D maps of strided tensors
+    auto load = [&](void* dst, const CUtensorMap* m, uint64_t* bar, int col, int row, int tok) {
+      if constexpr (PACKED) tma_load_3d(dst, m, bar, col, head, tok + row);
+      else if constexpr (STRIDED) tma_load_4d(dst, m, bar, col, row, unit % p.H, unit / p.H);
+      else tma_load_3d(dst, m, bar, col, row, unit);
+    };
     if (lane == 0 && !*abort_flag) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
       mbar_expect_tx(&bars->kv, 2 * C::kKTile);
-      const int c1 = PACKED ? head : key0, c2 = PACKED ? tok0k + key0 : unit;
       for (int cb = 0; cb < C::kNBlk; ++cb) {
-        tma_load_3d(smem + C::kOffK + cb * C::kKColBlk, &tmK, &bars->kv, cb * C::kBlk, c1, c2);
-        tma_load_3d(smem + C::kOffV + cb * C::kKColBlk, &tmV, &bars->kv, cb * C::kBlk, c1, c2);
+        load(smem + C::kOffK + cb * C::kKColBlk, &tmK, &bars->kv, cb * C::kBlk, key0, tok0k);
+        load(smem + C::kOffV + cb * C::kKColBlk, &tmV, &bars->kv, cb * C::kBlk, key0, tok0k);
       }
     }
     const float* lse = p.lse + stat0;
@@ -345,12 +351,11 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       const int q0 = qstep(s) * BQ;
       if (lane == 0) {
         mbar_expect_tx_only(&bars->full[stage], 2 * C::kQTile);
-        const int c1 = PACKED ? head : q0, c2 = PACKED ? tok0 + q0 : unit;
         for (int cb = 0; cb < C::kNBlk; ++cb) {
-          tma_load_3d(smem + C::kOffQ + stage * C::kQTile + cb * C::kQColBlk, &tmQ, &bars->full[stage],
-                      cb * C::kBlk, c1, c2);
-          tma_load_3d(smem + C::kOffDO + stage * C::kQTile + cb * C::kQColBlk, &tmDO, &bars->full[stage],
-                      cb * C::kBlk, c1, c2);
+          load(smem + C::kOffQ + stage * C::kQTile + cb * C::kQColBlk, &tmQ, &bars->full[stage], cb * C::kBlk, q0,
+               tok0);
+          load(smem + C::kOffDO + stage * C::kQTile + cb * C::kQColBlk, &tmDO, &bars->full[stage], cb * C::kBlk, q0,
+               tok0);
         }
       }
       float* st = stat + stage * 2 * BQ;
@@ -684,7 +689,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       const uint32_t col0 = half == 0 ? C::kTdV : C::kTdK;
       const float sc = half == 0 ? 1.f : p.scale;
       T* out = static_cast<T*>(half == 0 ? bp.dv : bp.dk) +
-               (PACKED ? row0k + static_cast<long long>(key) * rstride : (static_cast<long long>(unit) * Lk + key) * D);
+               (PACKED    ? row0k + static_cast<long long>(key) * rstride
+                : STRIDED ? dense_off(p, half == 0 ? kTdv : kTdk, unit / p.H, unit % p.H, key)
+                          : (static_cast<long long>(unit) * Lk + key) * D);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -760,6 +767,8 @@ cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
     return bp.f.causal ? launch_one<D, T, true, false, 2>(bp, m, s) : launch_one<D, T, false, false, 2>(bp, m, s);
   if (bp.f.dropout)
     return bp.f.causal ? launch_one<D, T, true, false, 3>(bp, m, s) : launch_one<D, T, false, false, 3>(bp, m, s);
+  if (bp.f.strided)
+    return bp.f.causal ? launch_one<D, T, true, false, 4>(bp, m, s) : launch_one<D, T, false, false, 4>(bp, m, s);
   if (bp.f.cu_seqlens != nullptr)
     return bp.f.causal ? launch_one<D, T, true, true, 0>(bp, m, s) : launch_one<D, T, false, true, 0>(bp, m, s);
   return bp.f.causal ? launch_one<D, T, true, false, 0>(bp, m, s) : launch_one<D, T, false, false, 0>(bp, m, s);

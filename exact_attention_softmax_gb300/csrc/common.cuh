@@ -17,8 +17,11 @@ constexpr int kDebugDropQArrive = 1;  // forward producer never loads Q: every w
 
 enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
+// Tensors of a call, for their dense-layout strides (Problem::st).
+enum Tensor : int { kTq = 0, kTk, kTv, kTo, kTdo, kTdq, kTdk, kTdv, kTensors };
+
 // One attention problem as the kernels see it. Dense: q/o [B,H,Lq,d],
-// k/v [B,H,Lk,d], lse [B,H,Lq]. Packed (cu_seqlens != nullptr): B sequences;
+// k/v [B,H,Lk,d] at any element strides (Problem::st), lse [B,H,Lq]. Packed (cu_seqlens != nullptr): B sequences;
 // q/o [Lq = total query tokens, H, d] with sequence s at rows
 // cu_seqlens[s]..cu_seqlens[s+1]; k/v [total_k, H, d] with rows from cu_k
 // (cu_k == cu_seqlens for self-attention); lse [H, Lq]; max_q and Lk bound the
@@ -54,7 +57,22 @@ struct Problem {
   unsigned drop_t;             // round(p * 256), 0..255
   float drop_scale;            // 256 / (256 - drop_t)
   unsigned seed_lo, seed_hi;
+  // Dense layout: element strides (batch, head, row) of every tensor of the
+  // call, indexed by Tensor; the head dim is contiguous. (Packed batches are
+  // [total, H, d] and ignore these.)
+  long long st[kTensors][3];
+  // 1 for a call on strided dense tensors (the *_strided entry points): its
+  // tensor maps are 4-D {d, L, H, B}, boxes addressed (column, row, head,
+  // batch), and it runs kernel variants of their own; 0 for contiguous
+  // tensors, whose maps are 3-D {d, L, B*H} addressed (column, row, unit).
+  int strided;
 };
+
+// Element offset of row `row` of unit (b, h) in dense tensor `t`.
+__host__ __device__ __forceinline__ long long dense_off(const Problem& p, int t, long long b, long long h,
+                                                        long long row) {
+  return b * p.st[t][0] + h * p.st[t][1] + row * p.st[t][2];
+}
 
 // Rows and keys per block of a block-sparse mask.
 constexpr int kMaskBlock = 128;

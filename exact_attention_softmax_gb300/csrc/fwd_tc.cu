@@ -248,14 +248,14 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
 }
 
 // EXT (dense layout only): 0 plain, 1 block-sparse (p.bmask), 2 additive mask
-// (p.amask), 3 dropout (p.dropout).
+// (p.amask), 3 dropout (p.dropout), 4 plain on strided tensors (p.strided).
 template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmM, unsigned* sched) {
   using C = Cfg<D, EXT>;
-  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3;
+  constexpr bool SPARSE = EXT == 1, BIAS = EXT == 2, DROP = EXT == 3, STRIDED = EXT == 4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
@@ -335,9 +335,13 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         const Item it = decode_item<CAUSAL, PACKED, SPARSE>(p, idx, npairs);
         idx = static_cast<int>(atomicAdd(sched, 1u)) + static_cast<int>(gridDim.x);
         if (it.nmax == 0) continue;
-        auto c1 = [&](int row) { return PACKED ? it.h : row; };
-        auto c2 = [&](int row) { return PACKED ? it.tok0 + row : it.unit; };      // query rows
-        auto c2k = [&](int row) { return PACKED ? it.tok0k + row : it.unit; };    // key rows
+        // boxes: packed (column, head, token); dense (column, row, unit), or
+        // (column, row, head, batch) through the 4-D maps of strided tensors
+        auto load = [&](void* dst, const CUtensorMap* m, uint64_t* bar, int col, int row, int tok0) {
+          if constexpr (PACKED) tma_load_3d(dst, m, bar, col, it.h, tok0 + row);
+          else if constexpr (STRIDED) tma_load_4d(dst, m, bar, col, row, it.unit % p.H, it.unit / p.H);
+          else tma_load_3d(dst, m, bar, col, row, it.unit);
+        };
         for (int t = 0; t < 2 && ok; ++t) {
           if ((t == 0 ? it.n0 : it.n1) == 0) continue;
           // buffer qb of tile t was last used kQBufs loads ago
@@ -348,8 +352,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           mbar_expect_tx(&bars->q_full[qb], C::kTileBytes);
           const int row = it.r0 + t * BM;
           for (int cb = 0; cb < C::kNBlk; ++cb)
-            tma_load_3d(smem + C::kOffQ + qb * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[qb],
-                        cb * C::kBlk, c1(row), c2(row));
+            load(smem + C::kOffQ + qb * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[qb], cb * C::kBlk,
+                 row, it.tok0);
         }
         constexpr bool sparse = SPARSE;
         int jk = -1;               // key block of the current loaded block
@@ -363,8 +367,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             const CUtensorMap* m = kv ? &tmV : &tmK;
             const int row = jk * BN;
             for (int cb = 0; cb < C::kNBlk; ++cb)
-              tma_load_3d(smem + C::kOffSlots + slot * C::kTileBytes + cb * C::kColBlkBytes, m, &bars->full[slot],
-                          cb * C::kBlk, c1(row), c2k(row));
+              load(smem + C::kOffSlots + slot * C::kTileBytes + cb * C::kColBlkBytes, m, &bars->full[slot],
+                   cb * C::kBlk, row, it.tok0k);
           }
         }
       }
@@ -850,8 +854,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       pend.on = true;
       pend.m = m_run;
       pend.l = l;
-      pend.orow = row < it.len_q ? (PACKED ? (static_cast<long long>(it.tok0 + row) * p.H + it.h) * D
-                                           : (static_cast<long long>(it.unit) * it.len_q + row) * D)
+      pend.orow = row < it.len_q ? (PACKED    ? (static_cast<long long>(it.tok0 + row) * p.H + it.h) * D
+                                    : STRIDED ? dense_off(p, kTo, it.unit / p.H, it.unit % p.H, row)
+                                              : (static_cast<long long>(it.unit) * it.len_q + row) * D)
                                  : -1;
       pend.li = PACKED ? static_cast<long long>(it.h) * p.Lq + it.tok0 + row
                        : static_cast<long long>(it.unit) * it.len_q + row;
@@ -933,6 +938,8 @@ cudaError_t launch_d(const Problem& p, const FwdMaps& m, cudaStream_t s) {
     return p.causal ? launch_one<D, T, true, false, 2>(p, m, s) : launch_one<D, T, false, false, 2>(p, m, s);
   if (p.dropout)
     return p.causal ? launch_one<D, T, true, false, 3>(p, m, s) : launch_one<D, T, false, false, 3>(p, m, s);
+  if (p.strided)
+    return p.causal ? launch_one<D, T, true, false, 4>(p, m, s) : launch_one<D, T, false, false, 4>(p, m, s);
   if (p.causal)
     return packed ? launch_one<D, T, true, true, 0>(p, m, s) : launch_one<D, T, true, false, 0>(p, m, s);
   return packed ? launch_one<D, T, false, true, 0>(p, m, s) : launch_one<D, T, false, false, 0>(p, m, s);

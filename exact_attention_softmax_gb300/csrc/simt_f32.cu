@@ -22,9 +22,9 @@ constexpr int kTile = 32;    // rows of the other operand staged per step
 
 struct Unit {
   int len_q, len_k;   // rows of this (batch|sequence, head)
-  long long base;     // element offset of query row 0 (q, o, dO, dq)
-  long long kbase;    // element offset of key row 0 (k, v, dk, dv)
-  long long stride;   // elements between consecutive rows
+  int b, h;           // batch (or sequence) and head
+  long long tok0;     // packed: token of query row 0 / key row 0
+  long long tok0k;
   long long stat;     // offset of row 0 in lse / delta
   bool bad;           // packed lengths outside their bounds
 };
@@ -32,24 +32,31 @@ struct Unit {
 __device__ __forceinline__ Unit unit_of(const Problem& p, int b, int h) {
   Unit u;
   u.bad = false;
+  u.b = b;
+  u.h = h;
+  u.tok0 = u.tok0k = 0;
   if (p.cu_seqlens == nullptr) {
     u.len_q = p.Lq;
     u.len_k = p.Lk;
-    u.stride = p.d;
-    u.base = (static_cast<long long>(b) * p.H + h) * p.Lq * p.d;
-    u.kbase = (static_cast<long long>(b) * p.H + h) * p.Lk * p.d;
     u.stat = (static_cast<long long>(b) * p.H + h) * p.Lq;
   } else {
     const int s0 = p.cu_seqlens[b], t0 = p.cu_k[b];
     u.len_q = p.cu_seqlens[b + 1] - s0;
     u.len_k = p.cu_k[b + 1] - t0;
-    u.stride = static_cast<long long>(p.H) * p.d;
-    u.base = static_cast<long long>(s0) * p.H * p.d + static_cast<long long>(h) * p.d;
-    u.kbase = static_cast<long long>(t0) * p.H * p.d + static_cast<long long>(h) * p.d;
+    u.tok0 = s0;
+    u.tok0k = t0;
     u.stat = static_cast<long long>(h) * p.Lq + s0;
     u.bad = u.len_q > p.max_q || u.len_k > p.Lk || (u.len_q > 0 && u.len_k <= 0);
   }
   return u;
+}
+
+// Element offset of row `row` of the unit in tensor `t`: dense at the
+// tensor's strides, packed [total, H, d] on the query or key token axis.
+__device__ __forceinline__ long long row_off(const Problem& p, const Unit& u, int t, long long row) {
+  if (p.cu_seqlens == nullptr) return dense_off(p, t, u.b, u.h, row);
+  const bool key = t == kTk || t == kTv || t == kTdk || t == kTdv;
+  return ((key ? u.tok0k : u.tok0) + row) * p.H * p.d + static_cast<long long>(u.h) * p.d;
 }
 
 // Dropout factor of score (i, j) of dense unit `unit` (see Problem::dropout).
@@ -75,10 +82,9 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
   const int row = row0 + threadIdx.x;
   const bool live = row < u.len_q;
   const int d = p.d;
-  const float* Q = static_cast<const float*>(p.q) + u.base;
-  const long long kvb = u.kbase;
-  const float* K = static_cast<const float*>(p.k) + kvb;
-  const float* V = static_cast<const float*>(p.v) + kvb;
+  const float* Q = static_cast<const float*>(p.q) + row_off(p, u, kTq, row);
+  const float* K = static_cast<const float*>(p.k);
+  const float* V = static_cast<const float*>(p.v);
 
   __shared__ float sk[kTile][DMAX];
   __shared__ float sv[kTile][DMAX];
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
   float qr[DMAX], acc[DMAX];
 #pragma unroll
   for (int c = 0; c < DMAX; ++c) {
-    qr[c] = (live && c < d) ? Q[row * u.stride + c] : 0.f;
+    qr[c] = (live && c < d) ? Q[c] : 0.f;
     acc[c] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -99,8 +105,8 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
     for (int e = threadIdx.x; e < kTile * DMAX; e += kRows) {
       const int r = e / DMAX, c = e % DMAX;
       const bool ok = (kb + r < u.len_k) && c < d;
-      sk[r][c] = ok ? K[(kb + r) * u.stride + c] : 0.f;
-      sv[r][c] = ok ? V[(kb + r) * u.stride + c] : 0.f;
+      sk[r][c] = ok ? K[row_off(p, u, kTk, kb + r) + c] : 0.f;
+      sv[r][c] = ok ? V[row_off(p, u, kTv, kb + r) + c] : 0.f;
     }
     __syncthreads();
     if (!live) continue;
@@ -129,12 +135,12 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
     }
   }
   if (!live) return;
-  float* O = static_cast<float*>(p.o) + u.base;
+  float* O = static_cast<float*>(p.o) + row_off(p, u, kTo, row);
   // a row with no visible key (block-sparse only) gets O = 0 and LSE = -inf
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int c = 0; c < DMAX; ++c)
-    if (c < d) O[row * u.stride + c] = acc[c] * inv;
+    if (c < d) O[c] = acc[c] * inv;
   p.lse[u.stat + row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
@@ -149,19 +155,18 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
   const int row = row0 + threadIdx.x;
   const bool live = row < u.len_q;
   const int d = p.d;
-  const long long kvb = u.kbase;
-  const float* Q = static_cast<const float*>(p.q) + u.base;
-  const float* dO = static_cast<const float*>(bp.dO) + u.base;
-  const float* K = static_cast<const float*>(p.k) + kvb;
-  const float* V = static_cast<const float*>(p.v) + kvb;
+  const float* Q = static_cast<const float*>(p.q) + row_off(p, u, kTq, row);
+  const float* dO = static_cast<const float*>(bp.dO) + row_off(p, u, kTdo, row);
+  const float* K = static_cast<const float*>(p.k);
+  const float* V = static_cast<const float*>(p.v);
 
   __shared__ float sk[kTile][DMAX];
   __shared__ float sv[kTile][DMAX];
   float qr[DMAX], dor[DMAX], dq[DMAX];
 #pragma unroll
   for (int c = 0; c < DMAX; ++c) {
-    qr[c] = (live && c < d) ? Q[row * u.stride + c] : 0.f;
-    dor[c] = (live && c < d) ? dO[row * u.stride + c] : 0.f;
+    qr[c] = (live && c < d) ? Q[c] : 0.f;
+    dor[c] = (live && c < d) ? dO[c] : 0.f;
     dq[c] = 0.f;
   }
   const float lse = live ? p.lse[u.stat + row] : 0.f;
@@ -175,8 +180,8 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
     for (int e = threadIdx.x; e < kTile * DMAX; e += kRows) {
       const int r = e / DMAX, c = e % DMAX;
       const bool ok = (kb + r < u.len_k) && c < d;
-      sk[r][c] = ok ? K[(kb + r) * u.stride + c] : 0.f;
-      sv[r][c] = ok ? V[(kb + r) * u.stride + c] : 0.f;
+      sk[r][c] = ok ? K[row_off(p, u, kTk, kb + r) + c] : 0.f;
+      sv[r][c] = ok ? V[row_off(p, u, kTv, kb + r) + c] : 0.f;
     }
     __syncthreads();
     if (!live) continue;
@@ -200,10 +205,10 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
     }
   }
   if (!live) return;
-  float* dQ = static_cast<float*>(bp.dq) + u.base;
+  float* dQ = static_cast<float*>(bp.dq) + row_off(p, u, kTdq, row);
 #pragma unroll
   for (int c = 0; c < DMAX; ++c)
-    if (c < d) dQ[row * u.stride + c] = dq[c] * p.scale;
+    if (c < d) dQ[c] = dq[c] * p.scale;
 }
 
 // dV_j = sum_i P_ij dO_i ; dK_j = scale * sum_i P_ij (dO_i.v_j - D_i) q_i
@@ -217,11 +222,10 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
   const int key = key0 + threadIdx.x;
   const bool live = key < u.len_k;
   const int d = p.d;
-  const long long kvb = u.kbase;
-  const float* Q = static_cast<const float*>(p.q) + u.base;
-  const float* dO = static_cast<const float*>(bp.dO) + u.base;
-  const float* K = static_cast<const float*>(p.k) + kvb;
-  const float* V = static_cast<const float*>(p.v) + kvb;
+  const float* Q = static_cast<const float*>(p.q);
+  const float* dO = static_cast<const float*>(bp.dO);
+  const float* K = static_cast<const float*>(p.k) + row_off(p, u, kTk, key);
+  const float* V = static_cast<const float*>(p.v) + row_off(p, u, kTv, key);
 
   __shared__ float sq[kTile][DMAX];
   __shared__ float sdo[kTile][DMAX];
@@ -229,8 +233,8 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
   float kr[DMAX], vr[DMAX], dk[DMAX], dv[DMAX];
 #pragma unroll
   for (int c = 0; c < DMAX; ++c) {
-    kr[c] = (live && c < d) ? K[key * u.stride + c] : 0.f;
-    vr[c] = (live && c < d) ? V[key * u.stride + c] : 0.f;
+    kr[c] = (live && c < d) ? K[c] : 0.f;
+    vr[c] = (live && c < d) ? V[c] : 0.f;
     dk[c] = 0.f;
     dv[c] = 0.f;
   }
@@ -240,8 +244,8 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
     for (int e = threadIdx.x; e < kTile * DMAX; e += kRows) {
       const int r = e / DMAX, c = e % DMAX;
       const bool ok = (qb + r < u.len_q) && c < d;
-      sq[r][c] = ok ? Q[(qb + r) * u.stride + c] : 0.f;
-      sdo[r][c] = ok ? dO[(qb + r) * u.stride + c] : 0.f;
+      sq[r][c] = ok ? Q[row_off(p, u, kTq, qb + r) + c] : 0.f;
+      sdo[r][c] = ok ? dO[row_off(p, u, kTdo, qb + r) + c] : 0.f;
     }
     if (threadIdx.x < kTile) {
       const int r = qb + threadIdx.x;
@@ -275,13 +279,13 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
     }
   }
   if (!live) return;
-  float* dK = static_cast<float*>(bp.dk) + kvb;
-  float* dV = static_cast<float*>(bp.dv) + kvb;
+  float* dK = static_cast<float*>(bp.dk) + row_off(p, u, kTdk, key);
+  float* dV = static_cast<float*>(bp.dv) + row_off(p, u, kTdv, key);
 #pragma unroll
   for (int c = 0; c < DMAX; ++c) {
     if (c < d) {
-      dK[key * u.stride + c] = dk[c] * p.scale;
-      dV[key * u.stride + c] = dv[c];
+      dK[c] = dk[c] * p.scale;
+      dV[c] = dv[c];
     }
   }
 }

@@ -18,8 +18,8 @@
  *    device that is current for the calling thread. The library allocates
  *    nothing, keeps no reference after the call returns, and runs
  *    asynchronously on `stream` (a cudaStream_t; NULL = legacy default).
- *  - Tensors are contiguous. Element type is `dtype` (sdpa_dtype) for
- *    q/k/v/o/dO/dq/dk/dv; lse is always float32.
+ *  - Tensors are contiguous (except in the *_strided calls). Element type is
+ *    `dtype` (sdpa_dtype) for q/k/v/o/dO/dq/dk/dv; lse is always float32.
  *  - Dense layout (cu_seqlens == NULL): q, o, dO, dq are [B, H, Lq, d];
  *    k, v, dk, dv are [B, H, Lk, d]; lse is [B, H, Lq].
  *  - Packed variable-length layout (cu_seqlens != NULL; the tutorial's
@@ -112,6 +112,24 @@ int sdpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     const int* cu_seqlens_q, const int* cu_seqlens_k, int dtype, void* stream);
 
 /*
+ * Forward over dense tensors at any element strides: the SDPA tutorial's
+ * module (section "Causal Self Attention") projects to [B, L, H * d] and
+ * views it as [B, L, H, d].transpose(1, 2), a [B, H, L, d] tensor whose rows
+ * are H * d elements apart; this call reads and writes such views in place,
+ * with no copy.
+ *   strides : HOST array of 12 element strides, (batch, head, row) for q, k,
+ *             v and o in that order; the head dim is contiguous (stride 1).
+ *             A dimension longer than 1 needs a positive stride; fp16 / bf16
+ *             strides must be multiples of 8 elements (16 bytes) and the
+ *             bases 16-byte aligned. Rows of o must not overlap.
+ *   lse     : contiguous [B, H, Lq] float32, as for sdpa_fwd.
+ * Other arguments, support and errors as for sdpa_fwd with cu_seqlens = NULL.
+ */
+int sdpa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                     const long long* strides, int dtype, void* stream);
+
+/*
  * Bytes of device workspace sdpa_bwd needs for these sizes (a float32 row
  * statistic D = rowsum(dO * O) and a float32 dQ accumulator, both over the
  * query rows). The FlashAttention news article (QbitAI repost, section
@@ -142,6 +160,21 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const f
              int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
              const int* cu_seqlens, int dtype,
              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward over dense tensors at any element strides (the backward of
+ * sdpa_fwd_strided).
+ *   strides : HOST array of 24 element strides, (batch, head, row) for q, k,
+ *             v, o, dO, dq, dk and dv in that order; rules as for
+ *             sdpa_fwd_strided. lse contiguous; the workspace as for sdpa_bwd
+ *             (its fp32 dQ accumulator is contiguous whatever dq's strides).
+ * Other arguments, support and errors as for sdpa_bwd with cu_seqlens = NULL.
+ */
+int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv,
+                     int B, int H, int Lq, int Lk, int d, float scale, int is_causal,
+                     const long long* strides, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward of sdpa_fwd_varlen: dq [total_q, H, d], dk and dv [total_k, H, d],

@@ -169,3 +169,18 @@ def test_trace_events_argument_checks(lib):
     assert lib.sdpa_trace_events(0, FAKE, None) == _abi.SDPA_ERR_ARG
     assert lib.sdpa_trace_events(0, None, None) == _abi.SDPA_OK
     assert lib.sdpa_trace_events(1, None, None) == _abi.SDPA_OK
+
+
+def test_strided_calls_check_their_strides(lib):
+    st = (ctypes.c_longlong * 12)(*([8192, 2048, 64] * 4))
+    ok = lib.sdpa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 32, 32, 64, 0.125, 0, None, 1, None)
+    assert ok == _abi.SDPA_ERR_ARG and b"stride" in lib.sdpa_last_error()
+    bad = (ctypes.c_longlong * 12)(*([8192, 2048, 68] * 4))        # rows 68 elements apart
+    assert lib.sdpa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 32, 32, 64, 0.125, 0, bad, 1, None) == \
+        _abi.SDPA_ERR_ARG
+    assert b"multiples of 8" in lib.sdpa_last_error()
+    neg = (ctypes.c_longlong * 12)(*([8192, -2048, 64] * 4))
+    assert lib.sdpa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 32, 32, 64, 0.125, 0, neg, 1, None) == \
+        _abi.SDPA_ERR_ARG
+    # nothing to compute: returns OK before looking at the strides' values
+    assert lib.sdpa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 0, 32, 64, 0.125, 0, st, 1, None) == _abi.SDPA_OK
