@@ -76,12 +76,19 @@ struct Cfg {
   // The additive-mask kernel gives up K/V ring slots at d >= 64 for its mask
   // slots: one 32-row x 128-key slot per softmax warp (two 64-key boxes).
   static constexpr bool kMask = EXT == 2;
-  static constexpr int kSlots = D == 128 ? (kMask ? 3 : 5) : (D == 64 ? (kMask ? 6 : 10) : 16);
+  // Where each CTA runs many work items (d <= 64) the epilogue stages every
+  // softmax warp's 32 output rows in shared memory, so the global stores go
+  // out row-contiguous (the mask kernel has no room; at d = 128 items are long
+  // and the direct stores cost little). d = 64 gives two K/V slots for it.
+  static constexpr bool kStageO = D <= 64 && !kMask;
+  static constexpr int kSlots = D == 128 ? (kMask ? 3 : 5) : (D == 64 ? (kMask ? 6 : 8) : 16);
   static constexpr int kOffQ = 0;
   static constexpr int kOffSlots = 2 * kQBufs * kTileBytes;
   static constexpr int kMaskWarpBytes = 32 * BN * 2;
   static constexpr int kOffMask = kOffSlots + kSlots * kTileBytes;
-  static constexpr int kOffBar = kOffMask + (kMask ? 8 * kMaskWarpBytes : 0);
+  static constexpr int kStageWarpBytes = 32 * D * 2;          // 32 rows of O
+  static constexpr int kOffStage = kOffMask + (kMask ? 8 * kMaskWarpBytes : 0);
+  static constexpr int kOffBar = kOffStage + (kStageO ? 8 * kStageWarpBytes : 0);
   static constexpr int kSmem = kOffBar + 640 + 1024;          // barriers + alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   // TMEM columns. P (BN fp16/bf16 per row, two per 32-bit column) has its own
@@ -581,7 +588,36 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       // O_t has been read out: the next item's first P.V may overwrite it
       tc_fence_before();
       mbar_arrive(&bars->o_free[t]);
-      if (e.orow >= 0) {
+      if constexpr (C::kStageO) {
+        // The warp's 32 rows go through shared memory: each lane writes its
+        // row as 16-byte chunks (chunk c of row r at slot c ^ f(r), so the 8
+        // lanes of a quarter-warp hit 8 different bank groups), then each
+        // store instruction takes whole rows, 512 contiguous bytes of them
+        // where rows are adjacent, instead of 32 rows of 16 bytes each.
+        constexpr int kChunks = D / 8;                     // 16-byte chunks per row
+        constexpr int kRowsPer = 32 / kChunks;             // rows per store instruction
+        auto slot = [](int r, int c) { return c ^ (kChunks == 8 ? (r & 7) : ((r >> 1) & 3)); };
+        const uint32_t stage = smem_u32(smem + C::kOffStage + warp * C::kStageWarpBytes);
+        __syncwarp();                                      // the previous epilogue's reads are done
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       ::"r"(stage + (lane * kChunks + slot(lane, c)) * 16), "r"(ov[4 * c]), "r"(ov[4 * c + 1]),
+                         "r"(ov[4 * c + 2]), "r"(ov[4 * c + 3]) : "memory");
+        __syncwarp();
+        const int c = lane % kChunks;
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+          const int r = i * kRowsPer + lane / kChunks;     // the row this lane stores a chunk of
+          const long long orow = __shfl_sync(0xffffffffu, e.orow, r);
+          uint4 w;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(stage + (r * kChunks + slot(r, c)) * 16)
+                       : "memory");
+          if (orow >= 0) *reinterpret_cast<uint4*>(static_cast<T*>(p.o) + orow + 8 * c) = w;
+        }
+        if (e.orow >= 0) p.lse[e.li] = e.l > 0.f ? (e.m + __log2f(e.l)) * kLn2 : -INFINITY;
+      } else if (e.orow >= 0) {
         T* orow = static_cast<T*>(p.o) + e.orow;
 #pragma unroll
         for (int x = 0; x < D / 8; ++x)
