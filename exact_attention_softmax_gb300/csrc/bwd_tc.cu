@@ -684,7 +684,11 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_done, 0, abort_flag, p.status));
     if (ok) {
-      // group 0 writes dV, group 1 writes dK = scale * dK_acc
+      // group 0 writes dV, group 1 writes dK = scale * dK_acc. Every MMA that
+      // read the Q/dO stages has finished (kv_done), so each warp stages its
+      // 32 rows there (16-byte chunk c of row r at slot c ^ (r % 8): the 8
+      // lanes of a quarter-warp hit 8 different bank groups) and stores them
+      // back whole rows per instruction instead of 32 rows of 16 bytes.
       tc_fence_after();
       const uint32_t col0 = half == 0 ? C::kTdV : C::kTdK;
       const float sc = half == 0 ? 1.f : p.scale;
@@ -692,6 +696,10 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
                (PACKED    ? row0k + static_cast<long long>(key) * rstride
                 : STRIDED ? dense_off(p, half == 0 ? kTdv : kTdk, unit / p.H, unit % p.H, key)
                           : (static_cast<long long>(unit) * Lk + key) * D);
+      constexpr int kChunks = D / 8;                   // 16-byte chunks per row
+      constexpr int kRowsPer = 32 / kChunks;           // rows per store instruction
+      static_assert(8 * 32 * D * 2 <= 2 * C::kStages * C::kQTile, "the Q/dO stages hold the staged rows");
+      const uint32_t stage = smem_u32(smem + C::kOffQ + warp * 32 * D * 2);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -701,17 +709,28 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (key < Lk) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = Pack2<T>::pack(__uint_as_float(o[8 * e + 0]) * sc, __uint_as_float(o[8 * e + 1]) * sc);
-            w.y = Pack2<T>::pack(__uint_as_float(o[8 * e + 2]) * sc, __uint_as_float(o[8 * e + 3]) * sc);
-            w.z = Pack2<T>::pack(__uint_as_float(o[8 * e + 4]) * sc, __uint_as_float(o[8 * e + 5]) * sc);
-            w.w = Pack2<T>::pack(__uint_as_float(o[8 * e + 6]) * sc, __uint_as_float(o[8 * e + 7]) * sc);
-            *reinterpret_cast<uint4*>(out + cc * 32 + 8 * e) = w;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int chunk = cc * 4 + e;
+          st_shared_v4(stage + (lane * kChunks + (chunk ^ (lane & 7))) * 16,
+                       Pack2<T>::pack(__uint_as_float(o[8 * e + 0]) * sc, __uint_as_float(o[8 * e + 1]) * sc),
+                       Pack2<T>::pack(__uint_as_float(o[8 * e + 2]) * sc, __uint_as_float(o[8 * e + 3]) * sc),
+                       Pack2<T>::pack(__uint_as_float(o[8 * e + 4]) * sc, __uint_as_float(o[8 * e + 5]) * sc),
+                       Pack2<T>::pack(__uint_as_float(o[8 * e + 6]) * sc, __uint_as_float(o[8 * e + 7]) * sc));
         }
+      }
+      __syncwarp();
+      const int c = lane % kChunks;
+      const long long base = reinterpret_cast<long long>(out);
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        const int rr = i * kRowsPer + lane / kChunks;  // the row whose chunk c this lane stores
+        const T* dst = reinterpret_cast<const T*>(__shfl_sync(0xffffffffu, base, rr));
+        uint4 w;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(stage + (rr * kChunks + (c ^ (rr & 7))) * 16)
+                     : "memory");
+        if (key - lane + rr < Lk) *reinterpret_cast<uint4*>(const_cast<T*>(dst) + 8 * c) = w;
       }
     }
   }
