@@ -89,7 +89,11 @@ struct BCfg {
   static constexpr int kMaxSteps = 2048;
   static constexpr int kMaskTile = 32 * BK * 2;
   static constexpr int kMaskSlot = 2 * kMaskTile;
-  static constexpr int kOffList = kOffStat + kStages * BQ * 8;
+  // d = 64: each dQ drain warp stages 32 rows x 32 columns of fp32 (4 KB)
+  // so its reductions go out as whole row segments
+  static constexpr int kDqStageBytes = kDqT ? 0 : 4 * 32 * 32 * 4;
+  static constexpr int kOffDqStage = kOffStat + kStages * BQ * 8;
+  static constexpr int kOffList = kOffDqStage + kDqStageBytes;
   static constexpr int kOffBar = kOffList + (kMask ? 2 * kMaskSlot : kMaxSteps * 2);
   static constexpr int kSmem = kOffBar + 256 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -527,8 +531,13 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
           bulk_commit();
         }
       } else {
-        const int q = q0 + r;
-        float* row = dq_unit + static_cast<long long>(q) * rstride;
+        // lane = query row: each 32-column piece of the warp's 32 rows goes
+        // through its 4 KB staging area (16-byte chunk c of row i at slot
+        // c ^ (i % 8)) and out as 16-byte reductions that cover four whole
+        // 128-byte row segments per instruction, not 32 scattered rows
+        const int lane = threadIdx.x & 31;
+        const int rbase = q0 + (warp & 3) * 32;                  // query row of lane 0
+        const uint32_t stg = smem_u32(smem + C::kOffDqStage + (warp - kDqWarp0) * 4096);
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -538,10 +547,20 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             tc_fence_before();
             mbar_arrive(&bars->dq_free[buf]);
           }
-          if (q < Lq) {
+          __syncwarp();                                          // the previous piece has been read
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              red_add_v4_f32(row + cc * 32 + e * 4, o[e * 4], o[e * 4 + 1], o[e * 4 + 2], o[e * 4 + 3]);
+          for (int e = 0; e < 8; ++e)
+            st_shared_v4(stg + (lane * 8 + (e ^ (lane & 7))) * 16, o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          __syncwarp();
+          const int c = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + lane / 8;
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(stg + (rr * 8 + (c ^ (rr & 7))) * 16) : "memory");
+            if (rbase + rr < Lq)
+              red_add_v4_f32(dq_unit + static_cast<long long>(rbase + rr) * rstride + cc * 32 + c * 4, w0, w1, w2, w3);
           }
         }
       }
