@@ -474,6 +474,13 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           for (int t = t_lo; t < t_hi && ok; ++t) {
             if ((t == 0 ? it.n0 : it.n1) == 0 || pre[t]) continue;
             qbuf[t] = t * C::kQBufs + qloads[t] % C::kQBufs;
+            // With an MMA warp per tile, tile 1 starts the CTA's first item
+            // once tile 0 has handed over its first P, so the two softmax
+            // groups run about half a block apart from then on: one group's
+            // TMEM loads and waits fall under the other's exponentials
+            // instead of both groups loading, then competing for the
+            // exponential unit, at the same moments.
+            if (C::kMmaWarps == 2 && t == 1 && k == 0 && it.n0 > 0 && !(ok = wait(&bars->p_full[0], 0))) break;
             ok = first_qk(it, t, fill);
           }
           if (!ok) break;
