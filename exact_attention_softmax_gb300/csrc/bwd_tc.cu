@@ -7,22 +7,26 @@
 // see it. Per query tile i of BQ rows, with keys on TMEM lanes:
 //
 //   S^T  = K Q_i^T,  dP^T = V dO_i^T                          (tcgen05, TMEM)
-//   P^T  = exp(scale S^T - LSE_i),  dS^T = P^T * (dP^T - D_i)  (CUDA cores -> SMEM)
-//   dV  += P^T dO_i ;  dK += dS^T Q_i                          (tcgen05, TMEM)
+//   P^T  = exp(scale S^T - LSE_i)                              (CUDA cores -> TMEM)
+//   dS^T = P^T * (dP^T - D_i)                                  (CUDA cores -> SMEM)
+//   dV  += P^T dO_i  (A from TMEM);  dK += dS^T Q_i            (tcgen05, TMEM)
 //   dQ_i partial = dS K   (d = 64: M = query rows)
 //             or  (K^T dS^T)^T (d = 128: M = head dims)       (tcgen05, TMEM)
 //
 // and the dQ partial is added into an fp32 accumulator in global memory (one
-// bulk shared->global reduce per tile at d = 128, vector reductions at d = 64). dK = scale * dK_acc and dV are
-// written at the end; dQ = scale * dQ_acc is rounded by a separate kernel.
+// bulk shared->global reduce per tile at d = 128, vector reductions of whole
+// row segments at d = 64). dK = scale * dK_acc and dV are written at the end;
+// dQ = scale * dQ_acc is rounded by a separate kernel.
 //
 // Warps: 0-3 and 4-7 build P^T / dS^T for the first and second half of the
 // tile's queries (then write dV and dK); 8-11 drain dQ; 12 loads with TMA;
 // 13 issues S^T and dP^T; 14 issues dV, dK and dQ; 15 loads the additive
 // mask (masked kernels; it idles otherwise). The softmax
 // groups release S^T / dP^T as soon as they hold them in registers, so the
-// next tile's S^T, dP^T run under their arithmetic, and dQ has two TMEM
-// buffers so its drain overlaps the next tile.
+// next tile's S^T, dP^T run under their arithmetic. P^T goes to TMEM, where
+// the dV MMA reads it, so only dS^T passes through shared memory (whose
+// bandwidth the MMAs' operand reads also use); the one dQ buffer is drained
+// well within a step.
 #include <type_traits>
 
 #include <algorithm>
@@ -78,8 +82,7 @@ struct BCfg {
   static constexpr int kOffV = kOffK + kKTile;
   static constexpr int kOffQ = kOffV + kKTile;                          // kStages Q tiles
   static constexpr int kOffDO = kOffQ + kStages * kQTile;               // kStages dO tiles
-  static constexpr int kOffPT = kOffDO + kStages * kQTile;
-  static constexpr int kOffDST = kOffPT + kPBytes;
+  static constexpr int kOffDST = kOffDO + kStages * kQTile;            // dS^T (P^T lives in TMEM)
   static constexpr int kDqBytes = kDqT ? BQ * D * 4 : 0;     // fp32 dQ staging tile (d = 128 only)
   static constexpr int kOffDQ = kOffDST + kPBytes;
   static constexpr int kOffStat = kOffDQ + kDqBytes;                    // kStages x (lse2[BQ], delta[BQ])
@@ -97,10 +100,13 @@ struct BCfg {
   static constexpr int kOffBar = kOffList + (kMask ? 2 * kMaskSlot : kMaxSteps * 2);
   static constexpr int kSmem = kOffBar + 256 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
-  // TMEM columns: S^T, dP^T, dV, dK, two dQ buffers
+  // TMEM columns: S^T, dP^T, dV, dK, one dQ buffer (its drain takes well
+  // under a step), and P^T (BQ 16-bit values per key row, two per column),
+  // which the dV MMA reads as its A operand, so P^T costs no shared memory
   static constexpr int kDqCols = kDqT ? BQ : D;
   static constexpr uint32_t kTS = 0, kTdP = BQ, kTdV = 2 * BQ, kTdK = 2 * BQ + D, kTdQ = 2 * BQ + 2 * D;
-  static_assert(kTdQ + 2 * kDqCols <= 512, "TMEM budget");
+  static constexpr uint32_t kTP = kTdQ + kDqCols;
+  static_assert(kTP + BQ / 2 <= 512, "TMEM budget");
   static_assert(kStages <= 3, "the barrier arrays hold 3 Q/dO stages");
 };
 
@@ -248,7 +254,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 
   const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
   const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
-  const uint32_t sPT = smem_u32(smem + C::kOffPT), sDST = smem_u32(smem + C::kOffDST);
+  const uint32_t sDST = smem_u32(smem + C::kOffDST);
   float* stat = reinterpret_cast<float*>(smem + C::kOffStat);   // [stage][2][BQ]
 
   if (threadIdx.x == 0) {
@@ -388,8 +394,8 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       const uint64_t dDSm = smem_desc(sDST, C::kPColBlk, 1024, kSwizzle128B);
       auto issue_dq = [&](int t) {
         if (!wait(&bars->pds_full, t & 1)) return false;
-        const int buf = t & 1;
-        if (t >= 2 && !wait(&bars->dq_free[buf], ((t - 2) >> 1) & 1)) return false;
+        const int buf = 0;
+        if (t >= 1 && !wait(&bars->dq_free[0], (t - 1) & 1)) return false;
         tc_fence_after();
         const uint32_t tdq = tmem + C::kTdQ + buf * C::kDqCols;
         // contraction over the 128 keys, both operands MN-major
@@ -439,7 +445,6 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       } else {
         // dV += P^T dO, dK += dS^T Q (A K-major over queries, B MN-major)
         constexpr uint32_t idKV = idesc_f16(fmt, 0, 1, BK, D);
-        const uint64_t dPT = smem_desc(sPT, 16, 1024, kSwizzle128B);
         const uint64_t dDST = smem_desc(sDST, 16, 1024, kSwizzle128B);
         const uint64_t dQm = smem_desc(sQ, C::kQColBlk, C::kSbo, C::kSw);
         const uint64_t dOm = smem_desc(sDO, C::kQColBlk, C::kSbo, C::kSw);
@@ -453,7 +458,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             const uint32_t aoff = ((ks / 4) * C::kPColBlk + (ks % 4) * 32) >> 4;
             const uint32_t boff = qoff + ((ks * 16 * C::kRowBytes) >> 4);
             const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
-            mma_ss(tmem + C::kTdV, dPT + aoff, dOm + boff, idKV, acc);
+            mma_ts(tmem + C::kTdV, tmem + C::kTP + ks * 8, dOm + boff, idKV, acc);
             mma_ss(tmem + C::kTdK, dDST + aoff, dQm + boff, idKV, acc);
           }
           mma_commit(&bars->pds_free);
@@ -499,8 +504,8 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     float* dq_unit = bp.dq_acc + (PACKED ? row0 : static_cast<long long>(unit) * Lq * D);
     const uint32_t sDQ = smem_u32(smem + C::kOffDQ);
     for (int s = 0; s < nsteps; ++s) {
-      const int buf = s & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full[buf], (s >> 1) & 1, abort_flag, p.status))) break;
+      const int buf = 0;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full[0], s & 1, abort_flag, p.status))) break;
       tc_fence_after();
       const int q0 = qstep(s) * BQ;
       const uint32_t tdq = tmem + lane_off + C::kTdQ + buf * C::kDqCols;
@@ -688,16 +693,28 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         // P^T / dS^T buffers are free once the previous tile's dV, dK, dQ MMAs finished
         if (ch == 0 && s > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_free, (s - 1) & 1, abort_flag, p.status));
         if (!ok) break;
-        // [key row][query] in 128-byte swizzled rows, 64 queries per column block
+        // P^T into TMEM (this thread's key row, two queries per column), dS^T
+        // into shared memory: [key row][query] in 128-byte swizzled rows, 64
+        // queries per column block
+        {
+          const uint32_t tp = tmem + lane_off + C::kTP + (half * NH + ch * CH) / 2;
+          if constexpr (CH == 64) {
+            tmem_st32(tp, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+          } else {
+#pragma unroll
+            for (int x = 0; x < CH / 32; ++x) tmem_st16(tp + x * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * x]));
+          }
+        }
 #pragma unroll
         for (int c8 = 0; c8 < CH / 8; ++c8) {
           const int chunk = half * (NH / 8) + ch * (CH / 8) + c8;   // 8-query chunk index within the tile
           const uint32_t off = (chunk / 8) * C::kPColBlk + r * 128 + (((chunk % 8) ^ (r & 7)) << 4);
-          st_shared_v4(sPT + off, pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
           st_shared_v4(sDST + off, dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2], dk[4 * c8 + 3]);
         }
       }
       if (!ok) break;
+      tmem_st_wait();
+      tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&bars->pds_full);
     }
