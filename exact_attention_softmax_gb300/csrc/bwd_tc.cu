@@ -73,8 +73,9 @@ struct BCfg {
   static constexpr int kPBytes = BK * BQ * 2;
   // Q/dO stages: a stage stays busy from its load until the dV/dK MMAs of
   // its step, about one step after its S^T MMA; a third stage lets the next
-  // load start early enough at d = 64 (d = 128, and the additive-mask kernel
-  // with its mask ring, have no room for it)
+  // load start early enough at d = 64 (the additive-mask kernel, with its
+  // mask ring, has no room for it; at d = 128, with dS^T in TMEM, a third
+  // stage measured slower: 5140 against 5091 us on the long causal batch)
   static constexpr bool kMask = EXT == 2;
   static constexpr int kStages = D == 64 && !kMask ? 3 : 2;
   // shared memory map
@@ -106,7 +107,11 @@ struct BCfg {
   static constexpr int kDqCols = kDqT ? BQ : D;
   static constexpr uint32_t kTS = 0, kTdP = BQ, kTdV = 2 * BQ, kTdK = 2 * BQ + D, kTdQ = 2 * BQ + 2 * D;
   static constexpr uint32_t kTP = kTdQ + kDqCols;
-  static_assert(kTP + BQ / 2 <= 512, "TMEM budget");
+  // d = 128 has room for dS^T as well (the dK MMA's A operand; dS^T still
+  // goes to shared memory, where the dQ MMA reads it)
+  static constexpr bool kDsTmem = D == 128;
+  static constexpr uint32_t kTDS = kTP + BQ / 2;
+  static_assert(kTP + BQ / 2 + (kDsTmem ? BQ / 2 : 0) <= 512, "TMEM budget");
   static_assert(kStages <= 3, "the barrier arrays hold 3 Q/dO stages");
 };
 
@@ -459,7 +464,8 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             const uint32_t boff = qoff + ((ks * 16 * C::kRowBytes) >> 4);
             const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
             mma_ts(tmem + C::kTdV, tmem + C::kTP + ks * 8, dOm + boff, idKV, acc);
-            mma_ss(tmem + C::kTdK, dDST + aoff, dQm + boff, idKV, acc);
+            if constexpr (C::kDsTmem) mma_ts(tmem + C::kTdK, tmem + C::kTDS + ks * 8, dQm + boff, idKV, acc);
+            else mma_ss(tmem + C::kTdK, dDST + aoff, dQm + boff, idKV, acc);
           }
           mma_commit(&bars->pds_free);
           mma_commit(&bars->empty[stage]);
@@ -693,12 +699,19 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         // P^T / dS^T buffers are free once the previous tile's dV, dK, dQ MMAs finished
         if (ch == 0 && s > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_free, (s - 1) & 1, abort_flag, p.status));
         if (!ok) break;
-        // P^T into TMEM (this thread's key row, two queries per column), dS^T
-        // into shared memory: [key row][query] in 128-byte swizzled rows, 64
-        // queries per column block
+        // P^T (and at d = 128 dS^T) into TMEM, this thread's key row, two
+        // queries per column; dS^T into shared memory: [key row][query] in
+        // 128-byte swizzled rows, 64 queries per column block
         {
           const uint32_t tp = tmem + lane_off + C::kTP + (half * NH + ch * CH) / 2;
-          if constexpr (CH == 64) {
+          if constexpr (C::kDsTmem) {
+            const uint32_t td = tmem + lane_off + C::kTDS + (half * NH + ch * CH) / 2;
+#pragma unroll
+            for (int x = 0; x < CH / 32; ++x) {
+              tmem_st16(tp + x * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * x]));
+              tmem_st16(td + x * 16, *reinterpret_cast<const uint32_t(*)[16]>(&dk[16 * x]));
+            }
+          } else if constexpr (CH == 64) {
             tmem_st32(tp, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
           } else {
 #pragma unroll
