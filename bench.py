@@ -415,6 +415,20 @@ def extra_results(dev, flush, peaks):
           lambda: ops.sdpa_bwd_blocksparse(q, k, v, o, lse, do, mask, *g, workspace=ws),
           4 * d * kept, 2.5 * 4 * d * kept,
           f"B={B} H={H} L={L} d={d} f16 non-causal, 50 % of 128x128 tiles kept (seeded)")
+    # the dense calls on the same shape, for the block-sparse saving
+    od, ld = torch.empty_like(q), torch.empty(B, H, L, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        ops.sdpa_fwd(q, k, v, od, ld)
+        ops.sdpa_bwd(q, k, v, od, ld, do, *g, workspace=ws)
+    torch.cuda.synchronize()
+    dense_f = statistics.median(time_calls(lambda: ops.sdpa_fwd(q, k, v, od, ld), 20, flush, stream)) * 1e3
+    dense_b = statistics.median(time_calls(lambda: ops.sdpa_bwd(q, k, v, od, ld, do, *g, workspace=ws), 20, flush,
+                                           stream)) * 1e3
+    e = out["blocksparse_f16_d64"]
+    e["dense_fwd_us"], e["dense_bwd_us"] = round(dense_f, 3), round(dense_b, 3)
+    e["fwd_time_vs_dense"] = round(e["fwd_us"] / dense_f, 4)
+    e["bwd_time_vs_dense"] = round(e["bwd_us"] / dense_b, 4)
+    del od, ld
     del q, k, v, do, o, lse, g, ws, x
 
     # additive mask: one [L, L] mask per head (about 10 % -inf), shared over the batch

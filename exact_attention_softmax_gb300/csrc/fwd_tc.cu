@@ -107,6 +107,11 @@ struct Cfg {
   // tiles' chains are serial and one warp alternating between them keeps the
   // tensor cores busier.
   static constexpr int kMmaWarps = kPAlias ? 1 : 2;
+  // Block-sparse with an MMA warp per tile (d <= 64): each tile streams only
+  // the key blocks its own mask row keeps, through the one K/V ring (the
+  // producer alternates the two tiles' blocks), so neither softmax group
+  // idles on a block only the other tile keeps.
+  static constexpr bool kTileStreams = EXT == 1 && !kPAlias;
   // Three warpgroups: two softmax groups and one for the producer and MMA
   // warps (the rest of it idles), so that registers can move between them.
   static constexpr int kThreads = 384;
@@ -182,6 +187,20 @@ struct Item {
 __device__ __forceinline__ bool loaded_block(const Item& it, int j) {
   return (j < it.lim0 && it.m0[j]) || (j < it.lim1 && it.m1[j]);
 }
+// First key block at or after j that mask row m keeps below lim.
+__device__ __forceinline__ int next_kept(const unsigned char* m, int lim, int j) {
+  while (j < lim && !m[j]) ++j;
+  return j;
+}
+// Per-tile streams: ring position, relative to the item's first fill, of the
+// K tile of tile t's i-th block (the producer loads tile 0's i-th block, then
+// tile 1's, for i = 0, 1, ...; a tile out of blocks is skipped), and the
+// number of fills of an item.
+__device__ __forceinline__ int tile_kpos(const Item& x, int i, int t) {
+  return 2 * (min(i, x.n0) + min(i, x.n1) + (t == 1 && i < x.n0 ? 1 : 0));
+}
+__device__ __forceinline__ int item_fills(const Item& x, bool tiles) { return tiles ? 2 * (x.n0 + x.n1) : 2 * x.nmax; }
+
 // First loaded key block at or after j.
 __device__ __forceinline__ int next_loaded(const Item& it, int j) {
   const int lim = max(it.lim0, it.lim1);
@@ -192,7 +211,7 @@ __device__ __forceinline__ int next_loaded(const Item& it, int j) {
 // Items are numbered unit-major, so the items of one (batch|sequence, head) run
 // side by side and share its K/V through L2; under causal masking the longest
 // rows of each unit come first.
-template <bool CAUSAL, bool PACKED, bool SPARSE>
+template <bool CAUSAL, bool PACKED, bool SPARSE, bool TILES = false>
 __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npairs) {
   Item it;
   // Causal items get shorter with their query position, so they are handed
@@ -246,6 +265,12 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
     it.lim1 = any1 ? it.n1 : 0;
     int c0 = 0, c1 = 0;
     for (int j = 0; j < max(it.lim0, it.lim1); ++j) {
+      if (TILES) {
+        // each tile counts the blocks its own row keeps
+        c0 += j < it.lim0 && it.m0[j];
+        c1 += j < it.lim1 && it.m1[j];
+        continue;
+      }
       if (!loaded_block(it, j)) continue;
       c0 += j < it.lim0;
       c1 += j < it.lim1;
@@ -281,7 +306,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars->full[i], 1);
-      mbar_init(&bars->empty[i], C::kMmaWarps);
+      mbar_init(&bars->empty[i], C::kTileStreams ? 1 : C::kMmaWarps);   // the fill's consumers
     }
     for (int i = 0; i < 2 * C::kQBufs; ++i) {
       mbar_init(&bars->q_full[i], 1);
@@ -342,7 +367,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         bars->item[q] = idx;
         mbar_arrive(&bars->item_full[q]);
         if (idx < 0) break;
-        const Item it = decode_item<CAUSAL, PACKED, SPARSE>(p, idx, npairs);
+        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, npairs);
         idx = static_cast<int>(atomicAdd(sched, 1u)) + static_cast<int>(gridDim.x);
         if (it.nmax == 0) continue;
         // boxes: packed (column, head, token); dense (column, row, unit), or
@@ -365,20 +390,38 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             load(smem + C::kOffQ + qb * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[qb], cb * C::kBlk,
                  row, it.tok0);
         }
-        constexpr bool sparse = SPARSE;
-        int jk = -1;               // key block of the current loaded block
-        for (int j = 0; j < it.nmax && ok; ++j) {
-          jk = sparse ? next_loaded(it, jk + 1) : j;
+        // K_jk and V_jk into the next two ring slots
+        auto fill_block = [&](int jk) {
           for (int kv = 0; kv < 2; ++kv, ++fill) {
             const int slot = fill % C::kSlots;
             const int round = fill / C::kSlots;
-            if (round > 0 && !(ok = mbar_wait(&bars->empty[slot], (round - 1) & 1, abort_flag, p.status))) break;
+            if (round > 0 && !(ok = mbar_wait(&bars->empty[slot], (round - 1) & 1, abort_flag, p.status))) return;
             mbar_expect_tx(&bars->full[slot], C::kTileBytes);
             const CUtensorMap* m = kv ? &tmV : &tmK;
             const int row = jk * BN;
             for (int cb = 0; cb < C::kNBlk; ++cb)
               load(smem + C::kOffSlots + slot * C::kTileBytes + cb * C::kColBlkBytes, m, &bars->full[slot],
                    cb * C::kBlk, row, it.tok0k);
+          }
+        };
+        if constexpr (C::kTileStreams) {
+          int j0 = -1, j1 = -1;    // key blocks of the two tiles' current blocks
+          for (int i = 0; i < it.nmax && ok; ++i) {
+            if (i < it.n0) {
+              j0 = next_kept(it.m0, it.lim0, j0 + 1);
+              fill_block(j0);
+            }
+            if (i < it.n1 && ok) {
+              j1 = next_kept(it.m1, it.lim1, j1 + 1);
+              fill_block(j1);
+            }
+          }
+        } else {
+          constexpr bool sparse = SPARSE;
+          int jk = -1;             // key block of the current loaded block
+          for (int j = 0; j < it.nmax && ok; ++j) {
+            jk = sparse ? next_loaded(it, jk + 1) : j;
+            fill_block(jk);
           }
         }
       }
@@ -467,7 +510,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       int idx = -1;
       ok = take(0, idx);
       while (ok && idx >= 0) {
-        const Item it = decode_item<CAUSAL, PACKED, SPARSE>(p, idx, npairs);
+        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, npairs);
         int qbuf[2];             // Q buffer of this item per tile
         for (int t = t_lo; t < t_hi; ++t) qbuf[t] = t * C::kQBufs + (qloads[t] - (pre[t] ? 1 : 0)) % C::kQBufs;
         if (it.nmax > 0) {
@@ -481,16 +524,26 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             // instead of both groups loading, then competing for the
             // exponential unit, at the same moments.
             if (C::kMmaWarps == 2 && t == 1 && k == 0 && it.n0 > 0 && !(ok = wait(&bars->p_full[0], 0))) break;
-            ok = first_qk(it, t, fill);
+            ok = first_qk(it, t, fill + (C::kTileStreams ? tile_kpos(it, 0, t) : 0));
           }
           if (!ok) break;
-          mma_commit(&bars->empty[fill % C::kSlots]);
+          if constexpr (C::kTileStreams) {
+            // this warp's tile consumed its own K_0
+            if ((t_lo == 0 ? it.n0 : it.n1) > 0) mma_commit(&bars->empty[(fill + tile_kpos(it, 0, t_lo)) % C::kSlots]);
+          } else {
+            mma_commit(&bars->empty[fill % C::kSlots]);
+          }
         }
         pre[0] = pre[1] = false;   // from here on pre[] is about the next item
-        for (int j = 0; j < it.nmax && ok; ++j) {
+        // blocks this warp walks: the item's loaded blocks, or with per-tile
+        // streams its own tile's kept blocks
+        const int jmax = C::kTileStreams ? (t_lo == 0 ? it.n0 : it.n1) : it.nmax;
+        for (int j = 0; j < jmax && ok; ++j) {
           // K_{j+1} sits at ring position fill + 2j + 2, V_j at fill + 2j + 1
-          const bool has_next = j + 1 < it.nmax;
-          const int kpos = fill + 2 * j + 2, vpos = fill + 2 * j + 1;
+          // (per-tile streams: at the tile's own positions)
+          const bool has_next = j + 1 < jmax;
+          const int kpos = C::kTileStreams ? fill + tile_kpos(it, j + 1, t_lo) : fill + 2 * j + 2;
+          const int vpos = C::kTileStreams ? fill + tile_kpos(it, j, t_lo) + 1 : fill + 2 * j + 1;
           if (has_next && !(ok = full_wait(kpos))) break;
           if (!(ok = full_wait(vpos))) break;
           tc_fence_after();
@@ -505,15 +558,19 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               issue_qk(t, qbuf[t], kpos % C::kSlots);
               mma_commit(&bars->s_full[t]);
               if (j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
-            } else if (!C::kPAlias && j + 1 == nt) {
+            } else if (!C::kPAlias && !C::kTileStreams && j + 1 == nt) {
               // last block of this tile: read the next work item and issue its
-              // first S_t now, under this block's softmax
+              // first S_t now, under this block's softmax. (Not with per-tile
+              // streams: there the next item's K_0 of this tile can come after
+              // the other tile's remaining blocks, more fills than the ring
+              // holds, while this warp still holds the slot of its last V.)
               if (next_idx == -2 && !(ok = take(k + 1, next_idx))) break;
               if (next_idx >= 0) {
-                const Item nx = decode_item<CAUSAL, PACKED, SPARSE>(p, next_idx, npairs);
+                const Item nx = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, next_idx, npairs);
                 if (nx.nmax > 0 && (t == 0 ? nx.n0 : nx.n1) > 0) {
                   blocks[t] += nt;            // the phases of S_t continue into the next item
-                  ok = first_qk(nx, t, fill + 2 * it.nmax);
+                  ok = first_qk(nx, t, fill + item_fills(it, C::kTileStreams) +
+                                           (C::kTileStreams ? tile_kpos(nx, 0, t) : 0));
                   blocks[t] -= nt;
                   if (!ok) break;
                   pre[t] = true;
@@ -543,7 +600,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           blocks[t] += nt;
           if (nt > 0) ++items[t];
         }
-        fill += 2 * it.nmax;
+        fill += item_fills(it, C::kTileStreams);
         ++k;
         if (next_idx != -2) {
           idx = next_idx;
@@ -660,7 +717,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[q]);
       if (idx < 0) break;
-      const Item it = decode_item<CAUSAL, PACKED, SPARSE>(p, idx, npairs);
+      const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, npairs);
       const int nt = t == 0 ? it.n0 : it.n1;
       const int rt = it.r0 + t * BM;
       const int row = rt + rl;                // row within the unit
@@ -682,7 +739,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       float m_run = -INFINITY, l = 0.f;      // maximum used in the exponent (base 2), running sum
       for (int j = 0; j < nt; ++j) {
         const int g = blocks + j;
-        jk = sparse ? next_loaded(it, jk + 1) : j;
+        jk = !sparse ? j : C::kTileStreams ? next_kept(mine, t == 0 ? it.lim0 : it.lim1, jk + 1)
+                                           : next_loaded(it, jk + 1);
         const int kbase = jk * BN;
         if (sparse && !mine[jk]) {
           // A loaded block this tile's mask row drops: its probabilities are
