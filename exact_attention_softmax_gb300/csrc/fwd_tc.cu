@@ -107,15 +107,24 @@ struct Cfg {
   // tiles' chains are serial and one warp alternating between them keeps the
   // tensor cores busier.
   static constexpr int kMmaWarps = kPAlias ? 1 : 2;
-  // Block-sparse with an MMA warp per tile (d <= 64): each tile streams only
-  // the key blocks its own mask row keeps, through the one K/V ring (the
-  // producer alternates the two tiles' blocks), so neither softmax group
-  // idles on a block only the other tile keeps.
+  // Block-sparse with an MMA warp per tile (d <= 64): the CTA runs two
+  // independent pipelines, one per tile slot, each with its own producer, MMA
+  // warp, softmax group, item queue and K/V ring. A slot claims single
+  // 128-row tiles and streams only the key blocks that tile's mask row keeps,
+  // so tiles keeping many and few blocks balance across slots and CTAs, and
+  // neither softmax group idles on a block only the other tile keeps. Each
+  // ring is read in order by one MMA warp alone, so that warp never waits on
+  // a slot whose previous fill has not landed (which a parity wait could not
+  // tell from the fill before that).
   static constexpr bool kTileStreams = EXT == 1 && !kPAlias;
+  static constexpr int kRings = kTileStreams ? 2 : 1;
+  static constexpr int kRing = kSlots / kRings;                // slots per ring
   // Three warpgroups: two softmax groups and one for the producer and MMA
-  // warps (the rest of it idles), so that registers can move between them.
+  // warps (its last warp idles, or with per-tile streams is the second
+  // producer), so that registers can move between them.
   static constexpr int kThreads = 384;
   static_assert(kPAlias || kColP + 2 * (BN / 2) <= 512, "TMEM budget");
+  static_assert(kRing * kRings == kSlots && kRing >= 3, "ring split");
   static_assert(kSlots <= 16 && kQBufs <= 2, "the barrier arrays hold 16 ring slots and 2 Q buffers per tile");
 };
 
@@ -130,9 +139,9 @@ struct __align__(8) Bars {
   uint64_t pv_done[2];    // O_t += P_t V_j finished
   uint64_t o_free[2];     // O_t read out by the epilogue: the next item may overwrite it
   uint64_t mfull[8];      // additive mask: softmax warp w's slot loaded
-  uint64_t item_full[4];  // work-item queue from the producer to the other roles
-  uint64_t item_empty[4];
-  int item[4];
+  uint64_t item_full[8];  // work-item queues from the producer(s) to the other roles
+  uint64_t item_empty[8];  // ([slot * kItemQueue + i]; with a single pipeline only slot 0)
+  int item[8];
   uint64_t done;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -171,7 +180,9 @@ __device__ __forceinline__ int tile_blocks(int r, int len_q, int len_k) {
   return min(nkv, last_row / BN + 1);
 }
 
-// One work item: 256 query rows (two 128-row tiles) of one (batch|sequence, head).
+// One work item: 256 query rows (two 128-row tiles) of one (batch|sequence,
+// head), or with per-slot pipelines one 128-row tile, described as an item
+// whose other tile is empty.
 struct Item {
   int unit, h, tok0, tok0k, len_q, len_k, r0, n0, n1, nmax;
   // block-sparse: the two tiles' mask rows and their key-block limits (causal
@@ -192,14 +203,11 @@ __device__ __forceinline__ int next_kept(const unsigned char* m, int lim, int j)
   while (j < lim && !m[j]) ++j;
   return j;
 }
-// Per-tile streams: ring position, relative to the item's first fill, of the
-// K tile of tile t's i-th block (the producer loads tile 0's i-th block, then
-// tile 1's, for i = 0, 1, ...; a tile out of blocks is skipped), and the
-// number of fills of an item.
-__device__ __forceinline__ int tile_kpos(const Item& x, int i, int t) {
-  return 2 * (min(i, x.n0) + min(i, x.n1) + (t == 1 && i < x.n0 ? 1 : 0));
+// Fills of ring r for an item: both tiles' shared stream, or with per-tile
+// streams tile r's own kept blocks.
+__device__ __forceinline__ int item_fills(const Item& x, bool tiles, int r) {
+  return 2 * (!tiles ? x.nmax : r == 0 ? x.n0 : x.n1);
 }
-__device__ __forceinline__ int item_fills(const Item& x, bool tiles) { return tiles ? 2 * (x.n0 + x.n1) : 2 * x.nmax; }
 
 // First loaded key block at or after j.
 __device__ __forceinline__ int next_loaded(const Item& it, int j) {
@@ -211,8 +219,11 @@ __device__ __forceinline__ int next_loaded(const Item& it, int j) {
 // Items are numbered unit-major, so the items of one (batch|sequence, head) run
 // side by side and share its K/V through L2; under causal masking the longest
 // rows of each unit come first.
+// nper: items per unit. With TILES item idx is a single 128-row tile run by
+// slot `slot`: it is described as tile `slot` of an item whose r0 is that much
+// lower, and the other tile keeps nothing.
 template <bool CAUSAL, bool PACKED, bool SPARSE, bool TILES = false>
-__device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npairs) {
+__device__ __forceinline__ Item decode_item(const Problem& p, int idx, int nper, int slot = 0) {
   Item it;
   // Causal items get shorter with their query position, so they are handed
   // out longest first across all units (ord-major), which keeps the last
@@ -222,9 +233,9 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
   // the units are taken one after another.
   const int units = p.B * p.H;
   constexpr bool kOrdMajor = CAUSAL || PACKED;
-  it.unit = kOrdMajor ? idx % units : idx / npairs;
-  const int ord = kOrdMajor ? idx / units : idx % npairs;
-  const int pair = kOrdMajor ? (npairs - 1 - ord) : ord;
+  it.unit = kOrdMajor ? idx % units : idx / nper;
+  const int ord = kOrdMajor ? idx / units : idx % nper;
+  const int pos = kOrdMajor ? (nper - 1 - ord) : ord;    // pair, or tile, within the unit
   it.h = 0;
   it.tok0 = it.tok0k = 0;
   if (PACKED) {
@@ -246,7 +257,22 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
     // side by side, so the rows of its mask they all read come from L2
     if (p.amask != nullptr && p.am_sb == 0 && p.am_sh != 0 && p.B > 1) it.unit = (it.unit % p.B) * p.H + it.unit / p.B;
   }
-  it.r0 = pair * 2 * BM;
+  if (TILES) {
+    const int rt = pos * BM;
+    it.r0 = rt - slot * BM;
+    const int n = tile_blocks<CAUSAL>(rt, it.len_q, it.len_k);
+    const unsigned char* mrow = p.bmask + (it.unit / p.H) * p.bm_sb + (it.unit % p.H) * p.bm_sh +
+                                static_cast<long long>(rt / kMaskBlock) * p.bm_sq;
+    int c = 0;                 // blocks the tile's mask row keeps
+    for (int j = 0; j < n; ++j) c += mrow[j] != 0;
+    it.m0 = it.m1 = mrow;
+    it.lim0 = it.lim1 = c > 0 ? n : 0;
+    it.n0 = slot == 0 ? c : 0;
+    it.n1 = slot == 1 ? c : 0;
+    it.nmax = c;
+    return it;
+  }
+  it.r0 = pos * 2 * BM;
   it.n0 = tile_blocks<CAUSAL>(it.r0, it.len_q, it.len_k);
   it.n1 = tile_blocks<CAUSAL>(it.r0 + BM, it.len_q, it.len_k);
   it.m0 = it.m1 = nullptr;
@@ -265,12 +291,6 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int npair
     it.lim1 = any1 ? it.n1 : 0;
     int c0 = 0, c1 = 0;
     for (int j = 0; j < max(it.lim0, it.lim1); ++j) {
-      if (TILES) {
-        // each tile counts the blocks its own row keeps
-        c0 += j < it.lim0 && it.m0[j];
-        c1 += j < it.lim1 && it.m1[j];
-        continue;
-      }
       if (!loaded_block(it, j)) continue;
       c0 += j < it.lim0;
       c1 += j < it.lim1;
@@ -296,9 +316,12 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Persistent: CTA b starts with work item b, then claims items dynamically.
-  const int npairs = ((PACKED ? p.max_q : p.Lq) + 2 * BM - 1) / (2 * BM);
-  const int nitems = npairs * p.B * p.H;
+  // Persistent: CTA b starts with work item b (with per-slot pipelines, slot
+  // s with item 2b + s), then claims items dynamically.
+  constexpr int kClaim = C::kTileStreams ? 2 : 1;       // claimers per CTA
+  constexpr int kItemRows = C::kTileStreams ? BM : 2 * BM;
+  const int nper = ((PACKED ? p.max_q : p.Lq) + kItemRows - 1) / kItemRows;   // items per unit
+  const int nitems = nper * p.B * p.H;
 
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sSlots = smem_u32(smem + C::kOffSlots);
@@ -306,7 +329,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars->full[i], 1);
-      mbar_init(&bars->empty[i], C::kTileStreams ? 1 : C::kMmaWarps);   // the fill's consumers
+      mbar_init(&bars->empty[i], C::kTileStreams ? 1 : C::kMmaWarps);   // the ring's consumers
     }
     for (int i = 0; i < 2 * C::kQBufs; ++i) {
       mbar_init(&bars->q_full[i], 1);
@@ -319,9 +342,11 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->o_free[t], BM);
     }
-    for (int i = 0; i < kItemQueue; ++i) {
+    for (int i = 0; i < 2 * kItemQueue; ++i) {
       mbar_init(&bars->item_full[i], 1);
-      mbar_init(&bars->item_empty[i], 8 + C::kMmaWarps);   // one arrival per consuming warp
+      // one arrival per consuming warp: a softmax group and an MMA warp per
+      // slot, or both groups and the MMA warp(s)
+      mbar_init(&bars->item_empty[i], C::kTileStreams ? 5 : 8 + C::kMmaWarps);
     }
     mbar_init(&bars->done, C::kMmaWarps);
     for (int w = 0; w < 8; ++w) mbar_init(&bars->mfull[w], 1);
@@ -348,27 +373,31 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
   if (warp >= 8) {
    // producer, MMA and idle warps
    regs_dec<kRegsControl>();
-   if (warp == kProducerWarp) {
+   // With per-slot pipelines the control group's fourth warp is slot 1's
+   // producer: each producer claims its slot's tiles, publishes them on the
+   // slot's queue and loads their Q and K/V into the slot's buffers and ring.
+   if (warp == kProducerWarp || (C::kTileStreams && warp == kProducerWarp + 3)) {
     // ------------------------------------------------------------ producer
+    const int pr = warp == kProducerWarp ? 0 : 1;   // this thread's slot (ring and queue)
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int fill = 0;             // ring position of the next K/V fill (K_0, V_0, K_1, V_1, ... per item)
+      int fill = 0;             // next position in ring pr (K_0, V_0, K_1, V_1, ... per item)
       int qloads[2] = {0, 0};   // Q loads so far per tile
       bool ok = true;
-      int idx = blockIdx.x;
+      int idx = kClaim * blockIdx.x + pr;
       for (int k = 0;; ++k) {
-        // publish the item (or the end marker) to the other roles
-        const int q = k % kItemQueue;
+        // publish the item (or the end marker) to the slot's consumers
+        const int q = pr * kItemQueue + k % kItemQueue;
         if (k >= kItemQueue && !(ok = mbar_wait(&bars->item_empty[q], (k / kItemQueue - 1) & 1, abort_flag, p.status)))
           break;
         if (!ok || idx >= nitems) idx = -1;
         bars->item[q] = idx;
         mbar_arrive(&bars->item_full[q]);
         if (idx < 0) break;
-        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, npairs);
-        idx = static_cast<int>(atomicAdd(sched, 1u)) + static_cast<int>(gridDim.x);
+        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, pr);
+        idx = static_cast<int>(atomicAdd(sched, 1u)) + kClaim * static_cast<int>(gridDim.x);
         if (it.nmax == 0) continue;
         // boxes: packed (column, head, token); dense (column, row, unit), or
         // (column, row, head, batch) through the 4-D maps of strided tensors
@@ -377,7 +406,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           else if constexpr (STRIDED) tma_load_4d(dst, m, bar, col, row, it.unit % p.H, it.unit / p.H);
           else tma_load_3d(dst, m, bar, col, row, it.unit);
         };
-        for (int t = 0; t < 2 && ok; ++t) {
+        for (int t = C::kTileStreams ? pr : 0; t < (C::kTileStreams ? pr + 1 : 2) && ok; ++t) {
           if ((t == 0 ? it.n0 : it.n1) == 0) continue;
           // buffer qb of tile t was last used kQBufs loads ago
           const int qb = t * C::kQBufs + qloads[t] % C::kQBufs, use = qloads[t] / C::kQBufs;
@@ -390,11 +419,11 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             load(smem + C::kOffQ + qb * C::kTileBytes + cb * C::kColBlkBytes, &tmQ, &bars->q_full[qb], cb * C::kBlk,
                  row, it.tok0);
         }
-        // K_jk and V_jk into the next two ring slots
+        // K_jk and V_jk into the next two slots of ring pr
         auto fill_block = [&](int jk) {
           for (int kv = 0; kv < 2; ++kv, ++fill) {
-            const int slot = fill % C::kSlots;
-            const int round = fill / C::kSlots;
+            const int slot = pr * C::kRing + fill % C::kRing;
+            const int round = fill / C::kRing;
             if (round > 0 && !(ok = mbar_wait(&bars->empty[slot], (round - 1) & 1, abort_flag, p.status))) return;
             mbar_expect_tx(&bars->full[slot], C::kTileBytes);
             const CUtensorMap* m = kv ? &tmV : &tmK;
@@ -405,16 +434,13 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           }
         };
         if constexpr (C::kTileStreams) {
-          int j0 = -1, j1 = -1;    // key blocks of the two tiles' current blocks
-          for (int i = 0; i < it.nmax && ok; ++i) {
-            if (i < it.n0) {
-              j0 = next_kept(it.m0, it.lim0, j0 + 1);
-              fill_block(j0);
-            }
-            if (i < it.n1 && ok) {
-              j1 = next_kept(it.m1, it.lim1, j1 + 1);
-              fill_block(j1);
-            }
+          // the key blocks this thread's tile keeps
+          const unsigned char* mine = pr == 0 ? it.m0 : it.m1;
+          const int lim = pr == 0 ? it.lim0 : it.lim1;
+          int jk = -1;
+          for (int i = 0; i < (pr == 0 ? it.n0 : it.n1) && ok; ++i) {
+            jk = next_kept(mine, lim, jk + 1);
+            fill_block(jk);
           }
         } else {
           constexpr bool sparse = SPARSE;
@@ -425,15 +451,15 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           }
         }
       }
-      // the last CTA to finish claiming resets this launch's scheduler slot
-      if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+      // the last claimer to finish resets this launch's scheduler slot
+      if (atomicAdd(sched + 1, 1u) == kClaim * gridDim.x - 1) {
         atomicExch(sched, 0u);
         atomicExch(sched + 1, 0u);
       }
       if (*abort_flag) {
         // Let copies already issued land before the CTA's shared memory is released.
-        for (int f = max(0, fill - C::kSlots); f < fill; ++f)
-          mbar_wait_drain(&bars->full[f % C::kSlots], (f / C::kSlots) & 1);
+        for (int f = max(0, fill - C::kRing); f < fill; ++f)
+          mbar_wait_drain(&bars->full[pr * C::kRing + f % C::kRing], (f / C::kRing) & 1);
         for (int t = 0; t < 2; ++t)
           for (int n = max(0, qloads[t] - C::kQBufs); n < qloads[t]; ++n)
             if (!(p.debug & kDebugDropQArrive))
@@ -442,10 +468,12 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     }
   } else if (warp >= kMmaWarp && warp < kMmaWarp + C::kMmaWarps) {
     // ------------------------------------------------------------ MMA issue
-    // Warp w serves Q tiles [t_lo, t_hi); lane 0 issues. Every MMA warp
-    // consumes every K/V fill: a slot's empty barrier takes one commit from each.
+    // Warp w serves Q tiles [t_lo, t_hi); lane 0 issues. Without per-tile
+    // streams every MMA warp consumes every K/V fill of the one ring (a slot's
+    // empty barrier takes one commit from each); with them warp t reads ring t.
     const int t_lo = C::kMmaWarps == 2 ? warp - kMmaWarp : 0;
     const int t_hi = C::kMmaWarps == 2 ? t_lo + 1 : 2;
+    const int ring = C::kTileStreams ? t_lo : 0;      // ring and item queue
     if (lane == 0) {
       constexpr uint32_t fmt = std::is_same<T, __half>::value ? 0u : 1u;
       constexpr uint32_t idS = idesc_f16(fmt, 0, 0, BM, BN);
@@ -473,19 +501,20 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
                  (acc || ks > 0) ? 1u : 0u);
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort_flag, p.status); };
-      auto full_wait = [&](int pos) { return wait(&bars->full[pos % C::kSlots], (pos / C::kSlots) & 1); };
+      auto slot_of = [&](int pos) { return ring * C::kRing + pos % C::kRing; };
+      auto full_wait = [&](int pos) { return wait(&bars->full[slot_of(pos)], (pos / C::kRing) & 1); };
       // Work items come from the producer's queue; the next one is read ahead
       // so that its first S_t can be issued before the current item's last P.V.
       int k = 0;                 // queue index of the current item
       int next_idx = -2;         // queue entry k + 1 once read (-2: not yet)
       auto take = [&](int kk, int& idx) {
-        const int q = kk % kItemQueue;
+        const int q = ring * kItemQueue + kk % kItemQueue;
         if (!wait(&bars->item_full[q], (kk / kItemQueue) & 1)) return false;
         idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
         mbar_arrive(&bars->item_empty[q]);
         return true;
       };
-      int fill = 0;              // ring position of the current item's K_0
+      int fill = 0;              // position of the current item's K_0 in this warp's ring
       int qloads[2] = {0, 0};    // Q tiles consumed per tile slot
       int blocks[2] = {0, 0};    // K/V blocks processed per tile slot (barrier phases)
       int items[2] = {0, 0};     // work items finished per tile slot
@@ -501,7 +530,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         if (!C::kPAlias && blocks[t] > 0 && !wait(&bars->s_free[t], (blocks[t] - 1) & 1)) return false;
         if (!full_wait(xfill)) return false;
         tc_fence_after();
-        issue_qk(t, qb, xfill % C::kSlots);
+        issue_qk(t, qb, slot_of(xfill));
         mma_commit(&bars->s_full[t]);
         if (nt == 1) mma_commit(&bars->q_empty[qb]);
         return true;
@@ -510,7 +539,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       int idx = -1;
       ok = take(0, idx);
       while (ok && idx >= 0) {
-        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, npairs);
+        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, t_lo);
         int qbuf[2];             // Q buffer of this item per tile
         for (int t = t_lo; t < t_hi; ++t) qbuf[t] = t * C::kQBufs + (qloads[t] - (pre[t] ? 1 : 0)) % C::kQBufs;
         if (it.nmax > 0) {
@@ -523,27 +552,23 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             // TMEM loads and waits fall under the other's exponentials
             // instead of both groups loading, then competing for the
             // exponential unit, at the same moments.
-            if (C::kMmaWarps == 2 && t == 1 && k == 0 && it.n0 > 0 && !(ok = wait(&bars->p_full[0], 0))) break;
-            ok = first_qk(it, t, fill + (C::kTileStreams ? tile_kpos(it, 0, t) : 0));
+            if (C::kMmaWarps == 2 && !C::kTileStreams && t == 1 && k == 0 && it.n0 > 0 &&
+                !(ok = wait(&bars->p_full[0], 0)))
+              break;
+            ok = first_qk(it, t, fill);
           }
           if (!ok) break;
-          if constexpr (C::kTileStreams) {
-            // this warp's tile consumed its own K_0
-            if ((t_lo == 0 ? it.n0 : it.n1) > 0) mma_commit(&bars->empty[(fill + tile_kpos(it, 0, t_lo)) % C::kSlots]);
-          } else {
-            mma_commit(&bars->empty[fill % C::kSlots]);
-          }
+          if (item_fills(it, C::kTileStreams, ring) > 0) mma_commit(&bars->empty[slot_of(fill)]);   // K_0 consumed
         }
         pre[0] = pre[1] = false;   // from here on pre[] is about the next item
         // blocks this warp walks: the item's loaded blocks, or with per-tile
         // streams its own tile's kept blocks
-        const int jmax = C::kTileStreams ? (t_lo == 0 ? it.n0 : it.n1) : it.nmax;
+        const int jmax = item_fills(it, C::kTileStreams, ring) / 2;
         for (int j = 0; j < jmax && ok; ++j) {
           // K_{j+1} sits at ring position fill + 2j + 2, V_j at fill + 2j + 1
-          // (per-tile streams: at the tile's own positions)
           const bool has_next = j + 1 < jmax;
-          const int kpos = C::kTileStreams ? fill + tile_kpos(it, j + 1, t_lo) : fill + 2 * j + 2;
-          const int vpos = C::kTileStreams ? fill + tile_kpos(it, j, t_lo) + 1 : fill + 2 * j + 1;
+          const int kpos = fill + 2 * j + 2;
+          const int vpos = fill + 2 * j + 1;
           if (has_next && !(ok = full_wait(kpos))) break;
           if (!(ok = full_wait(vpos))) break;
           tc_fence_after();
@@ -555,22 +580,18 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               // S_t may be overwritten once its softmax group holds it in registers
               if (!(ok = wait(&bars->s_free[t], g & 1))) break;
               tc_fence_after();
-              issue_qk(t, qbuf[t], kpos % C::kSlots);
+              issue_qk(t, qbuf[t], slot_of(kpos));
               mma_commit(&bars->s_full[t]);
               if (j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
             } else if (!C::kPAlias && !C::kTileStreams && j + 1 == nt) {
               // last block of this tile: read the next work item and issue its
-              // first S_t now, under this block's softmax. (Not with per-tile
-              // streams: there the next item's K_0 of this tile can come after
-              // the other tile's remaining blocks, more fills than the ring
-              // holds, while this warp still holds the slot of its last V.)
+              // first S_t now, under this block's softmax
               if (next_idx == -2 && !(ok = take(k + 1, next_idx))) break;
               if (next_idx >= 0) {
-                const Item nx = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, next_idx, npairs);
+                const Item nx = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, next_idx, nper, t_lo);
                 if (nx.nmax > 0 && (t == 0 ? nx.n0 : nx.n1) > 0) {
                   blocks[t] += nt;            // the phases of S_t continue into the next item
-                  ok = first_qk(nx, t, fill + item_fills(it, C::kTileStreams) +
-                                           (C::kTileStreams ? tile_kpos(nx, 0, t) : 0));
+                  ok = first_qk(nx, t, fill + item_fills(it, C::kTileStreams, ring));
                   blocks[t] -= nt;
                   if (!ok) break;
                   pre[t] = true;
@@ -582,17 +603,17 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
             // epilogue must have read it
             if (j == 0 && items[t] > 0 && !(ok = wait(&bars->o_free[t], (items[t] - 1) & 1))) break;
             tc_fence_after();
-            issue_pv(t, vpos % C::kSlots, j > 0);
+            issue_pv(t, slot_of(vpos), j > 0);
             mma_commit(&bars->pv_done[t]);
             if (C::kPAlias && j + 1 < nt) {
               // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
-              issue_qk(t, qbuf[t], kpos % C::kSlots);
+              issue_qk(t, qbuf[t], slot_of(kpos));
               mma_commit(&bars->s_full[t]);
               if (j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
             }
           }
-          mma_commit(&bars->empty[vpos % C::kSlots]);
-          if (has_next) mma_commit(&bars->empty[kpos % C::kSlots]);
+          mma_commit(&bars->empty[slot_of(vpos)]);
+          if (has_next) mma_commit(&bars->empty[slot_of(kpos)]);
         }
         if (!ok) break;
         for (int t = t_lo; t < t_hi; ++t) {
@@ -600,7 +621,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           blocks[t] += nt;
           if (nt > 0) ++items[t];
         }
-        fill += item_fills(it, C::kTileStreams);
+        fill += item_fills(it, C::kTileStreams, ring);
         ++k;
         if (next_idx != -2) {
           idx = next_idx;
@@ -711,13 +732,13 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     };
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int q = k % kItemQueue;
+      const int q = (C::kTileStreams ? t * kItemQueue : 0) + k % kItemQueue;
       if (!(ok = wait_all(&bars->item_full[q], (k / kItemQueue) & 1))) break;
       const int idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[q]);
       if (idx < 0) break;
-      const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, npairs);
+      const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, t);
       const int nt = t == 0 ? it.n0 : it.n1;
       const int rt = it.r0 + t * BM;
       const int row = rt + rl;                // row within the unit
@@ -1009,15 +1030,17 @@ cudaError_t launch_one(const Problem& p, const FwdMaps& m, cudaStream_t s) {
   }
   const int sms = dev < 64 ? sm_count[dev] : 1;
   const int rows = PACKED ? p.max_q : p.Lq;
-  const long long npairs = (rows + 2 * BM - 1) / (2 * BM);
-  const long long items = npairs * p.B * p.H;
+  constexpr bool kTiles = Cfg<D, EXT>::kTileStreams;     // two single-tile claimers per CTA
+  const long long nper = (rows + (kTiles ? BM : 2 * BM) - 1) / (kTiles ? BM : 2 * BM);
+  const long long items = nper * p.B * p.H;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   // d <= 64: persistent, one CTA per SM (each needs most of the SM's SMEM and all
   // of its TMEM) claiming items until none are left, so an item's prologue and
   // epilogue overlap its neighbours'. d = 128: one CTA per item measured faster
   // (its items are long, and the hardware's block scheduler balances them).
-  const long long want = D == 128 ? items : (items < sms ? items : sms);
+  const long long ctas = kTiles ? (items + 1) / 2 : items;
+  const long long want = D == 128 ? items : (ctas < sms ? ctas : sms);
   const unsigned grid = static_cast<unsigned>(want);
   static unsigned* sched_base[64] = {nullptr};
   if (dev >= 64) return cudaErrorInvalidDevice;

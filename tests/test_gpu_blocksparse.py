@@ -126,6 +126,34 @@ def test_blocksparse_many_items_per_cta(d, causal):
         _check_fwd((got[0][b:b + 1, h:h + 1], got[1][b:b + 1, h:h + 1]), ref, "f16")
 
 
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocksparse_uneven_tiles(d, causal):
+    """The two 128-row query tiles of each 256-row item keep very different
+    numbers of key blocks: one keeps every block, the other one or two, and
+    the roles swap from head to head. One tile then runs through many more
+    K/V fills than a ring holds before the other finishes, and on into its
+    next item, on many items per CTA. Sampled units against the oracle."""
+    B, H, L = 1, 40, 4096
+    nb = _nb(L)
+    m = np.zeros((H, nb, nb), dtype=np.uint8)
+    for h in range(H):
+        for r in range(nb):
+            if (r + h) % 2 == 0:
+                m[h, r, :] = 1               # every key block
+            else:
+                m[h, r, 0] = 1               # the first block, and under causal masking
+                m[h, r, r] = 1               # the diagonal one
+    mask = torch.from_numpy(m)
+    scale = d ** -0.5
+    x = wl.dense_inputs(B, H, L, L, d, "bf16", "normal", seed=50, with_do=False)
+    got = _run(x, mask, causal, scale, bwd=False)
+    for h in (0, 1, 38, 39):
+        sub = {n: x[n][:, h:h + 1] for n in ("q", "k", "v")}
+        ref = _oracle(sub, mask[h:h + 1], causal, scale, bwd=False)
+        _check_fwd((got[0][:, h:h + 1], got[1][:, h:h + 1]), ref, "bf16")
+
+
 def test_all_ones_mask_matches_dense_call():
     """With every tile kept the block-sparse forward gives the dense call's
     results bit for bit (same blocks, same order)."""
