@@ -60,6 +60,7 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr int kSchedSlots = 1024;
 __device__ unsigned g_fwd_sched[2 * kSchedSlots];
 constexpr int kItemQueue = 4;
+constexpr int kBarBytes = 704;   // shared memory for the barrier block
 
 template <int D, int EXT = 0>
 struct Cfg {
@@ -76,23 +77,30 @@ struct Cfg {
   // The additive-mask kernel gives up K/V ring slots at d >= 64 for its mask
   // slots: one 32-row x 128-key slot per softmax warp (two 64-key boxes).
   static constexpr bool kMask = EXT == 2;
-  // Where each CTA runs many work items (d <= 64) the epilogue stages every
-  // softmax warp's 32 output rows in shared memory, so the global stores go
-  // out row-contiguous (the mask kernel has no room; at d = 128 items are long
-  // and the direct stores cost little). d = 64 gives two K/V slots for it,
-  // except in the block-sparse kernel, which streams the union of its tiles'
-  // key blocks and measured 10 % slower with eight slots.
-  static constexpr bool kSparseK = EXT == 1;
-  static constexpr bool kStageO = D <= 64 && !kMask && !(D == 64 && kSparseK);
+  // Where each CTA runs many work items (Q double-buffered, d <= 64) the
+  // epilogue stages every softmax warp's 32 output rows in shared memory, so
+  // the global stores go out row-contiguous. The dense and dropout kernels
+  // stage them in a region of their own, for which d = 64 gives two K/V
+  // slots. The block-sparse kernel stages them in the item's own Q buffer
+  // instead, which no MMA reads once the item's last P.V has finished (a
+  // softmax group's 128 rows of O fill exactly one Q tile): no K/V slot is
+  // given up, but the buffer goes back to the producer after the (deferred)
+  // epilogue rather than after the item's last S_t, which delays the Q load
+  // two items on; that measured slower on the dense causal kernel's short
+  // items and on the mask kernel. The mask kernel has no room for a stage
+  // region and stores directly, as does d = 128, whose items are long.
+  static constexpr bool kStageQ = kQBufs == 2 && EXT == 1;
+  static constexpr bool kStageO = kQBufs == 2 && !kStageQ && !kMask;
   static constexpr int kSlots = D == 128 ? (kMask ? 3 : 5) : (D == 64 ? (kMask ? 6 : (kStageO ? 8 : 10)) : 16);
   static constexpr int kOffQ = 0;
   static constexpr int kOffSlots = 2 * kQBufs * kTileBytes;
   static constexpr int kMaskWarpBytes = 32 * BN * 2;
   static constexpr int kOffMask = kOffSlots + kSlots * kTileBytes;
   static constexpr int kStageWarpBytes = 32 * D * 2;          // 32 rows of O
+  static_assert(4 * kStageWarpBytes == kTileBytes, "a softmax group stages one Q tile");
   static constexpr int kOffStage = kOffMask + (kMask ? 8 * kMaskWarpBytes : 0);
   static constexpr int kOffBar = kOffStage + (kStageO ? 8 * kStageWarpBytes : 0);
-  static constexpr int kSmem = kOffBar + 640 + 1024;          // barriers + alignment slack
+  static constexpr int kSmem = kOffBar + kBarBytes + 1024;    // barriers + alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   // TMEM columns. P (BN fp16/bf16 per row, two per 32-bit column) has its own
   // columns when they fit; at d = 128 it overlays the upper half of S_t, which
@@ -130,7 +138,8 @@ struct Cfg {
 
 struct __align__(8) Bars {
   uint64_t q_full[4];     // Q_t loaded into buffer b ([t * kQBufs + b])
-  uint64_t q_empty[4];    // last S_t = Q_t K^T of a work item finished: buffer b may be reloaded
+  uint64_t q_empty[4];    // buffer b may be reloaded: its item's last S_t = Q_t K^T finished, or
+                          // (staging in Q) each softmax warp has read its staged rows out
   uint64_t full[16];
   uint64_t empty[16];
   uint64_t s_full[2];     // S_t written by the tensor cores
@@ -142,11 +151,12 @@ struct __align__(8) Bars {
   uint64_t item_full[8];  // work-item queues from the producer(s) to the other roles
   uint64_t item_empty[8];  // ([slot * kItemQueue + i]; with a single pipeline only slot 0)
   int item[8];
+  int item_n[8];          // per-slot pipelines: blocks the item's tile keeps, counted once by its producer
   uint64_t done;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
-static_assert(sizeof(Bars) <= 640, "the barrier block has 640 bytes of shared memory");
+static_assert(sizeof(Bars) <= kBarBytes, "the barrier block's shared memory");
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float m;
@@ -221,9 +231,10 @@ __device__ __forceinline__ int next_loaded(const Item& it, int j) {
 // rows of each unit come first.
 // nper: items per unit. With TILES item idx is a single 128-row tile run by
 // slot `slot`: it is described as tile `slot` of an item whose r0 is that much
-// lower, and the other tile keeps nothing.
+// lower, and the other tile keeps nothing; `kept` is the number of key blocks
+// its mask row keeps when already known (else -1: counted here).
 template <bool CAUSAL, bool PACKED, bool SPARSE, bool TILES = false>
-__device__ __forceinline__ Item decode_item(const Problem& p, int idx, int nper, int slot = 0) {
+__device__ __forceinline__ Item decode_item(const Problem& p, int idx, int nper, int slot = 0, int kept = -1) {
   Item it;
   // Causal items get shorter with their query position, so they are handed
   // out longest first across all units (ord-major), which keeps the last
@@ -263,8 +274,11 @@ __device__ __forceinline__ Item decode_item(const Problem& p, int idx, int nper,
     const int n = tile_blocks<CAUSAL>(rt, it.len_q, it.len_k);
     const unsigned char* mrow = p.bmask + (it.unit / p.H) * p.bm_sb + (it.unit % p.H) * p.bm_sh +
                                 static_cast<long long>(rt / kMaskBlock) * p.bm_sq;
-    int c = 0;                 // blocks the tile's mask row keeps
-    for (int j = 0; j < n; ++j) c += mrow[j] != 0;
+    int c = kept;              // blocks the tile's mask row keeps
+    if (c < 0) {
+      c = 0;
+      for (int j = 0; j < n; ++j) c += mrow[j] != 0;
+    }
     it.m0 = it.m1 = mrow;
     it.lim0 = it.lim1 = c > 0 ? n : 0;
     it.n0 = slot == 0 ? c : 0;
@@ -333,7 +347,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
     }
     for (int i = 0; i < 2 * C::kQBufs; ++i) {
       mbar_init(&bars->q_full[i], 1);
-      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->q_empty[i], C::kStageQ ? 4 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -393,10 +407,12 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         if (k >= kItemQueue && !(ok = mbar_wait(&bars->item_empty[q], (k / kItemQueue - 1) & 1, abort_flag, p.status)))
           break;
         if (!ok || idx >= nitems) idx = -1;
+        Item it{};
+        if (idx >= 0) it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, pr);
         bars->item[q] = idx;
+        bars->item_n[q] = it.nmax;         // the consumers need not count the kept blocks again
         mbar_arrive(&bars->item_full[q]);
         if (idx < 0) break;
-        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, pr);
         idx = static_cast<int>(atomicAdd(sched, 1u)) + kClaim * static_cast<int>(gridDim.x);
         if (it.nmax == 0) continue;
         // boxes: packed (column, head, token); dense (column, row, unit), or
@@ -507,10 +523,12 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       // so that its first S_t can be issued before the current item's last P.V.
       int k = 0;                 // queue index of the current item
       int next_idx = -2;         // queue entry k + 1 once read (-2: not yet)
+      int kept = -1;             // the current item's kept blocks (per-slot pipelines)
       auto take = [&](int kk, int& idx) {
         const int q = ring * kItemQueue + kk % kItemQueue;
         if (!wait(&bars->item_full[q], (kk / kItemQueue) & 1)) return false;
         idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
+        if (C::kTileStreams) kept = *reinterpret_cast<volatile int*>(&bars->item_n[q]);
         mbar_arrive(&bars->item_empty[q]);
         return true;
       };
@@ -532,14 +550,14 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         tc_fence_after();
         issue_qk(t, qb, slot_of(xfill));
         mma_commit(&bars->s_full[t]);
-        if (nt == 1) mma_commit(&bars->q_empty[qb]);
+        if (!C::kStageQ && nt == 1) mma_commit(&bars->q_empty[qb]);
         return true;
       };
       bool ok = true;
       int idx = -1;
       ok = take(0, idx);
       while (ok && idx >= 0) {
-        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, t_lo);
+        const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, t_lo, kept);
         int qbuf[2];             // Q buffer of this item per tile
         for (int t = t_lo; t < t_hi; ++t) qbuf[t] = t * C::kQBufs + (qloads[t] - (pre[t] ? 1 : 0)) % C::kQBufs;
         if (it.nmax > 0) {
@@ -582,7 +600,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               tc_fence_after();
               issue_qk(t, qbuf[t], slot_of(kpos));
               mma_commit(&bars->s_full[t]);
-              if (j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
+              if (!C::kStageQ && j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
             } else if (!C::kPAlias && !C::kTileStreams && j + 1 == nt) {
               // last block of this tile: read the next work item and issue its
               // first S_t now, under this block's softmax
@@ -609,7 +627,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
               // P_t overlays S_t: the next S_t is issued behind the MMA that reads P_t
               issue_qk(t, qbuf[t], slot_of(kpos));
               mma_commit(&bars->s_full[t]);
-              if (j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
+              if (!C::kStageQ && j + 2 == nt) mma_commit(&bars->q_empty[qbuf[t]]);
             }
           }
           mma_commit(&bars->empty[slot_of(vpos)]);
@@ -658,7 +676,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       bool on;
       float m, l;
       long long orow, li;     // output row offset (elements) and LSE index; orow < 0: row past the end
-    } pend{false, 0.f, 0.f, -1, 0};
+      int qb;                 // the item's Q buffer
+    } pend{false, 0.f, 0.f, -1, 0, 0};
+    int qn = 0;               // Q tiles this group's tile has been loaded with
     auto epilogue = [&](const Pending& e) {
       tc_fence_after();
       // l = 0 only for a row with no visible key (block-sparse): O = 0, LSE = -inf
@@ -676,7 +696,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       // O_t has been read out: the next item's first P.V may overwrite it
       tc_fence_before();
       mbar_arrive(&bars->o_free[t]);
-      if constexpr (C::kStageO) {
+      if constexpr (C::kStageQ || C::kStageO) {
         // The warp's 32 rows go through shared memory: each lane writes its
         // row as 16-byte chunks (chunk c of row r at slot c ^ f(r), so the 8
         // lanes of a quarter-warp hit 8 different bank groups), then each
@@ -685,8 +705,10 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         constexpr int kChunks = D / 8;                     // 16-byte chunks per row
         constexpr int kRowsPer = 32 / kChunks;             // rows per store instruction
         auto slot = [](int r, int c) { return c ^ (kChunks == 8 ? (r & 7) : ((r >> 1) & 3)); };
-        const uint32_t stage = smem_u32(smem + C::kOffStage + warp * C::kStageWarpBytes);
-        __syncwarp();                                      // the previous epilogue's reads are done
+        const uint32_t stage = C::kStageQ
+                                   ? smem_u32(smem + C::kOffQ + e.qb * C::kTileBytes + (warp & 3) * C::kStageWarpBytes)
+                                   : smem_u32(smem + C::kOffStage + warp * C::kStageWarpBytes);
+        if (C::kStageO) __syncwarp();                      // the previous epilogue's reads are done
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
@@ -703,6 +725,14 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
                        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(stage + (r * kChunks + slot(r, c)) * 16)
                        : "memory");
           if (orow >= 0) *reinterpret_cast<uint4*>(static_cast<T*>(p.o) + orow + 8 * c) = w;
+        }
+        if constexpr (C::kStageQ) {
+          // the staged rows have been read out: the producer may load the next
+          // Q into the buffer (its copy is an async-proxy write after these
+          // generic accesses)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->q_empty[e.qb]);
         }
         if (e.orow >= 0) p.lse[e.li] = e.l > 0.f ? (e.m + __log2f(e.l)) * kLn2 : -INFINITY;
       } else if (e.orow >= 0) {
@@ -735,10 +765,11 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       const int q = (C::kTileStreams ? t * kItemQueue : 0) + k % kItemQueue;
       if (!(ok = wait_all(&bars->item_full[q], (k / kItemQueue) & 1))) break;
       const int idx = *reinterpret_cast<volatile int*>(&bars->item[q]);
+      const int kept = C::kTileStreams ? *reinterpret_cast<volatile int*>(&bars->item_n[q]) : -1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[q]);
       if (idx < 0) break;
-      const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, t);
+      const Item it = decode_item<CAUSAL, PACKED, SPARSE, C::kTileStreams>(p, idx, nper, t, kept);
       const int nt = t == 0 ? it.n0 : it.n1;
       const int rt = it.r0 + t * BM;
       const int row = rt + rl;                // row within the unit
@@ -753,6 +784,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         }
         continue;
       }
+      const int qb_item = t * C::kQBufs + qn % C::kQBufs;   // the producer loaded this tile's Q there
+      ++qn;
       constexpr bool sparse = SPARSE;
       const unsigned char* mine = t == 0 ? it.m0 : it.m1;
       if (BIAS) issue_mask(it, 0);           // the item's first mask block
@@ -979,6 +1012,7 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       pend.on = true;
       pend.m = m_run;
       pend.l = l;
+      pend.qb = qb_item;
       pend.orow = row < it.len_q ? (PACKED    ? (static_cast<long long>(it.tok0 + row) * p.H + it.h) * D
                                     : STRIDED ? dense_off(p, kTo, it.unit / p.H, it.unit % p.H, row)
                                               : (static_cast<long long>(it.unit) * it.len_q + row) * D)
