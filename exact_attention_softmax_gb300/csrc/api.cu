@@ -397,7 +397,6 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
   if (!dO || !dq || !dk || !dv) return fail(SDPA_ERR_ARG, "null gradient pointer");
   if (dtype != SDPA_F32 && !(aligned16(dO) && aligned16(dq) && aligned16(dk) && aligned16(dv)))
     return fail(SDPA_ERR_ARG, "fp16/bf16 gradients must be 16-byte aligned");
-  if (dtype != SDPA_F32 && sh.d == 32) return fail(SDPA_ERR_UNSUPPORTED, "fp16/bf16 backward supports d in {64, 128}");
   const bool packed = sh.packed();
   // packed: the row statistics and dQ accumulator cover the total query rows
   const int nb = packed ? 1 : sh.B;

@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdProblem bp, long long 
   }
 }
 
-// Eight elements of one row per thread (the fp16 / bf16 head dims, 64 or
-// 128, are multiples of 8): two 16-byte loads of the contiguous accumulator,
+// Eight elements of one row per thread (the fp16 / bf16 head dims, 32, 64
+// or 128, are multiples of 8): two 16-byte loads of the contiguous accumulator,
 // one 16-byte store into dQ at its strides. Dense: blockIdx.y walks the units
 // and x the chunks of a unit; packed ([total, H, d], contiguous): x walks all.
 template <typename T, int D>
@@ -150,7 +150,10 @@ cudaError_t launch_dq_convert(const BwdProblem& bp, int dtype, cudaStream_t s) {
   const long long chunks = rows_per_unit(p) * p.d / 8;
   if (chunks == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>((chunks + 255) / 256), unit_blocks(p));
-  if (p.d == 64) {
+  if (p.d == 32) {
+    if (dtype == kF16) dq_convert_kernel<__half, 32><<<grid, 256, 0, s>>>(bp, chunks);
+    else dq_convert_kernel<__nv_bfloat16, 32><<<grid, 256, 0, s>>>(bp, chunks);
+  } else if (p.d == 64) {
     if (dtype == kF16) dq_convert_kernel<__half, 64><<<grid, 256, 0, s>>>(bp, chunks);
     else dq_convert_kernel<__nv_bfloat16, 64><<<grid, 256, 0, s>>>(bp, chunks);
   } else if (p.d == 128) {

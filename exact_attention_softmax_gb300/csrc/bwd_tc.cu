@@ -57,9 +57,9 @@ struct BCfg {
   static constexpr int kHalf = BQ / 2;                       // query columns per softmax group
   static constexpr bool kDqT = D == 128;                     // dQ computed transposed
   // Which MMA warp issues the dQ MMAs, so the two warps issue about as many
-  // MMAs per tile: d = 64 -> the S^T/dP^T warp (8 + 8 vs 16), d = 128 -> the
-  // dV/dK warp (16 vs 8 + 8).
-  static constexpr bool kDqOnS = D == 64;
+  // MMAs per tile: d <= 64 -> the S^T/dP^T warp (d = 64: 8 + 8 vs 16, d = 32:
+  // 4 + 8 vs 16), d = 128 -> the dV/dK warp (16 vs 8 + 8).
+  static constexpr bool kDqOnS = D <= 64;
   static constexpr int kBlk = D >= 64 ? 64 : D;
   static constexpr int kNBlk = D / kBlk;
   static constexpr uint32_t kSw = D >= 64 ? kSwizzle128B : kSwizzle64B;
@@ -73,11 +73,11 @@ struct BCfg {
   static constexpr int kPBytes = BK * BQ * 2;
   // Q/dO stages: a stage stays busy from its load until the dV/dK MMAs of
   // its step, about one step after its S^T MMA; a third stage lets the next
-  // load start early enough at d = 64 (the additive-mask kernel, with its
+  // load start early enough at d <= 64 (the additive-mask kernel, with its
   // mask ring, has no room for it; at d = 128, with dS^T in TMEM, a third
   // stage measured slower: 5140 against 5091 us on the long causal batch)
   static constexpr bool kMask = EXT == 2;
-  static constexpr int kStages = D == 64 && !kMask ? 3 : 2;
+  static constexpr int kStages = D <= 64 && !kMask ? 3 : 2;
   // shared memory map
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKTile;
@@ -735,9 +735,10 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     if (ok) {
       // group 0 writes dV, group 1 writes dK = scale * dK_acc. Every MMA that
       // read the Q/dO stages has finished (kv_done), so each warp stages its
-      // 32 rows there (16-byte chunk c of row r at slot c ^ (r % 8): the 8
-      // lanes of a quarter-warp hit 8 different bank groups) and stores them
-      // back whole rows per instruction instead of 32 rows of 16 bytes.
+      // 32 rows there (16-byte chunk c of row r at slot c ^ f(r), f(r) = r % 8,
+      // or (r / 2) % 4 for the 4-chunk rows of d = 32: the 8 lanes of a
+      // quarter-warp hit 8 different bank groups) and stores them back whole
+      // rows per instruction instead of 32 rows of 16 bytes.
       tc_fence_after();
       const uint32_t col0 = half == 0 ? C::kTdV : C::kTdK;
       const float sc = half == 0 ? 1.f : p.scale;
@@ -747,6 +748,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
                           : (static_cast<long long>(unit) * Lk + key) * D);
       constexpr int kChunks = D / 8;                   // 16-byte chunks per row
       constexpr int kRowsPer = 32 / kChunks;           // rows per store instruction
+      auto sw = [](int rr) { return kChunks >= 8 ? (rr & 7) : ((rr >> 1) & 3); };
       static_assert(8 * 32 * D * 2 <= 2 * C::kStages * C::kQTile, "the Q/dO stages hold the staged rows");
       const uint32_t stage = smem_u32(smem + C::kOffQ + warp * 32 * D * 2);
 #pragma unroll 1
@@ -761,7 +763,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int chunk = cc * 4 + e;
-          st_shared_v4(stage + (lane * kChunks + (chunk ^ (lane & 7))) * 16,
+          st_shared_v4(stage + (lane * kChunks + (chunk ^ sw(lane))) * 16,
                        Pack2<T>::pack(__uint_as_float(o[8 * e + 0]) * sc, __uint_as_float(o[8 * e + 1]) * sc),
                        Pack2<T>::pack(__uint_as_float(o[8 * e + 2]) * sc, __uint_as_float(o[8 * e + 3]) * sc),
                        Pack2<T>::pack(__uint_as_float(o[8 * e + 4]) * sc, __uint_as_float(o[8 * e + 5]) * sc),
@@ -777,7 +779,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         const T* dst = reinterpret_cast<const T*>(__shfl_sync(0xffffffffu, base, rr));
         uint4 w;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(stage + (rr * kChunks + (c ^ (rr & 7))) * 16)
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(stage + (rr * kChunks + (c ^ sw(rr))) * 16)
                      : "memory");
         if (key - lane + rr < Lk) *reinterpret_cast<uint4*>(const_cast<T*>(dst) + 8 * c) = w;
       }
@@ -846,9 +848,11 @@ cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
 
 cudaError_t launch_bwd_tc(const BwdProblem& bp, int dtype, const BwdMaps& m, cudaStream_t s) {
   if (dtype == kF16) {
+    if (bp.f.d == 32) return launch_d<32, __half>(bp, m, s);
     if (bp.f.d == 64) return launch_d<64, __half>(bp, m, s);
     if (bp.f.d == 128) return launch_d<128, __half>(bp, m, s);
   } else if (dtype == kBF16) {
+    if (bp.f.d == 32) return launch_d<32, __nv_bfloat16>(bp, m, s);
     if (bp.f.d == 64) return launch_d<64, __nv_bfloat16>(bp, m, s);
     if (bp.f.d == 128) return launch_d<128, __nv_bfloat16>(bp, m, s);
   }

@@ -153,7 +153,7 @@ size_t sdpa_bwd_workspace_size(int B, int H, int Lq, int d, int dtype);
  *               256-byte aligned; its contents on entry do not matter.
  * Other arguments as for sdpa_fwd, dense or packed (cu_seqlens != NULL; the
  * workspace is then sized with B = 1 and Lq = total). Supported: F32 with
- * d <= 128; F16/BF16 with d in {64, 128}.
+ * d <= 128; F16/BF16 with d in {32, 64, 128}.
  */
 int sdpa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dO, void* dq, void* dk, void* dv,
@@ -180,7 +180,7 @@ int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
  * Backward of sdpa_fwd_varlen: dq [total_q, H, d], dk and dv [total_k, H, d],
  * fully overwritten. Arguments as for sdpa_fwd_varlen plus those of sdpa_bwd;
  * the workspace is sdpa_bwd_workspace_size(1, H, total_q, d, dtype) bytes.
- * Supported: F32 with d <= 128; F16/BF16 with d in {64, 128}.
+ * Supported: F32 with d <= 128; F16/BF16 with d in {32, 64, 128}.
  */
 int sdpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
                     const void* dO, void* dq, void* dk, void* dv,

@@ -118,7 +118,7 @@ def test_varlen_cross_argument_errors(lib):
     args = [FAKE] * 9 + [3, H, tq, 900, 300, 400, d, 0.125, 1, FAKE, FAKE, 1]
     assert lib.sdpa_bwd_varlen(*args, FAKE, need - 1, None) == _abi.SDPA_ERR_WORKSPACE
     assert lib.sdpa_bwd_varlen(*(args[:19] + [None] + args[20:]), FAKE, need, None) == _abi.SDPA_ERR_ARG
-    assert lib.sdpa_bwd_varlen(*(args[:15] + [32] + args[16:]), FAKE, need, None) == _abi.SDPA_ERR_UNSUPPORTED
+    assert lib.sdpa_bwd_varlen(*(args[:15] + [48] + args[16:]), FAKE, need, None) == _abi.SDPA_ERR_UNSUPPORTED
 
 
 def test_masked_and_blocksparse_argument_errors(lib):

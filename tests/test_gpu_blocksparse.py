@@ -72,7 +72,7 @@ SHAPES = [(1, 2, 300, 333), (2, 1, 256, 512), (1, 1, 640, 200)]
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_blocksparse_fwd_bwd(dtype, d, causal, shape):

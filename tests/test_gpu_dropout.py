@@ -56,7 +56,7 @@ SHAPES = [(1, 2, 300, 333), (2, 1, 256, 200)]
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_dropout_fwd_bwd(dtype, d, causal, shape):

@@ -65,7 +65,7 @@ SHAPES = [(1, 2, 300, 333), (2, 1, 256, 200), (1, 1, 129, 520)]
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_masked_fwd_bwd(dtype, d, causal, shape):
@@ -89,7 +89,7 @@ def test_masked_broadcast_and_d32_forward(causal):
     _check_fwd(got, _oracle(x, mask, Lk, causal, 0.2, bwd=False), "f16")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("mshape", ["hqk", "qk", "b1qk"])
 def test_masked_broadcast_bwd(d, mshape):
     """Masks shared across the batch ([H, Lq, Lk]), across everything

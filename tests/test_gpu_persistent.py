@@ -5,8 +5,7 @@ the dropout counters from one item into the next. These batches have 240
 items (2 x 40 heads x 3 items of 256, 256 and 88 rows) on at most 152 CTAs,
 so that hand-over runs many times per CTA. Every (batch, head) unit is
 compared with the fp64 oracle: O and LSE by max-abs error, each gradient by
-its relative Frobenius error per unit. The backward (d = 64) runs on the same
-inputs. Plain bf16, the additive mask (per head and shared across the batch,
+its relative Frobenius error per unit. The backward runs on the same inputs. Plain bf16, the additive mask (per head and shared across the batch,
 which also reorders the items, or one per (batch, head)) and dropout are
 covered; the plain fp16 path has its many-item cases in the full-size
 workload tests."""
@@ -99,9 +98,9 @@ def _compare_units(got, ref, dtype):
 @pytest.mark.parametrize("d", [32, 64])
 @pytest.mark.parametrize("causal", [False, True])
 def test_plain_bf16_many_items(d, causal):
-    x = wl.dense_inputs(B, H, L, L, d, "bf16", "normal", seed=61, with_do=d == 64)
+    x = wl.dense_inputs(B, H, L, L, d, "bf16", "normal", seed=61, with_do=True)
     scale = d ** -0.5
-    bwd = d == 64          # the fp16/bf16 backward covers d in {64, 128}
+    bwd = True
     _compare_units(_call(x, causal, scale, bwd), _oracle(x, causal, scale, bwd), "bf16")
 
 
@@ -109,11 +108,11 @@ def test_plain_bf16_many_items(d, causal):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shared", [True, False], ids=["per-head-shared-over-batch", "per-unit"])
 def test_masked_many_items(dtype, d, causal, shared):
-    x = wl.dense_inputs(B, H, L, L, d, dtype, "normal", seed=62, with_do=d == 64)
+    x = wl.dense_inputs(B, H, L, L, d, dtype, "normal", seed=62, with_do=True)
     lead = (1, H) if shared else (B, H)
     mask = wl.attn_mask(lead + (L, L), dtype, seed=63, empty_rows=(5, 300))[..., :L]
     scale = d ** -0.5
-    bwd = d == 64
+    bwd = True
     got = _call(x, causal, scale, bwd, mask=mask)
     ref = _oracle(x, causal, scale, bwd, mask=mask)
     _compare_units(got, ref, dtype)
@@ -122,9 +121,9 @@ def test_masked_many_items(dtype, d, causal, shared):
 @pytest.mark.parametrize("dtype,d", [("f16", 32), ("bf16", 32), ("f16", 64), ("bf16", 64)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_dropout_many_items(dtype, d, causal):
-    x = wl.dense_inputs(B, H, L, L, d, dtype, "normal", seed=64, with_do=d == 64)
+    x = wl.dense_inputs(B, H, L, L, d, dtype, "normal", seed=64, with_do=True)
     scale = d ** -0.5
-    bwd = d == 64
+    bwd = True
     got = _call(x, causal, scale, bwd, dropout=0.3)
     ref = _oracle(x, causal, scale, bwd, dropout=0.3)
     _compare_units(got, ref, dtype)

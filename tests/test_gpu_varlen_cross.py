@@ -26,7 +26,7 @@ LK = [200, 5, 64, 7, 129, 1, 383]
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_cross_fwd_bwd(dtype, d, causal):
     from _gpu import assert_fwd_close, assert_grads_close, oracle_varlen_cross, run_varlen_cross
