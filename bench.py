@@ -477,6 +477,19 @@ def extra_results(dev, flush, peaks):
           "written into [B, L, E] / [B, L, 3E] views (strided calls, no copy)")
     del qkv, q, k, v, do, o, dqkv, g3, lse, ws
 
+    # the dispatcher example's d = 32 batch, trained: forward and backward
+    B, H, L, d = 32, 32, 1024, 32
+    x = wl.dense_inputs(B, H, L, L, d, "f16", "normal", seed=0)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = ops.sdpa_fwd(q, k, v)
+    ws = torch.empty(ops.sdpa_bwd_workspace_size(B, H, L, d, 1), dtype=torch.uint8, device=dev)
+    g = [torch.empty_like(t) for t in (q, k, v)]
+    timed("dense_f16_d32_train", lambda: ops.sdpa_fwd(q, k, v, o, lse),
+          lambda: ops.sdpa_bwd(q, k, v, o, lse, do, *g, workspace=ws),
+          4.0 * d * B * H * L * L, 2.5 * 4.0 * d * B * H * L * L,
+          f"B={B} H={H} L={L} d={d} f16 non-causal, forward and backward")
+    del x, q, k, v, do, o, lse, ws, g
+
     # packed cross-attention: 32 sequences, queries around 256 long, keys around 512
     lq = wl.varlen_lengths(32, 512, 0.5, 0)
     lk = wl.varlen_lengths(32, 1024, 0.5, 1)
