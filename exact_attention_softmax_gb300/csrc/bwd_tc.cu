@@ -119,8 +119,9 @@ struct __align__(8) BBars {
   uint64_t kv;
   uint64_t full[3];
   uint64_t empty[3];
-  uint64_t s_full;     // S^T, dP^T of the current tile in TMEM
-  uint64_t s_free;     // ... read into registers by both softmax groups
+  uint64_t s_full;     // S^T of the current tile in TMEM
+  uint64_t dp_full;    // dP^T of the current tile in TMEM
+  uint64_t s_free;     // S^T and dP^T read into registers by both softmax groups
   uint64_t pds_full;   // P^T, dS^T in shared memory
   uint64_t pds_free;   // ... consumed by the dV, dK, dQ MMAs
   uint64_t dq_full[2];
@@ -209,6 +210,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   // TMEM a chunk at a time); the other kernels take the half in one piece.
   constexpr int CH = (BIAS || DROP) && NH > 32 ? 32 : NH;
   constexpr int NCH = NH / CH;
+  constexpr bool kSplitDP = NCH == 1 && CH <= 32;   // P from S^T before dP^T is read
   static_assert(!BIAS || CH * BK * 2 == C::kMaskTile, "a mask slot holds one chunk of each softmax group");
   const Problem& p = bp.f;
   extern __shared__ uint8_t smem_raw[];
@@ -273,6 +275,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       mbar_init(&bars->dq_free[i], 128);
     }
     mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->s_free, 256);
     mbar_init(&bars->pds_full, 256);
     mbar_init(&bars->pds_free, 2);     // dV/dK warp and dQ warp
@@ -436,13 +439,15 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             const uint32_t ko = (cb * C::kKColBlk + within) >> 4, qo = qoff + ((cb * C::kQColBlk + within) >> 4);
             mma_ss(tmem + C::kTS, dK0 + ko, dQ0 + qo, idS, ks > 0);
           }
+          // S^T alone lets the softmax groups start on P while dP^T computes
+          mma_commit(&bars->s_full);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t cb = ks * 16 / C::kBlk, within = (ks * 16 % C::kBlk) * 2;
             const uint32_t ko = (cb * C::kKColBlk + within) >> 4, qo = qoff + ((cb * C::kQColBlk + within) >> 4);
             mma_ss(tmem + C::kTdP, dV0 + ko, dO0 + qo, idS, ks > 0);
           }
-          mma_commit(&bars->s_full);
+          mma_commit(&bars->dp_full);
           // dQ of the previous tile: needs its dS^T and a free dQ buffer
           if (C::kDqOnS && s > 0 && !(ok = issue_dq(s - 1))) break;
         }
@@ -591,18 +596,23 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     const T* mkey = reinterpret_cast<const T*>(smem + C::kOffList + half * C::kMaskTile) + r;
     for (int s = 0; s < nsteps; ++s) {
       const int stage = s % C::kStages;
+      // With one chunk of at most 32 columns (d = 128) P is computed from S^T
+      // while the dP^T MMAs run, and dP^T is loaded after it; otherwise (the
+      // 64 columns of d <= 64 would then spill) both are loaded together.
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, abort_flag, p.status) &&
-                                       mbar_wait(&bars->full[stage], (s / C::kStages) & 1, abort_flag, p.status));
+                                       mbar_wait(&bars->full[stage], (s / C::kStages) & 1, abort_flag, p.status) &&
+                                       (kSplitDP || mbar_wait(&bars->dp_full, s & 1, abort_flag, p.status)));
       if (!ok) break;
       tc_fence_after();
       uint32_t sv[NCH][CH], dv[NCH][CH];
 #pragma unroll
       for (int cc = 0; cc < CH / 32; ++cc) {
         tmem_ld32(tmem + lane_off + C::kTS + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[0][cc * 32]));
-        tmem_ld32(tmem + lane_off + C::kTdP + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[0][cc * 32]));
+        if (!kSplitDP)
+          tmem_ld32(tmem + lane_off + C::kTdP + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[0][cc * 32]));
       }
       tmem_ld_wait();
-      if (NCH == 1) {
+      if (NCH == 1 && !kSplitDP) {
         tc_fence_before();
         mbar_arrive(&bars->s_free);             // the next S^T / dP^T may be written
       }
@@ -637,7 +647,45 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         // row statistics of these query columns (written by the producer
         // before it arrived on full[stage])
         const float* slf = stat + stage * 2 * BQ + half * NH + ch * CH;
-        // the per-element causal / length test only where the tile needs it
+        // dropout factor of (query q0 + col, key)
+        auto zf_of = [&](int col) {
+          if (!DROP) return 1.f;
+          const uint32_t byte = __byte_perm(dw[col >> 4][(col & 15) >> 2], 0u, 0x4440u | (col & 3));
+          return byte >= p.drop_t ? p.drop_scale : 0.f;
+        };
+        // P of this chunk, kept (as bits, in place of S) for dS and packed
+        // for P^T; the per-element causal / length test only where the tile
+        // needs it
+        auto body_p = [&](auto masked) {
+          constexpr bool M = decltype(masked)::value;
+#pragma unroll
+          for (int g = 0; g < CH / 4; ++g) {
+            // loaded in program order: hoisting them costs registers and spills
+            float l4[4];
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(l4[0]), "=f"(l4[1]), "=f"(l4[2]), "=f"(l4[3]) : "r"(smem_u32(slf + 4 * g)));
+            float pr[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int col = 4 * g + h;
+              // P = 2^(S * scale * log2(e) - LSE2); with a mask S * scale + M
+              // is formed first, in natural-log units. (The plain d = 64
+              // kernels keep the addend as a subtraction: with the negated
+              // operand ptxas spills there and they measured slower.)
+              const float s_ = __uint_as_float(sv[ch][col]);
+              float pv;
+              if (BIAS) pv = ex2_approx(fmaf(fmaf(s_, p.scale, to_f32(mt[col * BK])), kLog2e, -l4[h]));
+              else if (D == 128 || DROP) pv = ex2_approx(fmaf(s_, c, -l4[h]));
+              else pv = ex2_approx(fmaf(s_, c, 0.f - l4[h]));
+              if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
+              sv[ch][col] = __float_as_uint(pv);
+              pr[h] = pv * zf_of(col);
+            }
+            pk[2 * g] = Pack2<T>::pack(pr[0], pr[1]);
+            pk[2 * g + 1] = Pack2<T>::pack(pr[2], pr[3]);
+          }
+        };
+        // P and dS together (when dP^T is already in registers)
         auto body = [&](auto masked) {
           constexpr bool M = decltype(masked)::value;
 #pragma unroll
@@ -652,21 +700,13 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               const int col = 4 * g + h;
-              // P = 2^(S * scale * log2(e) - LSE2); with a mask S * scale + M
-              // is formed first, in natural-log units. (The plain d = 64
-              // kernels keep the addend as a subtraction: with the negated
-              // operand ptxas spills there and they measured slower.)
               const float s_ = __uint_as_float(sv[ch][col]);
               float pv;
               if (BIAS) pv = ex2_approx(fmaf(fmaf(s_, p.scale, to_f32(mt[col * BK])), kLog2e, -l4[h]));
               else if (D == 128 || DROP) pv = ex2_approx(fmaf(s_, c, -l4[h]));
               else pv = ex2_approx(fmaf(s_, c, 0.f - l4[h]));
               if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
-              float zf = 1.f;           // dropout factor of (query q0 + col, key)
-              if (DROP) {
-                const uint32_t byte = __byte_perm(dw[col >> 4][(col & 15) >> 2], 0u, 0x4440u | (col & 3));
-                zf = byte >= p.drop_t ? p.drop_scale : 0.f;
-              }
+              const float zf = zf_of(col);
               pr[h] = pv * zf;
               ds[h] = pv * (__uint_as_float(dv[ch][col]) * zf - d4[h]);
             }
@@ -676,8 +716,41 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             dk[2 * g + 1] = Pack2<T>::pack(ds[2], ds[3]);
           }
         };
-        if (need_mask) body(std::true_type{});
-        else body(std::false_type{});
+        // dS = P * (dP - D) of this chunk (dropout: P * (dP * z - D)), packed
+        auto body_ds = [&]() {
+#pragma unroll
+          for (int g = 0; g < CH / 4; ++g) {
+            float d4[4];
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(d4[0]), "=f"(d4[1]), "=f"(d4[2]), "=f"(d4[3]) : "r"(smem_u32(slf + BQ + 4 * g)));
+            float ds[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int col = 4 * g + h;
+              ds[h] = __uint_as_float(sv[ch][col]) * (__uint_as_float(dv[ch][col]) * zf_of(col) - d4[h]);
+            }
+            dk[2 * g] = Pack2<T>::pack(ds[0], ds[1]);
+            dk[2 * g + 1] = Pack2<T>::pack(ds[2], ds[3]);
+          }
+        };
+        if constexpr (!kSplitDP) {
+          if (need_mask) body(std::true_type{});
+          else body(std::false_type{});
+        } else {
+          if (need_mask) body_p(std::true_type{});
+          else body_p(std::false_type{});
+          // dP^T, whose MMAs ran while P was computed
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full, s & 1, abort_flag, p.status));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < CH / 32; ++cc)
+            tmem_ld32(tmem + lane_off + C::kTdP + half * NH + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[0][cc * 32]));
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->s_free);             // the next S^T / dP^T may be written
+          body_ds();
+        }
         if (BIAS) {
           __syncwarp();
           if ((threadIdx.x & 31) == 0) mbar_arrive(&bars->mempty[n & 1]);   // slot read
