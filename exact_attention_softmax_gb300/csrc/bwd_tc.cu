@@ -122,8 +122,10 @@ struct __align__(8) BBars {
   uint64_t s_full;     // S^T of the current tile in TMEM
   uint64_t dp_full;    // dP^T of the current tile in TMEM
   uint64_t s_free;     // S^T and dP^T read into registers by both softmax groups
-  uint64_t pds_full;   // P^T, dS^T in shared memory
-  uint64_t pds_free;   // ... consumed by the dV, dK, dQ MMAs
+  uint64_t pds_full;   // P^T, dS^T in TMEM / shared memory (d = 128: dS^T only)
+  uint64_t pds_free;   // ... consumed by the dV, dK, dQ MMAs (d = 128: dK, dQ)
+  uint64_t p_full;     // d = 128: P^T in TMEM, ahead of dS^T
+  uint64_t p_free;     // ... consumed by the dV MMAs
   uint64_t dq_full[2];
   uint64_t dq_free[2];
   uint64_t kv_done;
@@ -210,7 +212,10 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
   // TMEM a chunk at a time); the other kernels take the half in one piece.
   constexpr int CH = (BIAS || DROP) && NH > 32 ? 32 : NH;
   constexpr int NCH = NH / CH;
-  constexpr bool kSplitDP = NCH == 1 && CH <= 32;   // P from S^T before dP^T is read
+  // P from S^T before dP^T is read, and P^T handed to the dV MMA before dS^T
+  // is formed (one chunk of at most 32 columns: d = 128)
+  constexpr bool kSplitDP = NCH == 1 && CH <= 32;
+  static_assert(!kSplitDP || C::kDsTmem, "the split path stores dS^T in TMEM");
   static_assert(!BIAS || CH * BK * 2 == C::kMaskTile, "a mask slot holds one chunk of each softmax group");
   const Problem& p = bp.f;
   extern __shared__ uint8_t smem_raw[];
@@ -279,6 +284,8 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     mbar_init(&bars->s_free, 256);
     mbar_init(&bars->pds_full, 256);
     mbar_init(&bars->pds_free, 2);     // dV/dK warp and dQ warp
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->p_free, 1);
     mbar_init(&bars->kv_done, 1);
     mbar_init(&bars->done, 2);
     for (int i = 0; i < 2; ++i) {
@@ -460,9 +467,29 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         const uint64_t dOm = smem_desc(sDO, C::kQColBlk, C::kSbo, C::kSw);
         for (int s = 0; s < nsteps && ok; ++s) {
           const int stage = s % C::kStages;
+          const uint32_t qoff = (stage * C::kQTile) >> 4;
+          if constexpr (kSplitDP) {
+            // dV as soon as P^T is in TMEM, then dK once dS^T is
+            if (!(ok = wait(&bars->p_full, s & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BQ / 16; ++ks)
+              mma_ts(tmem + C::kTdV, tmem + C::kTP + ks * 8, dOm + qoff + ((ks * 16 * C::kRowBytes) >> 4), idKV,
+                     (s > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&bars->p_free);
+            if (!(ok = wait(&bars->pds_full, s & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BQ / 16; ++ks)
+              mma_ts(tmem + C::kTdK, tmem + C::kTDS + ks * 8, dQm + qoff + ((ks * 16 * C::kRowBytes) >> 4), idKV,
+                     (s > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&bars->pds_free);
+            mma_commit(&bars->empty[stage]);
+            if (!C::kDqOnS && !(ok = issue_dq(s))) break;
+            continue;
+          }
           if (!(ok = wait(&bars->pds_full, s & 1))) break;
           tc_fence_after();
-          const uint32_t qoff = (stage * C::kQTile) >> 4;
 #pragma unroll
           for (int ks = 0; ks < BQ / 16; ++ks) {
             const uint32_t aoff = ((ks / 4) * C::kPColBlk + (ks % 4) * 32) >> 4;
@@ -739,6 +766,18 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         } else {
           if (need_mask) body_p(std::true_type{});
           else body_p(std::false_type{});
+          // P^T into TMEM once the previous step's dV MMAs have read it, so
+          // this step's dV runs while dS is formed
+          if (s > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_free, (s - 1) & 1, abort_flag, p.status));
+          if (!ok) break;
+          {
+            const uint32_t tp = tmem + lane_off + C::kTP + (half * NH) / 2;
+#pragma unroll
+            for (int x = 0; x < CH / 32; ++x) tmem_st16(tp + x * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * x]));
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full);
           // dP^T, whose MMAs ran while P was computed
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full, s & 1, abort_flag, p.status));
           if (!ok) break;
@@ -781,7 +820,7 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             const uint32_t td = tmem + lane_off + C::kTDS + (half * NH + ch * CH) / 2;
 #pragma unroll
             for (int x = 0; x < CH / 32; ++x) {
-              tmem_st16(tp + x * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * x]));
+              if (!kSplitDP) tmem_st16(tp + x * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * x]));
               tmem_st16(td + x * 16, *reinterpret_cast<const uint32_t(*)[16]>(&dk[16 * x]));
             }
           } else if constexpr (CH == 64) {
