@@ -23,7 +23,7 @@ __all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_f
            "sdpa_bwd_blocksparse", "sdpa_fwd_masked", "sdpa_bwd_masked", "sdpa_fwd_dropout",
            "sdpa_bwd_dropout", "sdpa_bwd_workspace_size",
            "sdpa_device_status", "sdpa_trace_events",
-           "sdpa_debug_set", "sdpa_last_error", "sdpa_version", "SdpaError"]
+           "sdpa_debug_set", "sdpa_debug_build", "sdpa_last_error", "sdpa_version", "SdpaError"]
 
 
 def _dtype_code(t):
@@ -455,3 +455,8 @@ def sdpa_last_error() -> str:
 
 def sdpa_version() -> int:
     return int(_abi.load().sdpa_version())
+
+
+def sdpa_debug_build() -> int:
+    """1 if the loaded library is the debug build (device-side bounds checks)."""
+    return int(_abi.load().sdpa_debug_build())

@@ -18,8 +18,14 @@ SDPA_ERR_UNSUPPORTED = -2
 SDPA_ERR_CUDA = -3
 SDPA_ERR_TIMEOUT = -4
 SDPA_ERR_WORKSPACE = -5
+SDPA_ERR_BOUNDS = -6
 SDPA_STATUS_TIMEOUT = 1
 SDPA_STATUS_SEQLEN = 2
+SDPA_STATUS_BOUNDS = 4
+
+# Another build of the library (e.g. the debug build,
+# ``lib/libsdpa_gb300_debug.so``) is loaded instead when this names it.
+LIB_ENV = "SDPA_GB300_LIB"
 
 # Every entry point the header declares, with its ctypes signature.
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -52,6 +58,7 @@ SIGNATURES = {
     "sdpa_debug_set": (_i, [_i]),
     "sdpa_last_error": (ctypes.c_char_p, []),
     "sdpa_version": (_i, []),
+    "sdpa_debug_build": (_i, []),
 }
 
 _lib = None
@@ -62,7 +69,7 @@ def load(path: str | None = None):
     global _lib
     if _lib is not None:
         return _lib
-    path = path or LIB_PATH
+    path = path or os.environ.get(LIB_ENV) or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is missing: build it with `python -m exact_attention_softmax_gb300.build` "

@@ -4,7 +4,11 @@ Every ``csrc/*.cu`` translation unit is compiled in parallel with
 ``nvcc -gencode arch=compute_103a,code=sm_103a`` and linked (static CUDA
 runtime, no libcuda link: the tensor-map encoder is fetched from the driver
 at run time) into ``exact_attention_softmax_gb300/lib/``. Run
-``python -m exact_attention_softmax_gb300.build`` or call :func:`build`.
+``python -m exact_attention_softmax_gb300.build`` or call :func:`build`;
+``--debug`` (``build(debug=True)``) builds ``libsdpa_gb300_debug.so`` instead,
+compiled with ``SDPA_DEBUG``: device-side bounds checks that skip a refused
+access and set a status bit rather than trap. The binding loads it when
+``SDPA_GB300_LIB`` names it.
 """
 from __future__ import annotations
 
@@ -23,6 +27,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libsdpa_gb300.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(LIB_DIR, "libsdpa_gb300_debug.so")
 # The exponential-unit throughput probe the benchmark measures its ceiling
 # with; a library of its own, outside the attention ABI.
 PROBE_DIR = os.path.join(PKG, "probe")
@@ -56,25 +62,29 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(x) > t for x in [src] + _headers())
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
-    """Compile (incrementally) and link the library; returns its path."""
+def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False, debug: bool = False) -> str:
+    """Compile (incrementally) and link the library (``debug``: the build with
+    device-side bounds checks); returns its path."""
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    flags = FLAGS + (["-DSDPA_DEBUG"] if debug else [])
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     # objects built on another host architecture are never reused
-    stamp = os.path.join(BUILD_DIR, "HOST_ARCH")
+    stamp = os.path.join(build_dir, "HOST_ARCH")
     here = platform.machine()
     if not os.path.exists(stamp) or open(stamp).read().strip() != here:
         force = True
     srcs = sources()
-    objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(pair):
         src, obj = pair
         if not force and not ptxas_info and not _stale(obj, src):
             return ""
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *flags, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -83,7 +93,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
     probe_srcs = sorted(os.path.join(PROBE_DIR, f) for f in os.listdir(PROBE_DIR) if f.endswith(".cu"))
 
     def build_probe():
-        if not force and os.path.exists(PROBE_PATH) and all(
+        if debug or not force and os.path.exists(PROBE_PATH) and all(
                 os.path.getmtime(PROBE_PATH) >= os.path.getmtime(x) for x in probe_srcs):
             return ""
         cmd = [nvcc, *ARCH, *FLAGS, "-shared", "-o", PROBE_PATH, *probe_srcs]
@@ -101,16 +111,16 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
             if log.strip():
                 print(f"== {os.path.basename(s)}\n{log}", file=sys.stderr)
     newest = max(os.path.getmtime(o) for o in objs)
-    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < newest:
-        tmp = LIB_PATH + ".tmp"
+    if force or not os.path.exists(lib_path) or os.path.getmtime(lib_path) < newest:
+        tmp = lib_path + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB_PATH)
+        os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(here + "\n")
-    return LIB_PATH
+    return lib_path
 
 
 def ensure_built() -> str:
@@ -118,4 +128,5 @@ def ensure_built() -> str:
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, ptxas_info="--ptxas" in sys.argv, force="--force" in sys.argv))
+    print(build(verbose=True, ptxas_info="--ptxas" in sys.argv, force="--force" in sys.argv,
+                debug="--debug" in sys.argv))

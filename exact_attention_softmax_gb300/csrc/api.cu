@@ -332,6 +332,20 @@ void set_strides(Problem& p, const long long* strides, int n) {
     for (int i = 0; i < 3; ++i) p.st[t][i] = strides[3 * t + i];
 }
 
+// Elements each tensor spans (largest element offset + 1) and rows of lse,
+// for the debug build's bounds checks; after set_strides.
+void set_extents(Problem& p, const Shape& sh) {
+  for (int t = 0; t < kTensors; ++t) {
+    const bool key = t == kTk || t == kTv || t == kTdk || t == kTdv;
+    const long long rows = key ? sh.total_k : sh.total_q;
+    if (sh.packed()) p.ext[t] = rows * sh.H * sh.d;
+    else if (sh.B == 0 || sh.H == 0 || rows == 0) p.ext[t] = 0;
+    else p.ext[t] = (sh.B - 1) * p.st[t][0] + (sh.H - 1) * p.st[t][1] + (rows - 1) * p.st[t][2] + sh.d;
+  }
+  p.lse_ext = static_cast<long long>(sh.packed() ? 1 : sh.B) * sh.H * sh.total_q;
+  if (p.debug & kDebugShortO) p.ext[kTo] -= sh.d;
+}
+
 int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o, float* lse, float scale,
             int is_causal, int dtype, void* stream, const BlockMask& bm = BlockMask{nullptr, 0, 0, 0}, bool sparse = false,
             const AddMask& am = AddMask{nullptr, 0, 0, 0}, bool masked = false,
@@ -348,6 +362,7 @@ int run_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* 
   Problem p{};
   fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am, dr);
   set_strides(p, strides, 4);
+  set_extents(p, sh);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -410,10 +425,12 @@ int run_bwd(const Shape& sh, const void* q, const void* k, const void* v, const 
   Problem& p = bp.f;
   fill_problem(p, sh, q, k, v, o, lse, scale, is_causal, bm, am, dr);
   set_strides(p, strides, kTensors);
+  set_extents(p, sh);
   rc = status_ptr(&p.status);
   if (rc != SDPA_OK) return rc;
   bp.dO = dO; bp.dq = dq; bp.dk = dk; bp.dv = dv;
   const size_t rows = static_cast<size_t>(nb) * sh.H * sh.total_q;
+  bp.acc_rows = static_cast<long long>(rows);
   bp.delta = static_cast<float*>(workspace);
   bp.dq_acc = dtype == SDPA_F32 ? nullptr
                                 : reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * 4 + 255) / 256 * 256);
@@ -599,6 +616,7 @@ extern "C" int sdpa_device_status(void* stream, unsigned* bits) {
   }
   if (bits) *bits = word;
   if (word & SDPA_STATUS_TIMEOUT) return fail(SDPA_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", word);
+  if (word & SDPA_STATUS_BOUNDS) return fail(SDPA_ERR_BOUNDS, "a device-side bounds check failed (status 0x%x)", word);
   if (word & SDPA_STATUS_SEQLEN) return fail(SDPA_ERR_ARG, "a packed sequence is longer than its bound or has queries but no keys (status 0x%x)", word);
   return SDPA_OK;
 }
@@ -622,3 +640,11 @@ extern "C" int sdpa_debug_set(int flags) {
 extern "C" const char* sdpa_last_error(void) { return g_last_error.c_str(); }
 
 extern "C" int sdpa_version(void) { return 100; }
+
+extern "C" int sdpa_debug_build(void) {
+#ifdef SDPA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdProblem bp, long long 
         const T* ge = reinterpret_cast<const T*>(&gv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc = fmaf(to_f<T>(oe[e]), to_f<T>(ge[e]), acc);
-        if (zero_acc) {
+        if (zero_acc && SDPA_CHECK(elem + sub * 8 + 8 <= bp.acc_rows * p.d, p.status)) {
           float4* A = reinterpret_cast<float4*>(bp.dq_acc + elem + sub * 8);
           A[0] = make_float4(0.f, 0.f, 0.f, 0.f);
           A[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdProblem bp, long long 
         const int c = sub * 8 + e;
         if (c < p.d) acc = fmaf(to_f<T>(O[c]), to_f<T>(dO[c]), acc);
       }
-      if (zero_acc) {
+      if (zero_acc && SDPA_CHECK(elem + p.d <= bp.acc_rows * p.d, p.status)) {
         float* A = bp.dq_acc + elem;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdProblem bp, long long 
       }
     }
     for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && sub == 0) bp.delta[dense ? r : packed_stat(p, r)] = acc;
+    const long long di = dense ? r : packed_stat(p, r);
+    if (live && sub == 0 && SDPA_CHECK(di < bp.acc_rows, p.status)) bp.delta[di] = acc;
   }
 }
 
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const BwdProblem bp, lo
   for (int u = blockIdx.y; u < units; u += gridDim.y) {
     const long long a_off = (static_cast<long long>(u) * chunks_per_unit + t) * 8;
     const long long q_off = p.strided ? dense_off(p, kTdq, u / p.H, u % p.H, i) + c : a_off;
+    if (!SDPA_CHECK(a_off + 8 <= bp.acc_rows * D && q_off + 8 <= p.ext[kTdq], p.status)) continue;
     const float4 a = *reinterpret_cast<const float4*>(bp.dq_acc + a_off);
     const float4 b = *reinterpret_cast<const float4*>(bp.dq_acc + a_off + 4);
     __align__(16) T out[8] = {from_f<T>(a.x * scale), from_f<T>(a.y * scale), from_f<T>(a.z * scale),

@@ -539,7 +539,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
     // bandwidth); with lane = head dim those would be scalar and slower.
     const int r = threadIdx.x & 127;                          // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float* dq_unit = bp.dq_acc + (PACKED ? row0 : static_cast<long long>(unit) * Lq * D);
+    const long long dq_base = PACKED ? row0 : static_cast<long long>(unit) * Lq * D;
+    float* dq_unit = bp.dq_acc + dq_base;
+    const long long dq_ext = bp.acc_rows * D;   // elements of the accumulator (debug bounds checks)
     const uint32_t sDQ = smem_u32(smem + C::kOffDQ);
     for (int s = 0; s < nsteps; ++s) {
       const int buf = 0;
@@ -565,11 +567,13 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
         if (r == 0) {
           const int rows = min(BQ, Lq - q0);
           if (!PACKED) {
-            bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0) * D, sDQ, static_cast<uint32_t>(rows * D * 4));
+            if (SDPA_CHECK(dq_base + static_cast<long long>(q0 + rows) * D <= dq_ext, p.status))
+              bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0) * D, sDQ, static_cast<uint32_t>(rows * D * 4));
           } else {
             // packed rows are H * D apart: one reduce per row
             for (int q = 0; q < rows; ++q)
-              bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0 + q) * rstride, sDQ + q * D * 4, D * 4);
+              if (SDPA_CHECK(dq_base + static_cast<long long>(q0 + q) * rstride + D <= dq_ext, p.status))
+                bulk_reduce_add_f32(dq_unit + static_cast<long long>(q0 + q) * rstride, sDQ + q * D * 4, D * 4);
           }
           bulk_commit();
         }
@@ -602,8 +606,9 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
             uint32_t w0, w1, w2, w3;
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(stg + (rr * 8 + (c ^ (rr & 7))) * 16) : "memory");
-            if (rbase + rr < Lq)
-              red_add_v4_f32(dq_unit + static_cast<long long>(rbase + rr) * rstride + cc * 32 + c * 4, w0, w1, w2, w3);
+            const long long qo = static_cast<long long>(rbase + rr) * rstride + cc * 32 + c * 4;
+            if (rbase + rr < Lq && SDPA_CHECK(dq_base + qo + 4 <= dq_ext, p.status))
+              red_add_v4_f32(dq_unit + qo, w0, w1, w2, w3);
           }
         }
       }
@@ -854,10 +859,11 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       tc_fence_after();
       const uint32_t col0 = half == 0 ? C::kTdV : C::kTdK;
       const float sc = half == 0 ? 1.f : p.scale;
-      T* out = static_cast<T*>(half == 0 ? bp.dv : bp.dk) +
-               (PACKED    ? row0k + static_cast<long long>(key) * rstride
-                : STRIDED ? dense_off(p, half == 0 ? kTdv : kTdk, unit / p.H, unit % p.H, key)
-                          : (static_cast<long long>(unit) * Lk + key) * D);
+      const long long out_off = PACKED    ? row0k + static_cast<long long>(key) * rstride
+                                : STRIDED ? dense_off(p, half == 0 ? kTdv : kTdk, unit / p.H, unit % p.H, key)
+                                          : (static_cast<long long>(unit) * Lk + key) * D;
+      T* out = static_cast<T*>(half == 0 ? bp.dv : bp.dk) + out_off;
+      const long long out_ext = p.ext[half == 0 ? kTdv : kTdk];   // debug bounds checks
       constexpr int kChunks = D / 8;                   // 16-byte chunks per row
       constexpr int kRowsPer = 32 / kChunks;           // rows per store instruction
       auto sw = [](int rr) { return kChunks >= 8 ? (rr & 7) : ((rr >> 1) & 3); };
@@ -889,11 +895,13 @@ bwd_tc_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, cons
       for (int i = 0; i < kChunks; ++i) {
         const int rr = i * kRowsPer + lane / kChunks;  // the row whose chunk c this lane stores
         const T* dst = reinterpret_cast<const T*>(__shfl_sync(0xffffffffu, base, rr));
+        const long long dst_off = __shfl_sync(0xffffffffu, out_off, rr);
         uint4 w;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(stage + (rr * kChunks + (c ^ sw(rr))) * 16)
                      : "memory");
-        if (key - lane + rr < Lk) *reinterpret_cast<uint4*>(const_cast<T*>(dst) + 8 * c) = w;
+        if (key - lane + rr < Lk && SDPA_CHECK(dst_off + 8 * c + 8 <= out_ext, p.status))
+          *reinterpret_cast<uint4*>(const_cast<T*>(dst) + 8 * c) = w;
       }
     }
   }

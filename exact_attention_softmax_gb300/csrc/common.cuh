@@ -10,10 +10,24 @@ namespace sdpa {
 
 constexpr unsigned kStatusTimeout = 1u;  // == SDPA_STATUS_TIMEOUT
 constexpr unsigned kStatusSeqlen = 2u;   // == SDPA_STATUS_SEQLEN
+constexpr unsigned kStatusBounds = 4u;   // == SDPA_STATUS_BOUNDS (debug build only)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per mbarrier wait
 
 // Debug switches (testing only; zero in normal use).
 constexpr int kDebugDropQArrive = 1;  // forward producer never loads Q: every wait times out
+constexpr int kDebugShortO = 2;       // debug build: O's extent one row short, so the
+                                      // last row's bounds check fails (its store is skipped)
+
+// Debug build (-DSDPA_DEBUG): device-side bounds checks on the kernels'
+// stores, reductions and shared-memory staging. A failed check sets
+// kStatusBounds in the status word and the guarded access is skipped: nothing
+// traps, and the host reports the bit. In the normal build a check is the
+// constant true and costs nothing.
+#ifdef SDPA_DEBUG
+#define SDPA_CHECK(cond, status) (::sdpa::bounds_ok((cond), (status)))
+#else
+#define SDPA_CHECK(cond, status) true
+#endif
 
 enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
@@ -61,12 +75,23 @@ struct Problem {
   // call, indexed by Tensor; the head dim is contiguous. (Packed batches are
   // [total, H, d] and ignore these.)
   long long st[kTensors][3];
+  // Elements each tensor spans from its base pointer (largest offset + 1),
+  // and rows of lse: what the debug build's bounds checks compare against.
+  long long ext[kTensors];
+  long long lse_ext;
   // 1 for a call on strided dense tensors (the *_strided entry points): its
   // tensor maps are 4-D {d, L, H, B}, boxes addressed (column, row, head,
   // batch), and it runs kernel variants of their own; 0 for contiguous
   // tensors, whose maps are 3-D {d, L, B*H} addressed (column, row, unit).
   int strided;
 };
+
+#ifdef SDPA_DEBUG
+__device__ __forceinline__ bool bounds_ok(bool ok, unsigned* status) {
+  if (!ok) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#endif
 
 // Element offset of row `row` of unit (b, h) in dense tensor `t`.
 __host__ __device__ __forceinline__ long long dense_off(const Problem& p, int t, long long b, long long h,
@@ -85,6 +110,7 @@ struct BwdProblem {
   void* dv;
   float* delta;       // [rows] fp32 workspace: rowsum(dO * O)
   float* dq_acc;      // [rows, d] fp32 workspace (tensor-core path only)
+  long long acc_rows; // rows of delta and dq_acc (debug bounds checks)
   int group;          // tensor-core kernel: units per scheduling group (set by its launcher)
 };
 

@@ -440,6 +440,11 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           for (int kv = 0; kv < 2; ++kv, ++fill) {
             const int slot = pr * C::kRing + fill % C::kRing;
             const int round = fill / C::kRing;
+            if (!SDPA_CHECK(slot >= 0 && slot < C::kSlots, p.status)) {
+              ok = false;
+              *abort_flag = 1u;
+              return;
+            }
             if (round > 0 && !(ok = mbar_wait(&bars->empty[slot], (round - 1) & 1, abort_flag, p.status))) return;
             mbar_expect_tx(&bars->full[slot], C::kTileBytes);
             const CUtensorMap* m = kv ? &tmV : &tmK;
@@ -705,8 +710,14 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
         constexpr int kChunks = D / 8;                     // 16-byte chunks per row
         constexpr int kRowsPer = 32 / kChunks;             // rows per store instruction
         auto slot = [](int r, int c) { return c ^ (kChunks == 8 ? (r & 7) : ((r >> 1) & 3)); };
+        // the staging Q buffer must be one of this tile's (else, in the debug
+        // build, the tile's first one: the status word already says the
+        // output is invalid)
+        const int qb = SDPA_CHECK(!C::kStageQ || (e.qb >= t * C::kQBufs && e.qb < (t + 1) * C::kQBufs), p.status)
+                           ? e.qb
+                           : t * C::kQBufs;
         const uint32_t stage = C::kStageQ
-                                   ? smem_u32(smem + C::kOffQ + e.qb * C::kTileBytes + (warp & 3) * C::kStageWarpBytes)
+                                   ? smem_u32(smem + C::kOffQ + qb * C::kTileBytes + (warp & 3) * C::kStageWarpBytes)
                                    : smem_u32(smem + C::kOffStage + warp * C::kStageWarpBytes);
         if (C::kStageO) __syncwarp();                      // the previous epilogue's reads are done
 #pragma unroll
@@ -724,7 +735,8 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(stage + (r * kChunks + slot(r, c)) * 16)
                        : "memory");
-          if (orow >= 0) *reinterpret_cast<uint4*>(static_cast<T*>(p.o) + orow + 8 * c) = w;
+          if (orow >= 0 && SDPA_CHECK(orow + 8 * c + 8 <= p.ext[kTo], p.status))
+            *reinterpret_cast<uint4*>(static_cast<T*>(p.o) + orow + 8 * c) = w;
         }
         if constexpr (C::kStageQ) {
           // the staged rows have been read out: the producer may load the next
@@ -732,10 +744,11 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
           // generic accesses)
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->q_empty[e.qb]);
+          if (lane == 0) mbar_arrive(&bars->q_empty[qb]);
         }
-        if (e.orow >= 0) p.lse[e.li] = e.l > 0.f ? (e.m + __log2f(e.l)) * kLn2 : -INFINITY;
-      } else if (e.orow >= 0) {
+        if (e.orow >= 0 && SDPA_CHECK(e.li < p.lse_ext, p.status))
+          p.lse[e.li] = e.l > 0.f ? (e.m + __log2f(e.l)) * kLn2 : -INFINITY;
+      } else if (e.orow >= 0 && SDPA_CHECK(e.orow + D <= p.ext[kTo] && e.li < p.lse_ext, p.status)) {
         T* orow = static_cast<T*>(p.o) + e.orow;
 #pragma unroll
         for (int x = 0; x < D / 8; ++x)
@@ -776,8 +789,9 @@ fwd_tc_kernel(const Problem p, const __grid_constant__ CUtensorMap tmQ,
       if (nt == 0) {
         // block-sparse: a tile whose mask row keeps nothing has no visible key:
         // O = 0, LSE = -inf
-        if (SPARSE && row < it.len_q) {
-          T* orow = static_cast<T*>(p.o) + (static_cast<long long>(it.unit) * it.len_q + row) * D;
+        const long long ro = (static_cast<long long>(it.unit) * it.len_q + row) * D;
+        if (SPARSE && row < it.len_q && SDPA_CHECK(ro + D <= p.ext[kTo] && ro / D < p.lse_ext, p.status)) {
+          T* orow = static_cast<T*>(p.o) + ro;
 #pragma unroll
           for (int x = 0; x < D / 8; ++x) *reinterpret_cast<uint4*>(orow + 8 * x) = make_uint4(0u, 0u, 0u, 0u);
           p.lse[static_cast<long long>(it.unit) * it.len_q + row] = -INFINITY;

@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(kRows) fwd_f32_kernel(Problem p) {
     }
   }
   if (!live) return;
-  float* O = static_cast<float*>(p.o) + row_off(p, u, kTo, row);
+  const long long oo = row_off(p, u, kTo, row);
+  if (!SDPA_CHECK(oo + d <= p.ext[kTo] && u.stat + row < p.lse_ext, p.status)) return;
+  float* O = static_cast<float*>(p.o) + oo;
   // a row with no visible key (block-sparse only) gets O = 0 and LSE = -inf
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -205,7 +207,9 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
     }
   }
   if (!live) return;
-  float* dQ = static_cast<float*>(bp.dq) + row_off(p, u, kTdq, row);
+  const long long qo = row_off(p, u, kTdq, row);
+  if (!SDPA_CHECK(qo + d <= p.ext[kTdq], p.status)) return;
+  float* dQ = static_cast<float*>(bp.dq) + qo;
 #pragma unroll
   for (int c = 0; c < DMAX; ++c)
     if (c < d) dQ[c] = dq[c] * p.scale;
@@ -279,8 +283,10 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
     }
   }
   if (!live) return;
-  float* dK = static_cast<float*>(bp.dk) + row_off(p, u, kTdk, key);
-  float* dV = static_cast<float*>(bp.dv) + row_off(p, u, kTdv, key);
+  const long long ko = row_off(p, u, kTdk, key), vo = row_off(p, u, kTdv, key);
+  if (!SDPA_CHECK(ko + d <= p.ext[kTdk] && vo + d <= p.ext[kTdv], p.status)) return;
+  float* dK = static_cast<float*>(bp.dk) + ko;
+  float* dV = static_cast<float*>(bp.dv) + vo;
 #pragma unroll
   for (int c = 0; c < DMAX; ++c) {
     if (c < d) {

@@ -64,13 +64,16 @@ typedef enum {
   SDPA_ERR_UNSUPPORTED = -2, /* head dim / dtype / mode this build does not implement */
   SDPA_ERR_CUDA = -3,        /* a CUDA runtime call failed (message names it) */
   SDPA_ERR_TIMEOUT = -4,     /* a kernel's bounded wait gave up (from sdpa_device_status) */
-  SDPA_ERR_WORKSPACE = -5    /* workspace NULL or smaller than sdpa_bwd_workspace_size() */
+  SDPA_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than sdpa_bwd_workspace_size() */
+  SDPA_ERR_BOUNDS = -6       /* debug build: a device-side bounds check failed (from sdpa_device_status) */
 } sdpa_status;
 
 /* Bits of the device status word (see sdpa_device_status). */
 #define SDPA_STATUS_TIMEOUT 1u   /* an mbarrier wait exceeded its time limit; outputs invalid */
 #define SDPA_STATUS_SEQLEN 2u    /* a packed sequence is longer than its bound (max_seqlen), or has
                                     queries but no keys; its outputs are left unwritten */
+#define SDPA_STATUS_BOUNDS 4u    /* debug build only: a device-side bounds check failed and the
+                                    access it guarded was skipped; outputs invalid */
 
 /*
  * Forward: O and LSE.
@@ -318,7 +321,8 @@ int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
 /*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device. Returns SDPA_OK, SDPA_ERR_TIMEOUT (bit SDPA_STATUS_TIMEOUT
- * was set), SDPA_ERR_ARG (bit SDPA_STATUS_SEQLEN was set) or SDPA_ERR_CUDA.
+ * was set), SDPA_ERR_BOUNDS (bit SDPA_STATUS_BOUNDS, debug build), SDPA_ERR_ARG
+ * (bit SDPA_STATUS_SEQLEN was set) or SDPA_ERR_CUDA.
  * If `bits` is not NULL the raw word is stored there.
  */
 int sdpa_device_status(void* stream, unsigned* bits);
@@ -342,9 +346,20 @@ int sdpa_trace_events(int which, void* begin_event, void* end_event);
  * Testing aid: sets debug flags for later calls on any thread and returns the
  * previous value. Flag 1 makes the forward tensor-core kernel skip its Q load,
  * so every wait in it runs out and sdpa_device_status() reports
- * SDPA_ERR_TIMEOUT after about a second. 0 (the default) is normal operation.
+ * SDPA_ERR_TIMEOUT after about a second. Flag 2 (debug build only) makes the
+ * forward's bounds checks take O as one row shorter than it is, so the store
+ * of its last row is refused and skipped and sdpa_device_status() reports
+ * SDPA_ERR_BOUNDS. 0 (the default) is normal operation.
  */
 int sdpa_debug_set(int flags);
+
+/*
+ * 1 for the debug build (compiled with SDPA_DEBUG: device-side bounds checks
+ * on the kernels' stores, reductions and shared-memory staging; a failed
+ * check skips the access and sets SDPA_STATUS_BOUNDS, nothing traps), 0 for
+ * the normal build, whose kernels carry no checks.
+ */
+int sdpa_debug_build(void);
 
 /*
  * Message for the last nonzero return on the calling thread ("" if none).
