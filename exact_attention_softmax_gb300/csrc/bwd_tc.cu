@@ -10,23 +10,25 @@
 //   P^T  = exp(scale S^T - LSE_i)                              (CUDA cores -> TMEM)
 //   dS^T = P^T * (dP^T - D_i)                                  (CUDA cores -> SMEM)
 //   dV  += P^T dO_i  (A from TMEM);  dK += dS^T Q_i            (tcgen05, TMEM)
-//   dQ_i partial = dS K   (d = 64: M = query rows)
+//   dQ_i partial = dS K   (d <= 64: M = query rows)
 //             or  (K^T dS^T)^T (d = 128: M = head dims)       (tcgen05, TMEM)
 //
 // and the dQ partial is added into an fp32 accumulator in global memory (one
 // bulk shared->global reduce per tile at d = 128, vector reductions of whole
-// row segments at d = 64). dK = scale * dK_acc and dV are written at the end;
-// dQ = scale * dQ_acc is rounded by a separate kernel.
+// row segments at d <= 64). dK = scale * dK_acc and dV are written at the
+// end; dQ = scale * dQ_acc is rounded by a separate kernel.
 //
 // Warps: 0-3 and 4-7 build P^T / dS^T for the first and second half of the
 // tile's queries (then write dV and dK); 8-11 drain dQ; 12 loads with TMA;
-// 13 issues S^T and dP^T; 14 issues dV, dK and dQ; 15 loads the additive
-// mask (masked kernels; it idles otherwise). The softmax
-// groups release S^T / dP^T as soon as they hold them in registers, so the
-// next tile's S^T, dP^T run under their arithmetic. P^T goes to TMEM, where
-// the dV MMA reads it, so only dS^T passes through shared memory (whose
-// bandwidth the MMAs' operand reads also use); the one dQ buffer is drained
-// well within a step.
+// 13 issues S^T and dP^T (and dQ at d <= 64); 14 issues dV and dK (and dQ at
+// d = 128); 15 loads the additive mask (masked kernels; it idles otherwise).
+// The softmax groups release S^T / dP^T as soon as they hold them in
+// registers, so the next tile's S^T, dP^T run under their arithmetic. P^T
+// goes to TMEM, where the dV MMA reads it, so only dS^T passes through shared
+// memory (whose bandwidth the MMAs' operand reads also use); the one dQ
+// buffer is drained well within a step. At d = 128 two handoffs inside a step
+// are split: S^T and dP^T commit separately, so P is formed while the dP^T
+// MMAs run, and P^T reaches the dV MMA before dS is formed.
 #include <type_traits>
 
 #include <algorithm>

@@ -25,7 +25,10 @@
 // dynamic queue: Q is double-buffered, the next item's first S_t is issued
 // while the current item's last block is still in its softmax, and the
 // current item's epilogue is deferred into the next item's first block, so
-// consecutive items overlap instead of draining the pipeline.
+// consecutive items overlap instead of draining the pipeline. The d <= 64
+// block-sparse kernel splits each CTA into two such pipelines, one per tile
+// slot (warp 11 is the second producer), each claiming single 128-row tiles
+// and streaming only the key blocks its tile's mask row keeps.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0, O_1 (d each) and P_0, P_1
 // (64 columns each) after them; at d = 128 P_t overlays the upper half of S_t.
 #include <atomic>
