@@ -140,13 +140,38 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- helpers
+def _code_only(text):
+    """C/C++ source with comments and blank space removed (string literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':                                   # string literal, escapes included
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(name):
-    """Short hash of a kernel's source (its .cu plus the shared device headers)."""
+    """Short hash of a kernel's code (its .cu plus the shared device headers,
+    comments and blank space left out, so an edit of a comment keeps the
+    counters taken on that code)."""
     csrc = os.path.join(ROOT, "exact_attention_softmax_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted([name, "ptx.cuh", "common.cuh"]):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
