@@ -169,7 +169,8 @@ def kernel_source_hash(name):
     counters taken on that code)."""
     csrc = os.path.join(ROOT, "exact_attention_softmax_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted([name, "ptx.cuh", "common.cuh"]):
+    deps = [name, "ptx.cuh", "common.cuh"] + (["bwd_common.cuh"] if name.startswith("bwd") else [])
+    for f in sorted(deps):
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -702,7 +703,9 @@ def run_ours(args):
     # per score element at the rate the probe measured.
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clk_mhz = clk.get("sm_max_mhz") or 2070
-    kinfo = {"fwd": ("fwd_tc_kernel", "fwd_tc.cu", fwd_f), "bwd": ("bwd_tc_kernel", "bwd_tc.cu", bwd_f)}
+    # (the d <= 64 backward of the plain workloads runs the persistent kernel)
+    bwd_k = ("bwd_persist_kernel", "bwd_persist.cu") if w.d <= 64 else ("bwd_tc_kernel", "bwd_tc.cu")
+    kinfo = {"fwd": ("fwd_tc_kernel", "fwd_tc.cu", fwd_f), "bwd": (bwd_k[0], bwd_k[1], bwd_f)}
     kernels = {}
     for key, ms in main_ms.items():
         name, src, f = kinfo[key]
