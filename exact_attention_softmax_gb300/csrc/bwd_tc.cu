@@ -797,8 +797,11 @@ cudaError_t launch_d(const BwdProblem& bp, const BwdMaps& m, cudaStream_t s) {
     return bp.f.causal ? launch_one<D, T, true, false, 2>(bp, m, s) : launch_one<D, T, false, false, 2>(bp, m, s);
   if (bp.f.dropout)
     return bp.f.causal ? launch_one<D, T, true, false, 3>(bp, m, s) : launch_one<D, T, false, false, 3>(bp, m, s);
-  // d <= 64 without mask or dropout: persistent CTAs (bwd_persist.cu)
-  if constexpr (D <= 64) return launch_bwd_persist<D, T>(bp, m, s);
+  // d <= 64 dense or strided, without mask or dropout: persistent CTAs
+  // (bwd_persist.cu). Packed batches stay here: their units are short (a few
+  // query steps per key block) and one CTA per key block measured faster.
+  if constexpr (D <= 64)
+    if (bp.f.cu_seqlens == nullptr) return launch_bwd_persist<D, T>(bp, m, s);
   if (bp.f.strided)
     return bp.f.causal ? launch_one<D, T, true, false, 4>(bp, m, s) : launch_one<D, T, false, false, 4>(bp, m, s);
   if (bp.f.cu_seqlens != nullptr)

@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(kRows) bwd_dq_f32_kernel(BwdProblem bp) {
   const Problem& p = bp.f;
   const int b = blockIdx.z, h = blockIdx.y;
   const Unit u = unit_of(p, b, h);
+  if (u.bad) {   // lengths outside their bounds: reported, nothing written
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusSeqlen);
+    return;
+  }
   const int row0 = blockIdx.x * kRows;
   if (row0 >= u.len_q) return;
   const int row = row0 + threadIdx.x;
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(kRows) bwd_dkdv_f32_kernel(BwdProblem bp) {
   const Problem& p = bp.f;
   const int b = blockIdx.z, h = blockIdx.y;
   const Unit u = unit_of(p, b, h);
+  if (u.bad) return;   // reported by the dQ kernel
   const int key0 = blockIdx.x * kRows;
   if (key0 >= u.len_k) return;
   const int key = key0 + threadIdx.x;

@@ -107,12 +107,14 @@ def test_cross_with_shared_offsets_matches_self_attention_call():
 @pytest.mark.parametrize("dtype", ["f16", "f32"])
 def test_cross_lengths_outside_bounds_are_reported(dtype):
     """A key length above max_seqlen_k, or queries with no keys, set the
-    SEQLEN status bit; the other sequences are still computed."""
-    from _gpu import cuda
+    SEQLEN status bit in the forward and in the backward; the other sequences
+    are still computed."""
+    from _gpu import GRAD_RTOL, cuda, rel_fro
+    from oracle import attn_bwd_unit
     dev = cuda()
     for lq, lk, mk in (([64, 40], [64, 300], 256), ([64, 40], [64, 0], 64)):
-        x = wl.varlen_cross_inputs(lq, lk, 1, 64, dtype, "normal", seed=26, with_do=False)
-        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        x = wl.varlen_cross_inputs(lq, lk, 1, 64, dtype, "normal", seed=26, with_do=True)
+        q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
         cq, ck = x["cu_seqlens_q"].to(dev), x["cu_seqlens_k"].to(dev)
         o, lse = ops.sdpa_fwd_varlen(q, k, v, cq, ck, max(lq), mk, is_causal=False)
         with pytest.raises(ops.SdpaError) as e:
@@ -124,3 +126,12 @@ def test_cross_lengths_outside_bounds_are_reported(dtype):
                                x["v"][:64, 0].double().numpy(), 0.125)
         tol = 4e-3 if dtype == "f16" else 1e-5
         assert np.max(np.abs(o[:64, 0].double().cpu().numpy() - ref)) < tol
+        grads = ops.sdpa_bwd_varlen(q, k, v, o, lse, do, cq, ck, max(lq), mk, is_causal=False)
+        with pytest.raises(ops.SdpaError) as e:
+            ops.sdpa_device_status()
+        assert e.value.code == -1
+        assert ops.sdpa_device_status() == 0
+        rg = attn_bwd_unit(*(x[n][:64, 0].double().numpy() for n in ("q", "k", "v", "do")), 0.125)
+        for name, g, r in zip(("dQ", "dK", "dV"), grads, rg):
+            err = rel_fro(g[:64, 0].double().cpu().numpy(), r)
+            assert err <= GRAD_RTOL[dtype], f"{name} {err:.3e}"
