@@ -73,6 +73,37 @@ def test_module_layout_fwd_bwd_against_oracle(dtype, d, causal):
         assert e <= GRAD_RTOL[dtype], f"{name} {e:.3e}"
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_module_layout_many_items(causal):
+    """More work items than SMs on strided views: 2 x 40 heads x 3 query items
+    (256, 256 and 88 rows) in the forward and x 5 key blocks in the
+    backward, whose d = 64 kernels are persistent, so each CTA carries its
+    state from one item to the next. Every (batch, head) unit is compared with
+    the fp64 oracle."""
+    from _gpu import FWD_ATOL, GRAD_RTOL, LSE_ATOL, f64, rel_fro
+    from oracle import attn_bwd_ref, attn_fwd_ref
+    B, L, H, d = 2, 600, 40, 64
+    q, k, v, do = _module_views(B, L, H, d, "f16", seed=84)
+    y, o, dqkv, dq, dk, dv = _out_views(B, L, H, d, q)
+    scale = d ** -0.5
+    _, lse = ops.sdpa_fwd(q, k, v, o, scale=scale, is_causal=causal)
+    ops.sdpa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale=scale, is_causal=causal)
+    assert ops.sdpa_device_status() == 0
+    assert not torch.isnan(y).any() and not torch.isnan(dqkv).any()
+    qn, kn, vn, don = (f64(t) for t in (q, k, v, do))
+    ro, rl = attn_fwd_ref(qn, kn, vn, scale, causal)
+    rg = attn_bwd_ref(qn, kn, vn, don, scale, causal)
+    got_o, got_l = f64(o), f64(lse)
+    got_g = [f64(t) for t in (dq, dk, dv)]
+    for b in range(B):
+        for h in range(H):
+            assert np.max(np.abs(got_o[b, h] - ro[b, h])) <= FWD_ATOL["f16"], (b, h)
+            assert np.max(np.abs(got_l[b, h] - rl[b, h])) <= LSE_ATOL["f16"], (b, h)
+            for name, g, r in zip(("dQ", "dK", "dV"), got_g, rg):
+                e = rel_fro(g[b, h], r[b, h])
+                assert e <= GRAD_RTOL["f16"], (name, b, h, e)
+
+
 @pytest.mark.parametrize("dtype,d", [("f16", 64), ("bf16", 128), ("f16", 32)])
 def test_strided_equals_contiguous_bit_for_bit(dtype, d):
     """The strided calls run the same arithmetic as the contiguous ones."""
