@@ -80,6 +80,32 @@ struct __align__(8) PBars {
 };
 static_assert(sizeof(PBars) <= kPBarBytes, "the barrier block's shared memory");
 
+// Packed fp32x2 arithmetic (one instruction for two lanes of values):
+// (a0, a1) * (c, c) + (b0, b1), (a0, a1) - (b0, b1) and (a0, a1) * (b0, b1).
+__device__ __forceinline__ uint64_t pack_f32x2(float a0, float a1) {
+  uint64_t x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  return x;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t x, float& a0, float& a1) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(x));
+}
+__device__ __forceinline__ void fma2v(float& o0, float& o1, float a0, float a1, float c, float b0, float b1) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pack_f32x2(a0, a1)), "l"(pack_f32x2(c, c)), "l"(pack_f32x2(b0, b1)));
+  unpack_f32x2(r, o0, o1);
+}
+__device__ __forceinline__ void sub2(float& o0, float& o1, float a0, float a1, float b0, float b1) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pack_f32x2(a0, a1)), "l"(pack_f32x2(b0, b1)));
+  unpack_f32x2(r, o0, o1);
+}
+__device__ __forceinline__ void mul2(float& o0, float& o1, float a0, float a1, float b0, float b1) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pack_f32x2(a0, a1)), "l"(pack_f32x2(b0, b1)));
+  unpack_f32x2(r, o0, o1);
+}
+
 template <int D, typename T, bool CAUSAL, bool PACKED, int EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_persist_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -570,12 +596,18 @@ bwd_persist_kernel(const BwdProblem bp, const __grid_constant__ CUtensorMap tmQ,
                        : "=f"(d4[0]), "=f"(d4[1]), "=f"(d4[2]), "=f"(d4[3]) : "r"(smem_u32(slf + BQ + 4 * gq)));
           float pr[4], ds[4];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
+          for (int h = 0; h < 4; h += 2) {
+            // two columns per packed fp32x2 instruction
             const int col = 4 * gq + h;
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), c, 0.f - l4[h]));
-            if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) pv = 0.f;
-            pr[h] = pv;
-            ds[h] = pv * (__uint_as_float(dv[col]) - d4[h]);
+            float e0, e1, t0, t1;
+            fma2v(e0, e1, __uint_as_float(sv[col]), __uint_as_float(sv[col + 1]), c, -l4[h], -l4[h + 1]);
+            float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+            if (M && ((CAUSAL && q0 + col < key) || key >= Lk)) p0 = 0.f;
+            if (M && ((CAUSAL && q0 + col + 1 < key) || key >= Lk)) p1 = 0.f;
+            sub2(t0, t1, __uint_as_float(dv[col]), __uint_as_float(dv[col + 1]), d4[h], d4[h + 1]);
+            mul2(ds[h], ds[h + 1], p0, p1, t0, t1);
+            pr[h] = p0;
+            pr[h + 1] = p1;
           }
           pk[2 * gq] = Pack2<T>::pack(pr[0], pr[1]);
           pk[2 * gq + 1] = Pack2<T>::pack(pr[2], pr[3]);
