@@ -703,8 +703,9 @@ def run_ours(args):
     # per score element at the rate the probe measured.
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clk_mhz = clk.get("sm_max_mhz") or 2070
-    # (the d <= 64 backward of the plain workloads runs the persistent kernel)
-    bwd_k = ("bwd_persist_kernel", "bwd_persist.cu") if w.d <= 64 else ("bwd_tc_kernel", "bwd_tc.cu")
+    # (the d <= 64 backward of dense batches runs the persistent kernel,
+    # packed batches and d = 128 the one-CTA-per-key-block kernel)
+    bwd_k = ("bwd_persist_kernel", "bwd_persist.cu") if w.d <= 64 and not w.varlen else ("bwd_tc_kernel", "bwd_tc.cu")
     kinfo = {"fwd": ("fwd_tc_kernel", "fwd_tc.cu", fwd_f), "bwd": (bwd_k[0], bwd_k[1], bwd_f)}
     kernels = {}
     for key, ms in main_ms.items():
